@@ -1,0 +1,209 @@
+"""Seeded synthetic inputs for the deformable-aggregation operator.
+
+This module holds workload tables and random draws only. None of the
+operator's arithmetic (coordinate transform, bilinear weights, sums,
+gradients) lives here. The CUDA path's tests and bench, and the CPU oracle's
+tests, all draw their inputs from this one module. That way both sides see the
+same bytes.
+
+Layouts follow the Sparse4D deformable_aggregation op. The page "Inside
+Sparse4D's CUDA core: deformable_aggregation bilinear interpolation and
+gradient back-propagation" fixes the HWC layout (§3.1) and the flattened
+multi-camera, multi-scale feature tensor built by feature_maps_format (§6):
+
+* ``mc_ms_feat``        [B, K*NPIX, C]   one row per pixel; camera-major,
+                                        then scale, then row-major pixels
+* ``spatial_shape``     [K, S, 2] int32  (H, W) of map (k, s)
+* ``level_start_index`` [K, S]    int32  first row of map (k, s)
+* ``sampling_location`` [B, A, P, K, 2]  normalised (x, y); x pairs with W
+* ``weights``           [B, A, P, K, S, G]
+* ``grad_out``          [B, A, C]
+
+The five workloads mirror the shapes and value distributions the pages work
+with: a 16x16 toy; the 6-camera, 4-scale Sparse4D head at inference (B=1) and
+training (B=6) sizes; a larger-image bf16-feature variant; and DCNv4-style
+dense queries (one anchor per pixel of a 56x56 map, 3x3 grid plus noise,
+unnormalised weights, see the DCNv4 page, "Solving the problem: 1. remove
+softmax"). No dataset is involved: everything is drawn from a seeded
+``torch.Generator``.
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Dict, Optional, Tuple
+
+import numpy as np
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    batch: int
+    num_cams: int
+    shapes: Tuple[Tuple[int, int], ...]  # (H, W) per scale, shared by every camera
+    num_embeds: int
+    num_groups: int
+    num_anchors: int
+    num_pts: int
+    feat_dtype: str  # "f32" or "bf16"
+    loc_kind: str  # "uniform" or "dcnv4_grid"
+    loc_lo: float
+    loc_hi: float
+    weight_kind: str  # "uniform01", "softmax" or "normal"
+    weight_sigma: float
+    backward: bool
+    seed: int
+    offset_sigma_px: float = 0.0  # dcnv4_grid only
+
+    @property
+    def num_scales(self) -> int:
+        return len(self.shapes)
+
+    @property
+    def npix(self) -> int:
+        return sum(h * w for h, w in self.shapes)
+
+    @property
+    def num_feat_rows(self) -> int:
+        return self.num_cams * self.npix
+
+    @property
+    def depth(self) -> int:
+        return self.num_embeds // self.num_groups
+
+    @property
+    def num_samples(self) -> int:
+        """Bilinear samples per pass: one per (b, a, p, k, s, g), each a D-vector."""
+        return (self.batch * self.num_anchors * self.num_pts * self.num_cams
+                * self.num_scales * self.num_groups)
+
+    def replace(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+SP4D_SHAPES = ((64, 176), (32, 88), (16, 44), (8, 22))
+LARGE_SHAPES = ((80, 200), (40, 100), (20, 50), (10, 25))
+
+WORKLOADS: Dict[str, Workload] = {
+    "tiny": Workload("tiny", 1, 1, ((16, 16),), 32, 1, 16, 4, "f32",
+                     "uniform", -0.1, 1.1, "uniform01", 0.0, True, 0),
+    "sp4d_inf": Workload("sp4d_inf", 1, 6, SP4D_SHAPES, 256, 8, 900, 13, "f32",
+                         "uniform", 0.0, 1.0, "softmax", 0.0, False, 1),
+    "sp4d_train": Workload("sp4d_train", 6, 6, SP4D_SHAPES, 256, 8, 900, 13, "f32",
+                           "uniform", -0.05, 1.05, "softmax", 0.0, True, 2),
+    "large_bf16": Workload("large_bf16", 1, 6, LARGE_SHAPES, 256, 8, 1800, 13, "bf16",
+                           "uniform", 0.0, 1.0, "softmax", 0.0, True, 3),
+    "dcnv4": Workload("dcnv4", 8, 1, ((56, 56),), 64, 4, 56 * 56, 9, "f32",
+                      "dcnv4_grid", 0.0, 0.0, "normal", 0.5, True, 4, offset_sigma_px=1.5),
+}
+
+# The order in which the workloads are listed by the project's configuration.
+WORKLOAD_ORDER = ("tiny", "sp4d_inf", "sp4d_train", "large_bf16", "dcnv4")
+
+
+@dataclasses.dataclass
+class Inputs:
+    """One draw of every operator input, as CPU tensors."""
+    wl: Workload
+    feat: torch.Tensor  # [B, rows, C] float32 or bfloat16
+    spatial_shape: torch.Tensor  # [K, S, 2] int32
+    level_start_index: torch.Tensor  # [K, S] int32
+    loc: torch.Tensor  # [B, A, P, K, 2] float32
+    weights: torch.Tensor  # [B, A, P, K, S, G] float32
+    grad_out: Optional[torch.Tensor]  # [B, A, C] float32
+
+    def feat_numpy(self) -> np.ndarray:
+        """Feature bytes for a consumer without bf16 support: float32, or the
+        raw uint16 bit patterns of bf16 values."""
+        if self.feat.dtype == torch.bfloat16:
+            return self.feat.view(torch.int16).numpy().view(np.uint16)
+        return self.feat.numpy()
+
+
+def map_tables(num_cams: int, shapes) -> Tuple[torch.Tensor, torch.Tensor]:
+    """spatial_shape [K,S,2] and level_start_index [K,S] for maps packed
+    camera-major, then scale (the feature_maps_format packing)."""
+    k_n, s_n = num_cams, len(shapes)
+    ss = torch.zeros(k_n, s_n, 2, dtype=torch.int32)
+    ls = torch.zeros(k_n, s_n, dtype=torch.int32)
+    row = 0
+    for k in range(k_n):
+        for s, (h, w) in enumerate(shapes):
+            ss[k, s, 0] = h
+            ss[k, s, 1] = w
+            ls[k, s] = row
+            row += h * w
+    return ss, ls
+
+
+def _draw_loc(wl: Workload, g: torch.Generator) -> torch.Tensor:
+    B, A, P, K = wl.batch, wl.num_anchors, wl.num_pts, wl.num_cams
+    if wl.loc_kind == "uniform":
+        u = torch.rand(B, A, P, K, 2, generator=g, dtype=torch.float64)
+        return (wl.loc_lo + (wl.loc_hi - wl.loc_lo) * u).to(torch.float32)
+    if wl.loc_kind == "dcnv4_grid":
+        # One anchor per pixel (i, j) of the single map; point p sits on the
+        # 3x3 grid around it, plus a Gaussian offset in pixels.
+        assert K == 1 and wl.num_scales == 1 and P == 9
+        H, W = wl.shapes[0]
+        assert A == H * W
+        a = torch.arange(A)
+        i = (a // W).to(torch.float64).view(1, A, 1)
+        j = (a % W).to(torch.float64).view(1, A, 1)
+        p = torch.arange(P)
+        dy = (p // 3 - 1).to(torch.float64).view(1, 1, P)
+        dx = (p % 3 - 1).to(torch.float64).view(1, 1, P)
+        off = torch.randn(B, A, P, 2, generator=g, dtype=torch.float64) * wl.offset_sigma_px
+        x = (j + 0.5 + dx + off[..., 0]) / W
+        y = (i + 0.5 + dy + off[..., 1]) / H
+        return torch.stack([x, y], dim=-1).view(B, A, P, 1, 2).to(torch.float32).contiguous()
+    raise ValueError(wl.loc_kind)
+
+
+def _draw_weights(wl: Workload, g: torch.Generator) -> torch.Tensor:
+    B, A, P, K, S, G = (wl.batch, wl.num_anchors, wl.num_pts, wl.num_cams,
+                        wl.num_scales, wl.num_groups)
+    if wl.weight_kind == "uniform01":
+        return torch.rand(B, A, P, K, S, G, generator=g, dtype=torch.float32)
+    if wl.weight_kind == "normal":
+        return (torch.randn(B, A, P, K, S, G, generator=g, dtype=torch.float32)
+                * wl.weight_sigma)
+    if wl.weight_kind == "softmax":
+        # Logits N(0,1), normalised over (P, K, S) for every (b, a, g): the
+        # Sparse4D head's weight normalisation. The operator itself never
+        # normalises (the DCNv4 page removes softmax altogether).
+        z = torch.randn(B, A, P, K, S, G, generator=g, dtype=torch.float64)
+        z = z.permute(0, 1, 5, 2, 3, 4).reshape(B, A, G, P * K * S).softmax(-1)
+        z = z.reshape(B, A, G, P, K, S).permute(0, 1, 3, 4, 5, 2)
+        return z.to(torch.float32).contiguous()
+    raise ValueError(wl.weight_kind)
+
+
+def make_inputs(wl: Workload | str, seed: Optional[int] = None) -> Inputs:
+    """Draw every input of ``wl`` from ``torch.Generator().manual_seed(seed)``.
+
+    Draw order is fixed (feat, loc, weights, grad_out), so a workload's bytes
+    depend only on its fields and seed.
+    """
+    if isinstance(wl, str):
+        wl = WORKLOADS[wl]
+    g = torch.Generator().manual_seed(wl.seed if seed is None else seed)
+    B, C = wl.batch, wl.num_embeds
+    feat = torch.randn(B, wl.num_feat_rows, C, generator=g, dtype=torch.float32)
+    if wl.feat_dtype == "bf16":
+        feat = feat.to(torch.bfloat16)  # round to nearest even
+    ss, ls = map_tables(wl.num_cams, wl.shapes)
+    loc = _draw_loc(wl, g)
+    w = _draw_weights(wl, g)
+    grad_out = torch.randn(B, wl.num_anchors, C, generator=g, dtype=torch.float32)
+    return Inputs(wl, feat, ss, ls, loc, w, grad_out)
+
+
+def small_variant(name: str, batch: int = 1, num_anchors: int = 24) -> Workload:
+    """A cut-down copy of a named workload with the same maps, channels and
+    distributions but few anchors, for fast CPU/GPU parity runs."""
+    wl = WORKLOADS[name]
+    if wl.loc_kind == "dcnv4_grid":
+        return wl.replace(name=name + "_small", batch=batch)
+    return wl.replace(name=name + "_small", batch=batch, num_anchors=num_anchors)

@@ -1,0 +1,144 @@
+"""CPU oracle for the deformable-aggregation operator (test infrastructure).
+
+This package wraps ``da_oracle.c``, a plain single-threaded C implementation
+of what the operator computes, through ctypes. Only these may import it:
+
+* the tests;
+* ``__graft_entry__.smoke()``;
+* the CPU-baseline and reference legs of ``bench.py``.
+
+The product path (``deformable_view_feature_gb300``) never imports it.
+
+``da_oracle.c`` names the page passages each step follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "da_oracle.c")
+_LIB = os.path.join(_HERE, "_build", "libda_oracle.so")
+
+# -ffp-contract=off: the coordinate step must round twice (see da_oracle.c).
+CFLAGS = ["-O3", "-std=c11", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc into ``oracle/_build``; return the .so path."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    os.makedirs(os.path.dirname(_LIB), exist_ok=True)
+    tmp = _LIB + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+    os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        lib = ctypes.CDLL(build())
+        i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
+        lib.dao_forward.argtypes = [i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, i64, i64, vp]
+        lib.dao_forward.restype = i32
+        lib.dao_backward.argtypes = ([i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp, i64, i64,
+                                                  vp, vp, vp])
+        lib.dao_backward.restype = i32
+        lib.dao_bilinear.argtypes = [vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float]
+        lib.dao_bilinear.restype = ctypes.c_double
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _prep(feat, spatial_shape, level_start_index, loc, weights):
+    feat = np.ascontiguousarray(feat)
+    if feat.dtype == np.uint16:
+        bf16 = 1
+    elif feat.dtype == np.float32:
+        bf16 = 0
+    else:
+        raise TypeError("feat must be float32, or uint16 holding bf16 bits")
+    ss = np.ascontiguousarray(spatial_shape, dtype=np.int32)
+    ls = np.ascontiguousarray(level_start_index, dtype=np.int32)
+    loc = np.ascontiguousarray(loc, dtype=np.float32)
+    weights = np.ascontiguousarray(weights, dtype=np.float32)
+    B, rows, C = feat.shape
+    _, A, P, K, _ = loc.shape
+    S = ss.shape[1] if ss.ndim == 3 else 0
+    G = weights.shape[-1]
+    assert weights.shape == (B, A, P, K, S, G), weights.shape
+    assert ss.shape == (K, S, 2) and ls.shape == (K, S)
+    return feat, bf16, ss, ls, loc, weights, (B, K, S, C, G, A, P, rows)
+
+
+def forward(feat, spatial_shape, level_start_index, loc, weights,
+            ba_range: Optional[Tuple[int, int]] = None) -> np.ndarray:
+    """out [B, A, C] float32 (or [n, C] rows for ``ba_range=(begin, end)``
+    over flat anchor index b*A+a)."""
+    feat, bf16, ss, ls, loc, weights, dims = _prep(feat, spatial_shape, level_start_index,
+                                                   loc, weights)
+    B, K, S, C, G, A, P, rows = dims
+    lo, hi = (0, B * A) if ba_range is None else ba_range
+    out = np.empty((hi - lo, C), dtype=np.float32)
+    rc = _load().dao_forward(B, K, S, C, G, A, P, rows, _ptr(ss), _ptr(ls), _ptr(feat), bf16,
+                             _ptr(loc), _ptr(weights), lo, hi, _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle forward rejected its arguments (code {rc})")
+    return out.reshape(B, A, C) if ba_range is None else out
+
+
+def backward(feat, spatial_shape, level_start_index, loc, weights, grad_out,
+             ba_range: Optional[Tuple[int, int]] = None):
+    """(grad_feat [B, rows, C], grad_loc, grad_weight), all float32.
+
+    With ``ba_range``, grad_feat holds the selected anchors' contributions and
+    grad_loc / grad_weight hold the selected anchors' rows only.
+    """
+    feat, bf16, ss, ls, loc, weights, dims = _prep(feat, spatial_shape, level_start_index,
+                                                   loc, weights)
+    B, K, S, C, G, A, P, rows = dims
+    grad_out = np.ascontiguousarray(grad_out, dtype=np.float32)
+    assert grad_out.shape == (B, A, C)
+    lo, hi = (0, B * A) if ba_range is None else ba_range
+    gf = np.empty((B, rows, C), dtype=np.float32)
+    gl = np.empty((hi - lo, P, K, 2), dtype=np.float32)
+    gw = np.empty((hi - lo, P, K, S, G), dtype=np.float32)
+    rc = _load().dao_backward(B, K, S, C, G, A, P, rows, _ptr(ss), _ptr(ls), _ptr(feat), bf16,
+                              _ptr(loc), _ptr(weights), _ptr(grad_out), lo, hi,
+                              _ptr(gf), _ptr(gl), _ptr(gw))
+    if rc != 0:
+        raise ValueError(f"oracle backward rejected its arguments (code {rc})")
+    if ba_range is None:
+        gl = gl.reshape(B, A, P, K, 2)
+        gw = gw.reshape(B, A, P, K, S, G)
+    return gf, gl, gw
+
+
+def bilinear(fmap: np.ndarray, c: int, x: float, y: float) -> float:
+    """One bilinear sample of channel c of an HWC float32 map at normalised (x, y)."""
+    fmap = np.ascontiguousarray(fmap, dtype=np.float32)
+    H, W, C = fmap.shape
+    return _load().dao_bilinear(_ptr(fmap), H, W, C, c, float(x), float(y))
+
+
+def run_inputs(inp, backward_pass: bool = True, ba_range=None):
+    """Run the oracle on a ``da_inputs.Inputs`` draw; returns a dict of arrays."""
+    args = (inp.feat_numpy(), inp.spatial_shape.numpy(), inp.level_start_index.numpy(),
+            inp.loc.numpy(), inp.weights.numpy())
+    res = {"out": forward(*args, ba_range=ba_range)}
+    if backward_pass:
+        gf, gl, gw = backward(*args, inp.grad_out.numpy(), ba_range=ba_range)
+        res.update(grad_feat=gf, grad_loc=gl, grad_weight=gw)
+    return res

@@ -1,0 +1,267 @@
+/*
+ * CPU oracle for the Sparse4D deformable-aggregation operator.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this library. The CUDA path shares no code,
+ * header or table with it.
+ *
+ * The code is plain, single-threaded C11. It is slow and written to be easy
+ * to check by eye against the page "Inside Sparse4D's CUDA core:
+ * deformable_aggregation bilinear interpolation and gradient
+ * back-propagation" (深入Sparse4D的CUDA核心：图解deformable_aggregation算子的双线性插值与梯度回传):
+ *   - §3.1: HWC layout; the pixel (i, j) of a map starts at i*W*C + j*C;
+ *   - §3.2: bilinear interpolation: floor gives the four corners, lh/lw/hh/hw
+ *     give their weights, corners outside the map read 0, and the value is
+ *     w1*v1 + w2*v2 + w3*v3 + w4*v4;
+ *   - §4.1: the three gradients. top_grad = grad_output * weight is
+ *     scattered to the corners with the corner weights;
+ *     grad_w = lh*(v4-v3) + hh*(v2-v1) scaled by the width feeds
+ *     sampling_location[0]; grad_h = lw*(v4-v2) + hw*(v3-v1) scaled by the
+ *     height feeds sampling_location[1]; grad_weights += grad_output * val;
+ *   - §5.1: the sum runs over the six dimensions batch, pts, embeds,
+ *     anchors, cams and scales.
+ *
+ * Precision (the page's own listing declares h_im, lh, hh, lw, hw as float):
+ *   - the sampling coordinate h_im = y*H - 0.5 and the fractional weights
+ *     lh, hh, lw, hw are computed in fp32, with two roundings and no fused
+ *     multiply-add (build with -ffp-contract=off). They decide which integer
+ *     corners are read, so both implementations must take that decision in
+ *     the same precision;
+ *   - everything after that is accumulated in double and rounded to fp32 once,
+ *     at the end.
+ *
+ * Readings where the page is garbled or silent:
+ *   - §3.2 prints only part of the bounds test. Here a corner is read iff
+ *     0 <= row <= H-1 and 0 <= col <= W-1, with all four inequalities for
+ *     every corner; otherwise it reads 0;
+ *   - a sample whose h_im or w_im is not finite reads nothing and gets zero
+ *     gradients;
+ *   - every output is overwritten, never accumulated into.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define DAO_OK 0
+#define DAO_ERR_ARGS 1
+#define DAO_ERR_NOMEM 2
+
+/* The four corners of one bilinear sample, in the page's order:
+ * 1 = (h_low, w_low), 2 = (h_low, w_high), 3 = (h_high, w_low),
+ * 4 = (h_high, w_high). row[i] is the feature row, or -1 outside the map. */
+typedef struct {
+    int64_t row[4];
+    float lh, lw, hh, hw;
+} footprint;
+
+static void make_footprint(float x, float y, int32_t H, int32_t W, int64_t start,
+                           footprint *f)
+{
+    /* §3.2: the normalised location times the map size, shifted half a pixel. */
+    float yh = y * (float)H;
+    float h_im = yh - 0.5f;
+    float xw = x * (float)W;
+    float w_im = xw - 0.5f;
+    int i;
+    for (i = 0; i < 4; ++i) f->row[i] = -1;
+    f->lh = f->lw = f->hh = f->hw = 0.0f;
+    if (!isfinite(h_im) || !isfinite(w_im)) return;
+
+    float h_low = floorf(h_im);
+    float w_low = floorf(w_im);
+    f->lh = h_im - h_low;
+    f->lw = w_im - w_low;
+    f->hh = 1.0f - f->lh;
+    f->hw = 1.0f - f->lw;
+
+    double rows[4] = {h_low, h_low, (double)h_low + 1.0, (double)h_low + 1.0};
+    double cols[4] = {w_low, (double)w_low + 1.0, w_low, (double)w_low + 1.0};
+    for (i = 0; i < 4; ++i) {
+        if (rows[i] >= 0.0 && rows[i] <= (double)(H - 1) &&
+            cols[i] >= 0.0 && cols[i] <= (double)(W - 1)) {
+            f->row[i] = start + (int64_t)rows[i] * W + (int64_t)cols[i];
+        }
+    }
+}
+
+/* w1..w4 of §3.2, formed in double from the fp32 fractional weights. */
+static void corner_weights(const footprint *f, double cw[4])
+{
+    cw[0] = (double)f->hh * (double)f->hw;
+    cw[1] = (double)f->hh * (double)f->lw;
+    cw[2] = (double)f->lh * (double)f->hw;
+    cw[3] = (double)f->lh * (double)f->lw;
+}
+
+static double feat_value(const void *feat, int feat_bf16, int64_t index)
+{
+    if (feat_bf16) {
+        /* bf16 is the top half of an fp32 bit pattern: widening is exact. */
+        uint32_t bits = (uint32_t)((const uint16_t *)feat)[index] << 16;
+        float v;
+        memcpy(&v, &bits, sizeof v);
+        return (double)v;
+    }
+    return (double)((const float *)feat)[index];
+}
+
+static int check_dims(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
+                      const int32_t *shape, const int32_t *start)
+{
+    int k, s;
+    if (B < 0 || K < 0 || S < 0 || A < 0 || P < 0 || C <= 0 || G <= 0 || C % G) return 0;
+    if (rows < 0) return 0;
+    for (k = 0; k < K; ++k)
+        for (s = 0; s < S; ++s) {
+            int32_t H = shape[(k * S + s) * 2], W = shape[(k * S + s) * 2 + 1];
+            int64_t st = start[k * S + s];
+            if (H <= 0 || W <= 0 || st < 0 || st + (int64_t)H * W > rows) return 0;
+        }
+    return 1;
+}
+
+/*
+ * Forward (§3.2 and §5.1):
+ *   out[b,a,c] = sum over p,k,s of
+ *                weights[b,a,p,k,s,g(c)] * bilinear(map (b,k,s), loc[b,a,p,k], c),
+ * with g(c) = c / (C/G). Only anchors with flat index b*A+a in
+ * [ba_begin, ba_end) are computed; out holds their rows only, starting at
+ * ba_begin.
+ */
+int dao_forward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
+                const int32_t *shape, const int32_t *start,
+                const void *feat, int feat_bf16,
+                const float *loc, const float *weights,
+                int64_t ba_begin, int64_t ba_end, float *out)
+{
+    if (!check_dims(B, K, S, C, G, A, P, rows, shape, start)) return DAO_ERR_ARGS;
+    if (ba_begin < 0 || ba_end < ba_begin || ba_end > (int64_t)B * A) return DAO_ERR_ARGS;
+    const int D = C / G;
+    double *acc = (double *)malloc(sizeof(double) * (size_t)C);
+    double *val = (double *)malloc(sizeof(double) * (size_t)D);
+    if (!acc || !val) { free(acc); free(val); return DAO_ERR_NOMEM; }
+
+    int64_t ba;
+    for (ba = ba_begin; ba < ba_end; ++ba) {
+        const int64_t b = ba / A;
+        memset(acc, 0, sizeof(double) * (size_t)C);
+        int p, k, s, g, c, i;
+        for (p = 0; p < P; ++p)
+            for (k = 0; k < K; ++k) {
+                const float *xy = loc + ((ba * P + p) * K + k) * 2;
+                for (s = 0; s < S; ++s) {
+                    const int32_t H = shape[(k * S + s) * 2];
+                    const int32_t W = shape[(k * S + s) * 2 + 1];
+                    footprint f;
+                    double cw[4];
+                    make_footprint(xy[0], xy[1], H, W, start[k * S + s], &f);
+                    corner_weights(&f, cw);
+                    for (g = 0; g < G; ++g) {
+                        const double w = weights[(((ba * P + p) * K + k) * S + s) * G + g];
+                        for (c = 0; c < D; ++c) val[c] = 0.0;
+                        for (i = 0; i < 4; ++i) {
+                            if (f.row[i] < 0) continue;
+                            const int64_t base = (b * rows + f.row[i]) * C + (int64_t)g * D;
+                            for (c = 0; c < D; ++c)
+                                val[c] += cw[i] * feat_value(feat, feat_bf16, base + c);
+                        }
+                        for (c = 0; c < D; ++c) acc[g * D + c] += w * val[c];
+                    }
+                }
+            }
+        for (int c2 = 0; c2 < C; ++c2) out[(ba - ba_begin) * C + c2] = (float)acc[c2];
+    }
+    free(acc);
+    free(val);
+    return DAO_OK;
+}
+
+/*
+ * Backward (§4.1), for the anchors with flat index in [ba_begin, ba_end):
+ *   grad_feat   [B, rows, C]      : every element is written; it holds the
+ *                                   contributions of the selected anchors;
+ *   grad_loc    [ba_end-ba_begin, P, K, 2];
+ *   grad_weight [ba_end-ba_begin, P, K, S, G].
+ */
+int dao_backward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
+                 const int32_t *shape, const int32_t *start,
+                 const void *feat, int feat_bf16,
+                 const float *loc, const float *weights, const float *grad_out,
+                 int64_t ba_begin, int64_t ba_end,
+                 float *grad_feat, float *grad_loc, float *grad_weight)
+{
+    if (!check_dims(B, K, S, C, G, A, P, rows, shape, start)) return DAO_ERR_ARGS;
+    if (ba_begin < 0 || ba_end < ba_begin || ba_end > (int64_t)B * A) return DAO_ERR_ARGS;
+    const int D = C / G;
+    const int64_t nfeat = (int64_t)B * rows * C;
+    double *gf = (double *)calloc((size_t)(nfeat > 0 ? nfeat : 1), sizeof(double));
+    double *gl = (double *)calloc((size_t)(P * K * 2 > 0 ? P * K * 2 : 1), sizeof(double));
+    if (!gf || !gl) { free(gf); free(gl); return DAO_ERR_NOMEM; }
+
+    int64_t ba;
+    for (ba = ba_begin; ba < ba_end; ++ba) {
+        const int64_t b = ba / A;
+        const int64_t lba = ba - ba_begin;
+        memset(gl, 0, sizeof(double) * (size_t)(P * K * 2));
+        int p, k, s, g, c, i;
+        for (p = 0; p < P; ++p)
+            for (k = 0; k < K; ++k) {
+                const float *xy = loc + ((ba * P + p) * K + k) * 2;
+                for (s = 0; s < S; ++s) {
+                    const int32_t H = shape[(k * S + s) * 2];
+                    const int32_t W = shape[(k * S + s) * 2 + 1];
+                    footprint f;
+                    double cw[4];
+                    make_footprint(xy[0], xy[1], H, W, start[k * S + s], &f);
+                    corner_weights(&f, cw);
+                    const double lh = f.lh, lw = f.lw, hh = f.hh, hw = f.hw;
+                    for (g = 0; g < G; ++g) {
+                        const int64_t widx = (((ba * P + p) * K + k) * S + s) * G + g;
+                        const double w = weights[widx];
+                        double gw_sum = 0.0, gh_sum = 0.0, gweight = 0.0;
+                        for (c = 0; c < D; ++c) {
+                            const double go = grad_out[ba * C + (int64_t)g * D + c];
+                            const double top_grad = go * w;
+                            double v[4] = {0.0, 0.0, 0.0, 0.0};
+                            for (i = 0; i < 4; ++i) {
+                                if (f.row[i] < 0) continue;
+                                const int64_t idx = (b * rows + f.row[i]) * C + (int64_t)g * D + c;
+                                v[i] = feat_value(feat, feat_bf16, idx);
+                                gf[idx] += cw[i] * top_grad;
+                            }
+                            const double grad_w = lh * (v[3] - v[2]) + hh * (v[1] - v[0]);
+                            const double grad_h = lw * (v[3] - v[1]) + hw * (v[2] - v[0]);
+                            gw_sum += (double)W * grad_w * top_grad;
+                            gh_sum += (double)H * grad_h * top_grad;
+                            const double val = cw[0] * v[0] + cw[1] * v[1] + cw[2] * v[2] + cw[3] * v[3];
+                            gweight += go * val;
+                        }
+                        gl[(p * K + k) * 2 + 0] += gw_sum;
+                        gl[(p * K + k) * 2 + 1] += gh_sum;
+                        grad_weight[widx - ba_begin * (int64_t)P * K * S * G] = (float)gweight;
+                    }
+                }
+            }
+        for (i = 0; i < P * K * 2; ++i) grad_loc[lba * P * K * 2 + i] = (float)gl[i];
+    }
+    int64_t e;
+    for (e = 0; e < nfeat; ++e) grad_feat[e] = (float)gf[e];
+    free(gf);
+    free(gl);
+    return DAO_OK;
+}
+
+/* Bilinear value of one channel at one location, for pin tests. */
+double dao_bilinear(const float *map, int32_t H, int32_t W, int32_t C, int32_t c,
+                    float x, float y)
+{
+    footprint f;
+    double cw[4], v = 0.0;
+    int i;
+    make_footprint(x, y, H, W, 0, &f);
+    corner_weights(&f, cw);
+    for (i = 0; i < 4; ++i)
+        if (f.row[i] >= 0) v += cw[i] * (double)map[f.row[i] * C + c];
+    return v;
+}
