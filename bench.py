@@ -1,0 +1,389 @@
+"""Benchmark: fwd+bwd bilinear samples/s of the deformable-aggregation op.
+
+The default workload is the 6-camera, 4-scale Sparse4D training shape:
+  * B=6, maps 64x176, 32x88, 16x44, 8x22;
+  * C=256, G=8, 900 anchors, 13 points;
+  * fp32 features.
+One step is one pass of the whole path: da_forward, then da_backward (the
+grad_feat zero-fill plus the gradient kernel). Inputs are synthetic and seeded
+(da_inputs), and resident in HBM when the timed region starts. The feature
+tensor alone (551 MB) is larger than L2, so no L2 flush is done between
+steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line on rank 0. It holds:
+  * value: samples/s over all ranks;
+  * roofline: algorithmic bytes of the dominant call (da_backward) divided by
+    its CUDA-event time, against the measured HBM copy bandwidth;
+  * e2e: the same metric with host buffers and host<->device copies inside
+    the timed region;
+  * cpu_baseline: the CPU oracle timed on a bounded sample of anchors;
+  * clocks: nvidia-smi samples taken during the timed region.
+
+--impl reference times the CPU oracle (the only reference this project has)
+on the same workload, one bounded sample of anchors per step.
+
+With N > 1 (torchrun), each rank runs an independent replica of the workload
+on its own GPU: the op does not shard, so there is no collective on the data
+path ("scaling": "weak").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import da_inputs  # noqa: E402
+
+METRIC = "fwd+bwd bilinear samples/sec at 6-cam Sparse4D shape; GB/s vs HBM peak"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_bytes(*ts):
+    return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def algorithmic_bytes(inp: da_inputs.Inputs):
+    """Compulsory DRAM bytes per call: every tensor read or written once.
+    grad_feat counts twice in the backward (a zero-fill and a write-back)."""
+    feat, loc, w, go = inp.feat, inp.loc, inp.weights, inp.grad_out
+    out_b = go.numel() * 4
+    gf_b = feat.numel() * 4
+    fwd = tensor_bytes(feat, loc, w) + out_b
+    grad_loc_b, grad_w_b = loc.numel() * 4, w.numel() * 4
+    bwd = tensor_bytes(feat, loc, w, go) + 2 * gf_b + grad_loc_b + grad_w_b
+    return fwd, bwd
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling in the background; keeps samples by wall time."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1 + 0.05):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax = float(parts[3])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[6:10]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- dist
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- CPU oracle legs
+
+def oracle_sample(inp: da_inputs.Inputs, n_anchors: int, start: int = 0):
+    """Time the CPU oracle (fwd + bwd) on anchors [start, start+n) of the flat
+    b*A+a index. Returns (samples, seconds)."""
+    import oracle  # test infrastructure: only this leg and --impl reference use it
+    wl = inp.wl
+    args = (inp.feat_numpy(), inp.spatial_shape.numpy(), inp.level_start_index.numpy(),
+            inp.loc.numpy(), inp.weights.numpy())
+    rng = (start, start + n_anchors)
+    t0 = time.perf_counter()
+    oracle.forward(*args, ba_range=rng)
+    if wl.backward:
+        oracle.backward(*args, inp.grad_out.numpy(), ba_range=rng)
+    dt = time.perf_counter() - t0
+    per_anchor = wl.num_pts * wl.num_cams * wl.num_scales * wl.num_groups
+    return n_anchors * per_anchor, dt
+
+
+def cpu_baseline(inp, n_anchors: int):
+    samples, dt = oracle_sample(inp, n_anchors)
+    return {"value": samples / dt, "unit": "samples/s", "cores": 1, "kind": "oracle",
+            "sample": (f"single-threaded C oracle, fwd+bwd over anchors 0..{n_anchors - 1} "
+                       f"of {inp.wl.batch * inp.wl.num_anchors} ({samples} samples, {dt:.1f} s); "
+                       f"host has {os.cpu_count()} cores")}
+
+
+def run_reference(a, wl):
+    rank, world, _ = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), 0
+    if rank != 0:
+        return
+    inp = da_inputs.make_inputs(wl)
+    n = max(1, min(a.ref_anchors, wl.batch * wl.num_anchors))
+    nba = wl.batch * wl.num_anchors
+    for i in range(a.warmup):
+        oracle_sample(inp, n, (i * n) % max(1, nba - n + 1))
+    tot_s, tot_t = 0, 0.0
+    for i in range(a.steps):
+        s, dt = oracle_sample(inp, n, (i * n) % max(1, nba - n + 1))
+        tot_s += s
+        tot_t += dt
+    v = tot_s / tot_t
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "samples/s", "n_gpus": a.gpus,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * tot_t / a.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded da_inputs draw; no dataset)",
+        "config": config_of(wl, "CPU oracle; each step a bounded sample of "
+                                f"{n} anchors"),
+        "cpu_baseline": {"value": v, "unit": "samples/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{n} anchors (fwd+bwd) per step of the single-threaded C "
+                                   f"oracle; host has {os.cpu_count()} cores"},
+        "e2e": {"value": v, "unit": "samples/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl, l2):
+    return {"workload": f"{wl.name}: B{wl.batch} K{wl.num_cams} S{wl.num_scales} maps "
+                        + "/".join(f"{h}x{w}" for h, w in wl.shapes)
+                        + f" C{wl.num_embeds} G{wl.num_groups} A{wl.num_anchors} P{wl.num_pts} "
+                        + f"{wl.feat_dtype} features",
+            "samples_per_step": wl.num_samples, "passes": "fwd+bwd" if wl.backward else "fwd",
+            "l2": l2, "parallelism": "replicas (one independent workload per GPU)"}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(a, wl):
+    import deformable_view_feature_gb300 as da
+    da.load_library()
+    rank, world, local = dist_setup(a.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    inp = da_inputs.make_inputs(wl)
+    feat = inp.feat.to(dev)
+    loc = inp.loc.to(dev)
+    w = inp.weights.to(dev)
+    go = inp.grad_out.to(dev)
+    ss, ls = inp.spatial_shape, inp.level_start_index
+    out = torch.empty(go.shape, device=dev)
+    gf = torch.empty(feat.shape, device=dev)
+    gl = torch.empty(loc.shape, device=dev)
+    gw = torch.empty(w.shape, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    fwd_bytes, bwd_bytes = algorithmic_bytes(inp)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        da.da_forward(feat, ss, ls, loc, w, out=out, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if wl.backward:
+            da.da_backward(feat, ss, ls, loc, w, go, grad_feat=gf, grad_loc=gl, grad_weight=gw,
+                           stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+
+    clocks = ClockSampler(local if world > 1 else 0)
+    clocks.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(a.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    barrier(world)
+    time.sleep(0.1)
+    clocks.stop()
+    ms = start.elapsed_time(end)
+    ms_max = max_over_ranks(ms, world)
+    fwd_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(a.steps)]
+    bwd_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(a.steps)] if wl.backward else []
+
+    samples_total = wl.num_samples * a.steps * world
+    value = samples_total / (ms_max / 1e3)
+
+    # End to end through the public API: pinned host inputs, copies in the timed region.
+    h_in = [t.pin_memory() for t in (inp.feat, inp.loc, inp.weights, inp.grad_out)]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, gf, gl, gw)]
+    d_in = [feat, loc, w, go]
+    e2e_steps = max(1, min(a.steps, a.e2e_steps))
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for d, h in zip(d_in, h_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            for h, d in zip(h_out, (out, gf, gl, gw)):
+                h.copy_(d, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    barrier(world)
+    h2d = tensor_bytes(*h_in)
+    d2h = tensor_bytes(*h_out)
+    e2e = {"value": wl.num_samples * e2e_steps * world / (e2e_ms / 1e3), "unit": "samples/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    if wl.backward:
+        dom_ms, dom_bytes, dom = statistics.mean(bwd_ms), bwd_bytes, "da_backward"
+    else:
+        dom_ms, dom_bytes, dom = statistics.mean(fwd_ms), fwd_bytes, "da_forward"
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    step_ms = ms_max / a.steps
+    line = {
+        "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": step_ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32"
+        if wl.feat_dtype == "f32" else "bf16-features/f32",
+        "data": "synthetic (seeded da_inputs draw with the workload's shapes and distributions)",
+        "config": config_of(wl, "inputs larger than L2 (feature map "
+                                f"{inp.feat.numel() * inp.feat.element_size() / 1e6:.0f} MB), no flush"),
+        "gbs_step": (fwd_bytes + (bwd_bytes if wl.backward else 0)) / (step_ms / 1e3) / 1e9,
+        "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms) if bwd_ms else None,
+        "roofline": {"bound": "hbm", "kernel": dom + (" (grad_feat zero-fill + gradient kernel)"
+                                                       if dom == "da_backward" else ""),
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "algorithmic_bytes": dom_bytes, "traffic": None},
+        "e2e": e2e,
+        "gpu_launches": a.steps * (1 + (2 if wl.backward else 0)),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    if world == 1 and not a.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp, a.cpu_anchors)
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="sp4d_train", choices=list(da_inputs.WORKLOADS))
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-anchors", type=int, default=1800,
+                    help="anchors in the CPU-baseline sample")
+    ap.add_argument("--ref-anchors", type=int, default=300,
+                    help="anchors per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    wl = da_inputs.WORKLOADS[a.workload]
+    if a.impl == "reference":
+        run_reference(a, wl)
+    else:
+        run_ours(a, wl)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and a.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

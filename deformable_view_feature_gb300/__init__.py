@@ -1,0 +1,212 @@
+"""GB300 deformable aggregation: thin Python binding of libda.so.
+
+The functions here only marshal arguments. They check tensor shapes, pick the
+stream, allocate outputs with torch and call the C ABI (include/da.h). Every
+step of the operator runs in the library's CUDA kernels. There is no fallback:
+if libda.so has not been built, or the tensors are not on a CUDA device, the
+call raises.
+
+    out = da_forward(mc_ms_feat, spatial_shape, level_start_index,
+                     sampling_location, weights)
+    grad_feat, grad_loc, grad_weight = da_backward(
+        mc_ms_feat, spatial_shape, level_start_index, sampling_location,
+        weights, grad_out)
+
+``DeformableAggregationFunction`` wraps the two as a torch autograd function.
+It takes the inputs of the op of the same name on the page "Inside Sparse4D's
+CUDA core" (§6).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+from . import build as _build
+
+__all__ = ["da_forward", "da_backward", "DeformableAggregationFunction", "DaError",
+           "library_path", "load_library", "da_version"]
+
+DA_F32, DA_BF16 = 0, 1
+_STATUS = {0: "DA_OK", 1: "DA_ERR_NULL", 2: "DA_ERR_SHAPE", 3: "DA_ERR_ALIGN",
+           4: "DA_ERR_UNSUPPORTED", 5: "DA_ERR_CUDA"}
+
+
+class DaError(RuntimeError):
+    """A non-OK status from libda.so."""
+
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{_STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+class DaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("num_cams", ctypes.c_int32),
+                ("num_scales", ctypes.c_int32), ("num_embeds", ctypes.c_int32),
+                ("num_groups", ctypes.c_int32), ("num_anchors", ctypes.c_int32),
+                ("num_pts", ctypes.c_int32), ("feat_dtype", ctypes.c_int32),
+                ("num_feat_rows", ctypes.c_int64)]
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library():
+    """Load libda.so (it must already be built: ``deformable_view_feature_gb300.build``)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libda.so is not built ({path}); run "
+                           "`python -m deformable_view_feature_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp = ctypes.c_void_p
+    lib.da_forward.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp]
+    lib.da_forward.restype = ctypes.c_int
+    lib.da_backward.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.da_backward.restype = ctypes.c_int
+    lib.da_status_string.argtypes = [ctypes.c_int]
+    lib.da_status_string.restype = ctypes.c_char_p
+    lib.da_last_error.argtypes = []
+    lib.da_last_error.restype = ctypes.c_char_p
+    lib.da_version.argtypes = []
+    lib.da_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def da_version() -> int:
+    return load_library().da_version()
+
+
+def _check(status: int):
+    if status != 0:
+        raise DaError(status, load_library().da_last_error().decode(errors="replace"))
+
+
+def _host_i32(t) -> torch.Tensor:
+    """The small map tables travel as host int32 arrays (copied if on a device)."""
+    t = torch.as_tensor(t)
+    return t.detach().to(device="cpu", dtype=torch.int32).contiguous()
+
+
+def _dptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    if t is None or t.numel() == 0:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensors must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream or None
+
+
+def _dims(feat: torch.Tensor, ss: torch.Tensor, loc: torch.Tensor, weights: torch.Tensor) -> DaDims:
+    if feat.dim() != 3:
+        raise ValueError("mc_ms_feat must be [B, rows, C]")
+    B, rows, C = feat.shape
+    if loc.dim() != 5 or loc.shape[-1] != 2:
+        raise ValueError("sampling_location must be [B, A, P, K, 2]")
+    _, A, P, K, _ = loc.shape
+    if ss.dim() != 3 or ss.shape[0] != K or ss.shape[2] != 2:
+        raise ValueError("spatial_shape must be [K, S, 2]")
+    S = ss.shape[1]
+    if weights.dim() != 6 or tuple(weights.shape[:5]) != (B, A, P, K, S):
+        raise ValueError("weights must be [B, A, P, K, S, G]")
+    if loc.shape[0] != B:
+        raise ValueError("batch sizes differ")
+    G = weights.shape[5]
+    if feat.dtype == torch.float32:
+        dt = DA_F32
+    elif feat.dtype == torch.bfloat16:
+        dt = DA_BF16
+    else:
+        raise TypeError("mc_ms_feat must be float32 or bfloat16")
+    if loc.dtype != torch.float32 or weights.dtype != torch.float32:
+        raise TypeError("sampling_location and weights must be float32")
+    return DaDims(B, K, S, C, G, A, P, dt, rows)
+
+
+def da_forward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
+               sampling_location: torch.Tensor, weights: torch.Tensor,
+               out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """Forward pass on the current (or given) CUDA stream; returns out [B, A, C] fp32."""
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims(mc_ms_feat, ss, sampling_location, weights)
+    if out is None:
+        out = torch.empty(d.batch, d.num_anchors, d.num_embeds, device=mc_ms_feat.device,
+                          dtype=torch.float32)
+    elif out.shape != (d.batch, d.num_anchors, d.num_embeds) or out.dtype != torch.float32:
+        raise ValueError("out must be float32 [B, A, C]")
+    _check(lib.da_forward(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
+                          ls.data_ptr() if ls.numel() else None, _dptr(sampling_location),
+                          _dptr(weights), _dptr(out), _stream_handle(stream)))
+    return out
+
+
+def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
+                sampling_location: torch.Tensor, weights: torch.Tensor, grad_out: torch.Tensor,
+                grad_feat: Optional[torch.Tensor] = None, grad_loc: Optional[torch.Tensor] = None,
+                grad_weight: Optional[torch.Tensor] = None,
+                stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Backward pass; returns (grad_feat fp32, grad_loc, grad_weight)."""
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims(mc_ms_feat, ss, sampling_location, weights)
+    dev = mc_ms_feat.device
+    if tuple(grad_out.shape) != (d.batch, d.num_anchors, d.num_embeds) or grad_out.dtype != torch.float32:
+        raise ValueError("grad_out must be float32 [B, A, C]")
+    if grad_feat is None:
+        grad_feat = torch.empty(mc_ms_feat.shape, device=dev, dtype=torch.float32)
+    if grad_loc is None:
+        grad_loc = torch.empty(sampling_location.shape, device=dev, dtype=torch.float32)
+    if grad_weight is None:
+        grad_weight = torch.empty(weights.shape, device=dev, dtype=torch.float32)
+    for name, t, shape in (("grad_feat", grad_feat, mc_ms_feat.shape),
+                           ("grad_loc", grad_loc, sampling_location.shape),
+                           ("grad_weight", grad_weight, weights.shape)):
+        if t.shape != shape or t.dtype != torch.float32:
+            raise ValueError(f"{name} must be float32 {tuple(shape)}")
+    _check(lib.da_backward(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
+                           ls.data_ptr() if ls.numel() else None, _dptr(sampling_location),
+                           _dptr(weights), _dptr(grad_out), _dptr(grad_feat), _dptr(grad_loc),
+                           _dptr(grad_weight), _stream_handle(stream)))
+    return grad_feat, grad_loc, grad_weight
+
+
+class DeformableAggregationFunction(torch.autograd.Function):
+    """Autograd wrapper with the argument list of Sparse4D's op:
+    (mc_ms_feat, spatial_shape, scale_start_index, sampling_location, weights)."""
+
+    @staticmethod
+    def forward(ctx, mc_ms_feat, spatial_shape, scale_start_index, sampling_location, weights):
+        mc_ms_feat = mc_ms_feat.contiguous()
+        sampling_location = sampling_location.contiguous().float()
+        weights = weights.contiguous().float()
+        ss, ls = _host_i32(spatial_shape), _host_i32(scale_start_index)
+        ctx.save_for_backward(mc_ms_feat, sampling_location, weights)
+        ctx.tables = (ss, ls)
+        return da_forward(mc_ms_feat, ss, ls, sampling_location, weights)
+
+    @staticmethod
+    def backward(ctx, grad_output):
+        mc_ms_feat, sampling_location, weights = ctx.saved_tensors
+        ss, ls = ctx.tables
+        gf, gl, gw = da_backward(mc_ms_feat, ss, ls, sampling_location, weights,
+                                 grad_output.contiguous().float())
+        if mc_ms_feat.dtype != torch.float32:
+            gf = gf.to(mc_ms_feat.dtype)
+        return gf, None, None, gl, gw

@@ -1,0 +1,190 @@
+// extern "C" entry points of libda.so (declared in include/da.h): host-side
+// argument validation, then kernel launches on the caller's stream.
+//
+// The interface mirrors the autograd function DeformableAggregationFunction of
+// the page "Inside Sparse4D's CUDA core", §6:
+// (mc_ms_feat, spatial_shape, scale_start_index, sampling_location, weights).
+// Here the start index is called level_start_index, the two small map tables
+// are host arrays (so the host can check every map against the feature rows
+// without a device round trip), and the sizes travel in da_dims.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+
+#include "da_internal.cuh"
+
+namespace {
+
+thread_local char g_err[256] = "";
+
+da_status fail(da_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Checks shared by both passes; fills the kernel's Problem and the chunk count.
+da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_shape,
+                  const int32_t *level_start_index, const float *loc, const float *weights,
+                  da::Problem &pb, int &chunks)
+{
+    if (!dims) return fail(DA_ERR_NULL, "dims is NULL");
+    const da_dims d = *dims;
+    if (d.batch < 0 || d.num_cams < 0 || d.num_scales < 0 || d.num_anchors < 0 || d.num_pts < 0)
+        return fail(DA_ERR_SHAPE, "negative size in dims");
+    if (d.num_embeds < 1 || d.num_groups < 1 || d.num_embeds % d.num_groups != 0)
+        return fail(DA_ERR_SHAPE, "num_embeds (%d) must be a positive multiple of num_groups (%d)",
+                    d.num_embeds, d.num_groups);
+    if (d.feat_dtype != DA_F32 && d.feat_dtype != DA_BF16)
+        return fail(DA_ERR_SHAPE, "unknown feat_dtype %d", d.feat_dtype);
+    if (d.num_feat_rows < 0 || d.num_feat_rows > DA_MAX_ROWS)
+        return fail(DA_ERR_SHAPE, "num_feat_rows %lld outside [0, %d]",
+                    static_cast<long long>(d.num_feat_rows), DA_MAX_ROWS);
+    const int64_t nmaps = static_cast<int64_t>(d.num_cams) * d.num_scales;
+    if (nmaps > DA_MAX_MAPS)
+        return fail(DA_ERR_UNSUPPORTED, "num_cams*num_scales = %lld exceeds %d",
+                    static_cast<long long>(nmaps), DA_MAX_MAPS);
+    const int D = d.num_embeds / d.num_groups;
+    const int elem = d.feat_dtype == DA_BF16 ? 2 : 4;
+    const int row_bytes = D * elem;
+    if (row_bytes != 16 && row_bytes != 32 && row_bytes != 64 && row_bytes != 128)
+        return fail(DA_ERR_UNSUPPORTED, "group width D*elem = %d bytes; supported: 16, 32, 64, 128",
+                    row_bytes);
+    chunks = row_bytes / 16;
+
+    const int64_t num_ba = static_cast<int64_t>(d.batch) * d.num_anchors;
+    const int64_t pks = static_cast<int64_t>(d.num_pts) * nmaps;
+    if (num_ba > INT32_MAX || pks > INT32_MAX || static_cast<int64_t>(d.num_pts) * d.num_cams > INT32_MAX)
+        return fail(DA_ERR_UNSUPPORTED, "batch*anchors or pts*cams*scales exceeds int32");
+
+    if (nmaps > 0 && (!spatial_shape || !level_start_index))
+        return fail(DA_ERR_NULL, "spatial_shape / level_start_index is NULL");
+    for (int64_t i = 0; i < nmaps; ++i) {
+        const int32_t H = spatial_shape[2 * i], W = spatial_shape[2 * i + 1];
+        const int32_t st = level_start_index[i];
+        if (H < 1 || W < 1 || H > DA_MAX_MAP_SIDE || W > DA_MAX_MAP_SIDE)
+            return fail(DA_ERR_SHAPE, "map %lld has shape %d x %d", static_cast<long long>(i), H, W);
+        if (st < 0 || static_cast<int64_t>(st) + static_cast<int64_t>(H) * W > d.num_feat_rows)
+            return fail(DA_ERR_SHAPE, "map %lld (start %d, %d x %d) does not fit in %lld feature rows",
+                        static_cast<long long>(i), st, H, W, static_cast<long long>(d.num_feat_rows));
+        pb.maps[i] = da::MapInfo{H, W, st, 0};
+    }
+
+    const int64_t n_feat = static_cast<int64_t>(d.batch) * d.num_feat_rows * d.num_embeds;
+    const int64_t n_samp = num_ba * pks;
+    if (n_feat > 0 && !feat) return fail(DA_ERR_NULL, "mc_ms_feat is NULL");
+    if (n_samp > 0 && (!loc || !weights)) return fail(DA_ERR_NULL, "sampling_location / weights is NULL");
+    if (!aligned(feat, 16)) return fail(DA_ERR_ALIGN, "mc_ms_feat must be 16-byte aligned");
+    if (!aligned(loc, 8)) return fail(DA_ERR_ALIGN, "sampling_location must be 8-byte aligned");
+    if (!aligned(weights, 4)) return fail(DA_ERR_ALIGN, "weights must be 4-byte aligned");
+
+    pb.feat = feat;
+    pb.loc = loc;
+    pb.weights = weights;
+    pb.rows = d.num_feat_rows;
+    pb.B = d.batch;
+    pb.A = d.num_anchors;
+    pb.P = d.num_pts;
+    pb.K = d.num_cams;
+    pb.S = d.num_scales;
+    pb.C = d.num_embeds;
+    pb.G = d.num_groups;
+    pb.D = D;
+    pb.pks = static_cast<int32_t>(pks);
+    pb.pk = d.num_pts * d.num_cams;
+    pb.num_ba = static_cast<int32_t>(num_ba);
+    pb.anchors_per_cta = d.num_groups < da::kWarps ? da::kWarps / d.num_groups : 1;
+    return DA_OK;
+}
+
+da_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(DA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+}  // namespace
+
+extern "C" {
+
+da_status da_forward(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                     const int32_t *level_start_index, const float *sampling_location,
+                     const float *weights, float *out, da_stream_t stream)
+{
+    da::FwdArgs a{};
+    int chunks = 0;
+    da_status st = prepare(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location,
+                           weights, a.pb, chunks);
+    if (st != DA_OK) return st;
+    const int64_t n_out = static_cast<int64_t>(a.pb.num_ba) * a.pb.C;
+    if (n_out > 0 && !out) return fail(DA_ERR_NULL, "out is NULL");
+    if (!aligned(out, 16)) return fail(DA_ERR_ALIGN, "out must be 16-byte aligned");
+    a.out = out;
+    if (n_out == 0) return DA_OK;
+    const cudaError_t e = da::launch_forward(a, dims->feat_dtype, chunks, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return DA_OK;
+}
+
+da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                      const int32_t *level_start_index, const float *sampling_location,
+                      const float *weights, const float *grad_out, float *grad_feat, float *grad_loc,
+                      float *grad_weight, da_stream_t stream)
+{
+    da::BwdArgs a{};
+    int chunks = 0;
+    da_status st = prepare(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location,
+                           weights, a.pb, chunks);
+    if (st != DA_OK) return st;
+    const da::Problem &pb = a.pb;
+    const int64_t n_out = static_cast<int64_t>(pb.num_ba) * pb.C;
+    const int64_t n_gf = static_cast<int64_t>(pb.B) * pb.rows * pb.C;
+    const int64_t n_gl = static_cast<int64_t>(pb.num_ba) * pb.pk * 2;
+    const int64_t n_gw = static_cast<int64_t>(pb.num_ba) * pb.pks * pb.G;
+    if (n_out > 0 && !grad_out) return fail(DA_ERR_NULL, "grad_out is NULL");
+    if (n_gf > 0 && !grad_feat) return fail(DA_ERR_NULL, "grad_feat is NULL");
+    if (n_gl > 0 && !grad_loc) return fail(DA_ERR_NULL, "grad_loc is NULL");
+    if (n_gw > 0 && !grad_weight) return fail(DA_ERR_NULL, "grad_weight is NULL");
+    if (!aligned(grad_out, 16)) return fail(DA_ERR_ALIGN, "grad_out must be 16-byte aligned");
+    if (!aligned(grad_feat, 16)) return fail(DA_ERR_ALIGN, "grad_feat must be 16-byte aligned");
+    if (!aligned(grad_loc, 4)) return fail(DA_ERR_ALIGN, "grad_loc must be 4-byte aligned");
+    if (!aligned(grad_weight, 4)) return fail(DA_ERR_ALIGN, "grad_weight must be 4-byte aligned");
+    // The per-CTA grad_loc staging area must fit in shared memory.
+    const int64_t smem = static_cast<int64_t>(pb.anchors_per_cta) * pb.pk * 2 * 4;
+    if (smem > 200 * 1024)
+        return fail(DA_ERR_UNSUPPORTED, "pts*cams = %d too large for the grad_loc staging area", pb.pk);
+    a.grad_out = grad_out;
+    a.grad_feat = grad_feat;
+    a.grad_loc = grad_loc;
+    a.grad_weight = grad_weight;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = da::launch_zero_fill(grad_feat, n_gf, s);
+    if (e != cudaSuccess) return cuda_fail(e, "grad_feat zero-fill");
+    if (n_out == 0) return DA_OK;
+    e = da::launch_backward(a, dims->feat_dtype, chunks, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return DA_OK;
+}
+
+const char *da_status_string(da_status status)
+{
+    switch (status) {
+        case DA_OK: return "DA_OK";
+        case DA_ERR_NULL: return "DA_ERR_NULL";
+        case DA_ERR_SHAPE: return "DA_ERR_SHAPE";
+        case DA_ERR_ALIGN: return "DA_ERR_ALIGN";
+        case DA_ERR_UNSUPPORTED: return "DA_ERR_UNSUPPORTED";
+        case DA_ERR_CUDA: return "DA_ERR_CUDA";
+    }
+    return "DA_ERR_UNKNOWN";
+}
+
+const char *da_last_error(void) { return g_err; }
+
+int32_t da_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,165 @@
+// Internal declarations shared by the CUDA translation units of libda.so.
+// The public C ABI is include/da.h. Nothing here is exported.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "da.h"
+
+namespace da {
+
+constexpr int kWarps = 8;            // warps per CTA in the sampling kernels
+constexpr int kThreads = kWarps * 32;
+
+// One feature map (k, s): H x W pixels starting at feature row `start`.
+struct MapInfo {
+    int32_t H, W, start, pad;
+};
+
+// Everything a sampling kernel needs about the problem. It is passed by value
+// as a kernel parameter, so the map table lives in the constant bank.
+struct Problem {
+    const void *feat;
+    const float *loc;
+    const float *weights;
+    int64_t rows;             // feature rows per batch item
+    int32_t B, A, P, K, S, C, G, D;
+    int32_t pks;              // P*K*S samples per (b, a, g)
+    int32_t pk;               // P*K locations per (b, a)
+    int32_t num_ba;           // B*A
+    int32_t anchors_per_cta;  // anchors (all groups) owned by one CTA
+    MapInfo maps[DA_MAX_MAPS];
+};
+
+struct FwdArgs {
+    Problem pb;
+    float *out;
+};
+
+struct BwdArgs {
+    Problem pb;
+    const float *grad_out;
+    float *grad_feat;
+    float *grad_loc;
+    float *grad_weight;
+};
+
+// `chunks` = D * sizeof(feature) / 16, one of 1, 2, 4, 8.
+cudaError_t launch_forward(const FwdArgs &a, int feat_dtype, int chunks, cudaStream_t st);
+cudaError_t launch_backward(const BwdArgs &a, int feat_dtype, int chunks, cudaStream_t st);
+cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st);
+
+// Grid size that covers num_ba anchors, anchors_per_cta at a time.
+inline int64_t sampling_grid(const Problem &pb)
+{
+    return (static_cast<int64_t>(pb.num_ba) + pb.anchors_per_cta - 1) / pb.anchors_per_cta;
+}
+
+// ------------------------------------------------------------------ device helpers
+
+// Bilinear footprint of one sample. The steps are those of the page "Inside
+// Sparse4D's CUDA core", §3.2:
+//   h_im = y*H - 0.5 and w_im = x*W - 0.5, each rounded twice (a product,
+//   then a difference; no fused multiply-add), because floor() of them picks
+//   the integer corners;
+//   corners 1..4 = (h_low, w_low), (h_low, w_low+1), (h_low+1, w_low),
+//   (h_low+1, w_low+1) with weights hh*hw, hh*lw, lh*hw, lh*lw;
+//   a corner is read only if 0 <= row <= H-1 and 0 <= col <= W-1.
+// row[i] is the feature row of corner i within its batch item, or -1 when the
+// corner is outside the map. A sample whose coordinates are not finite has
+// no corners and zero weights.
+struct Footprint {
+    int32_t row[4];
+    float cw[4];
+    float lh, lw, hh, hw;
+};
+
+__device__ __forceinline__ void footprint(float x, float y, const MapInfo &m, Footprint &f)
+{
+    const float h_im = __fsub_rn(__fmul_rn(y, static_cast<float>(m.H)), 0.5f);
+    const float w_im = __fsub_rn(__fmul_rn(x, static_cast<float>(m.W)), 0.5f);
+    if (!(isfinite(h_im) && isfinite(w_im))) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f.row[i] = -1;
+            f.cw[i] = 0.f;
+        }
+        f.lh = f.lw = f.hh = f.hw = 0.f;
+        return;
+    }
+    const float hl = floorf(h_im);
+    const float wl = floorf(w_im);
+    f.lh = h_im - hl;
+    f.lw = w_im - wl;
+    f.hh = 1.f - f.lh;
+    f.hw = 1.f - f.lw;
+    // Clamp before converting: any h_low outside [-2, H] has both rows outside
+    // the map, and so does its clamped value.
+    const int ih = static_cast<int>(fminf(fmaxf(hl, -2.f), static_cast<float>(m.H)));
+    const int iw = static_cast<int>(fminf(fmaxf(wl, -2.f), static_cast<float>(m.W)));
+    const bool r0 = ih >= 0 && ih < m.H;
+    const bool r1 = ih >= -1 && ih < m.H - 1;
+    const bool c0 = iw >= 0 && iw < m.W;
+    const bool c1 = iw >= -1 && iw < m.W - 1;
+    const int base = m.start + ih * m.W + iw;
+    f.row[0] = (r0 && c0) ? base : -1;
+    f.row[1] = (r0 && c1) ? base + 1 : -1;
+    f.row[2] = (r1 && c0) ? base + m.W : -1;
+    f.row[3] = (r1 && c1) ? base + m.W + 1 : -1;
+    f.cw[0] = f.hh * f.hw;
+    f.cw[1] = f.hh * f.lw;
+    f.cw[2] = f.lh * f.hw;
+    f.cw[3] = f.lh * f.lw;
+}
+
+// 16-byte read-only load of one chunk of a feature row.
+__device__ __forceinline__ uint4 ldg16(const void *p)
+{
+    return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// The 16 bytes as floats: 4 fp32 values, or 8 bf16 values widened exactly.
+template <typename T>
+struct Chunk;
+
+template <>
+struct Chunk<float> {
+    static constexpr int kVec = 4;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float (&v)[4])
+    {
+        v[0] = __uint_as_float(r.x);
+        v[1] = __uint_as_float(r.y);
+        v[2] = __uint_as_float(r.z);
+        v[3] = __uint_as_float(r.w);
+    }
+};
+
+struct Bf16Tag {};
+
+template <>
+struct Chunk<Bf16Tag> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float (&v)[8])
+    {
+        v[0] = __uint_as_float(r.x << 16);
+        v[1] = __uint_as_float(r.x & 0xffff0000u);
+        v[2] = __uint_as_float(r.y << 16);
+        v[3] = __uint_as_float(r.y & 0xffff0000u);
+        v[4] = __uint_as_float(r.z << 16);
+        v[5] = __uint_as_float(r.z & 0xffff0000u);
+        v[6] = __uint_as_float(r.w << 16);
+        v[7] = __uint_as_float(r.w & 0xffff0000u);
+    }
+};
+
+// Vector reduction of four floats into global memory (sm_90+).
+__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
+{
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                 :
+                 : "l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "memory");
+}
+
+}  // namespace da

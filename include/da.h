@@ -1,0 +1,162 @@
+/*
+ * da.h: C ABI of the GB300 deformable-aggregation library (libda.so).
+ *
+ * The operator is Sparse4D's deformable aggregation. The page "Inside
+ * Sparse4D's CUDA core: deformable_aggregation bilinear interpolation and
+ * gradient back-propagation" (深入Sparse4D的CUDA核心：图解deformable_aggregation算子的双线性插值与梯度回传)
+ * defines it:
+ *   - §3.1: HWC feature layout;
+ *   - §3.2: bilinear sampling with per-corner zeroing outside the map;
+ *   - §4.1: the three gradients;
+ *   - §5.1: the six-dimensional decomposition;
+ *   - §6: the inputs of DeformableAggregationFunction and the packing done
+ *     by feature_maps_format.
+ *
+ * Notation: B batch, K cameras, S scales, C channels (num_embeds),
+ * G groups, D = C / G channels per group, A anchors, P points per anchor.
+ * Map (k, s) has H x W pixels and starts at feature row level_start_index[k, s].
+ *
+ *   out[b,a,c] = sum_{p,k,s} weights[b,a,p,k,s,c/D] *
+ *                bilinear(map (b,k,s), h = y*H - 0.5, w = x*W - 0.5, channel c)
+ *
+ * with (x, y) = sampling_location[b,a,p,k,0..1]; x is scaled by the width and
+ * y by the height. A corner outside the map reads 0. No softmax or other
+ * normalisation is applied to the weights: the DCNv4 page ("Solving the
+ * problem: 1. remove softmax") treats them as unbounded reals.
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers marked "device" point to memory the calling CUDA context can
+ *     read or write from kernels. Pointers marked "host" point to ordinary
+ *     host memory, read during the call only.
+ *   - The caller owns every buffer; the library allocates nothing.
+ *   - Work is enqueued on `stream`, or on the legacy default stream when it is
+ *     NULL. The call returns without synchronising. Outputs are valid once the
+ *     stream reaches that point.
+ *   - Outputs are overwritten, never accumulated into.
+ *   - Sizes may be 0 (B, A, P, K or S). An empty sum leaves zeros in the
+ *     outputs. A pointer may be NULL only when its tensor has no elements.
+ *   - Arguments are validated on the host before anything is enqueued. On any
+ *     error nothing is enqueued and a non-zero da_status is returned;
+ *     da_last_error() gives a one-line reason. The only exception is
+ *     DA_ERR_CUDA, which a failed launch can return after part of the work was
+ *     enqueued.
+ *   - The library keeps no state between calls. Calls on different streams
+ *     may run concurrently, provided they write to different buffers.
+ */
+#ifndef DA_H_
+#define DA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here without the CUDA headers. */
+typedef struct CUstream_st *da_stream_t;
+
+typedef enum da_status {
+    DA_OK = 0,
+    DA_ERR_NULL = 1,        /* a required pointer is NULL */
+    DA_ERR_SHAPE = 2,       /* sizes negative, inconsistent, or a map outside the feature rows */
+    DA_ERR_ALIGN = 3,       /* a pointer is not aligned as required below */
+    DA_ERR_UNSUPPORTED = 4, /* valid sizes this build has no kernel for (see da_forward) */
+    DA_ERR_CUDA = 5         /* a CUDA launch or runtime call failed */
+} da_status;
+
+typedef enum da_dtype {
+    DA_F32 = 0,  /* IEEE binary32 features */
+    DA_BF16 = 1  /* bfloat16 features; all arithmetic and every other tensor stay fp32 */
+} da_dtype;
+
+typedef struct da_dims {
+    int32_t batch;        /* B >= 0 */
+    int32_t num_cams;     /* K >= 0 */
+    int32_t num_scales;   /* S >= 0; K*S <= DA_MAX_MAPS */
+    int32_t num_embeds;   /* C >= 1 */
+    int32_t num_groups;   /* G >= 1, C % G == 0 */
+    int32_t num_anchors;  /* A >= 0 */
+    int32_t num_pts;      /* P >= 0 */
+    int32_t feat_dtype;   /* a da_dtype */
+    int64_t num_feat_rows;/* feature rows per batch item, 0 <= rows <= DA_MAX_ROWS */
+} da_dims;
+
+#define DA_MAX_MAPS 64              /* largest K*S */
+#define DA_MAX_MAP_SIDE (1 << 24)   /* largest H or W */
+#define DA_MAX_ROWS (1 << 30)       /* largest num_feat_rows; row indices stay in int32 */
+
+/*
+ * Forward pass: the sampling and weighting of page §3.2, summed over the
+ * dimensions of page §5.1.
+ *
+ *   mc_ms_feat        device [B, num_feat_rows, C], feat_dtype, 16-byte aligned.
+ *                     Row level_start_index[k,s] + i*W + j holds pixel (i, j)
+ *                     of map (k, s) (HWC, page §3.1).
+ *   spatial_shape     host   [K, S, 2] int32: (H, W) of each map, 1..DA_MAX_MAP_SIDE.
+ *   level_start_index host   [K, S] int32: first row of each map. The map must
+ *                     fit: start + H*W <= num_feat_rows. Maps may overlap.
+ *   sampling_location device [B, A, P, K, 2] fp32, (x, y) normalised to the
+ *                     image, 8-byte aligned. The same (x, y) serves every scale.
+ *   weights           device [B, A, P, K, S, G] fp32, 4-byte aligned.
+ *   out               device [B, A, C] fp32, 16-byte aligned; overwritten.
+ *
+ * Supported: D * sizeof(feature) in {16, 32, 64, 128} bytes. That is D in
+ * {4, 8, 16, 32} for fp32 and D in {8, 16, 32, 64} for bf16. Other D return
+ * DA_ERR_UNSUPPORTED.
+ * Arithmetic: h = y*H - 0.5 and w = x*W - 0.5 are each rounded twice (a
+ * product, then a difference; no fused multiply-add). Corner weights and sums
+ * are fp32.
+ */
+da_status da_forward(const da_dims *dims,
+                     const void *mc_ms_feat,
+                     const int32_t *spatial_shape,
+                     const int32_t *level_start_index,
+                     const float *sampling_location,
+                     const float *weights,
+                     float *out,
+                     da_stream_t stream);
+
+/*
+ * Backward pass: the three gradients of page §4.1, for a loss L with
+ * dL/d out = grad_out.
+ *
+ *   inputs as for da_forward, plus
+ *   grad_out    device [B, A, C] fp32, 16-byte aligned.
+ *   grad_feat   device [B, num_feat_rows, C] fp32 for both feature types,
+ *               16-byte aligned; overwritten. Rows outside every map get 0.
+ *               The scatter-add order is unspecified, so the bits may differ
+ *               from run to run.
+ *   grad_loc    device [B, A, P, K, 2] fp32, 4-byte aligned; overwritten.
+ *               [...,0] is dL/dx (scaled by W), [...,1] is dL/dy (scaled by H).
+ *   grad_weight device [B, A, P, K, S, G] fp32, 4-byte aligned; overwritten.
+ *
+ * The call zero-fills grad_feat and then scatters into it. grad_loc and
+ * grad_weight are written exactly once per element.
+ */
+da_status da_backward(const da_dims *dims,
+                      const void *mc_ms_feat,
+                      const int32_t *spatial_shape,
+                      const int32_t *level_start_index,
+                      const float *sampling_location,
+                      const float *weights,
+                      const float *grad_out,
+                      float *grad_feat,
+                      float *grad_loc,
+                      float *grad_weight,
+                      da_stream_t stream);
+
+/* Static name of a status code. */
+const char *da_status_string(da_status status);
+
+/* One-line reason for the last non-OK status returned on this thread. The
+ * pointer stays valid until the next call on this thread. */
+const char *da_last_error(void);
+
+/* ABI version: major * 10000 + minor * 100 + patch. */
+int32_t da_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DA_H_ */

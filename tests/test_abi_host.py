@@ -1,0 +1,158 @@
+"""Host-side checks of the C ABI; no GPU is needed and nothing is launched.
+
+* libda.so builds (nvcc cross-compiles) and loads.
+* It exports every function that include/da.h declares.
+* Argument validation returns the documented status codes.
+Every call here fails validation, or has nothing to do, before any CUDA call.
+Fake device addresses are safe for that reason: they are never dereferenced.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import deformable_view_feature_gb300 as da
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "da.h")
+
+DA_OK, DA_ERR_NULL, DA_ERR_SHAPE, DA_ERR_ALIGN, DA_ERR_UNSUPPORTED = 0, 1, 2, 3, 4
+FAKE = 0x7F0000000000  # 256-byte aligned stand-in for a device address
+
+
+@pytest.fixture(scope="module")
+def lib():
+    da.build.build()
+    return da.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(da_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function(lib):
+    names = _declared_functions()
+    assert {"da_forward", "da_backward", "da_status_string", "da_last_error", "da_version"} <= set(names)
+    out = subprocess.run(["nm", "-D", "--defined-only", da.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\bT (da_\w+)", out))
+    missing = [n for n in names if n not in exported]
+    assert not missing, f"declared in da.h but not exported: {missing}"
+    for n in names:
+        getattr(lib, n)  # resolvable through ctypes
+
+
+def test_header_compiles_as_plain_c(tmp_path):
+    src = tmp_path / "use.c"
+    src.write_text('#include "da.h"\nint main(void){ da_dims d = {0}; (void)d; return (int)DA_OK; }\n')
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-c",
+                    str(src), "-o", str(tmp_path / "use.o")], check=True)
+
+
+def test_status_strings_and_version(lib):
+    assert lib.da_status_string(0) == b"DA_OK"
+    assert lib.da_status_string(4) == b"DA_ERR_UNSUPPORTED"
+    assert lib.da_version() >= 100
+
+
+def _dims(**kw):
+    d = dict(batch=1, num_cams=1, num_scales=1, num_embeds=32, num_groups=1, num_anchors=4,
+             num_pts=2, feat_dtype=0, num_feat_rows=16)
+    d.update(kw)
+    return da.DaDims(**d)
+
+
+def _tables(H=4, W=4, start=0):
+    ss = (ctypes.c_int32 * 2)(H, W)
+    ls = (ctypes.c_int32 * 1)(start)
+    return ss, ls
+
+
+def _fwd(lib, dims, ss=None, ls=None, feat=FAKE, loc=FAKE, w=FAKE, out=FAKE):
+    if ss is None:
+        ss, ls = _tables()
+    return lib.da_forward(ctypes.byref(dims) if dims is not None else None, feat, ss, ls, loc, w,
+                          out, None)
+
+
+def _bwd(lib, dims, feat=FAKE, loc=FAKE, w=FAKE, go=FAKE, gf=FAKE, gl=FAKE, gw=FAKE):
+    ss, ls = _tables()
+    return lib.da_backward(ctypes.byref(dims), feat, ss, ls, loc, w, go, gf, gl, gw, None)
+
+
+def test_null_dims(lib):
+    assert _fwd(lib, None) == DA_ERR_NULL
+
+
+@pytest.mark.parametrize("kw", [dict(batch=-1), dict(num_groups=3), dict(num_embeds=0),
+                                dict(feat_dtype=7), dict(num_feat_rows=-5),
+                                dict(num_feat_rows=(1 << 30) + 1)])
+def test_bad_sizes(lib, kw):
+    assert _fwd(lib, _dims(**kw)) == DA_ERR_SHAPE
+    assert b"" != lib.da_last_error()
+
+
+def test_map_must_fit_rows(lib):
+    ss, ls = _tables(H=4, W=5)  # 20 rows > 16
+    assert _fwd(lib, _dims(), ss, ls) == DA_ERR_SHAPE
+    ss, ls = _tables(H=0, W=5)
+    assert _fwd(lib, _dims(), ss, ls) == DA_ERR_SHAPE
+    ss, ls = _tables(start=-1)
+    assert _fwd(lib, _dims(), ss, ls) == DA_ERR_SHAPE
+
+
+@pytest.mark.parametrize("C,G,dt", [(12, 1, 0), (64, 1, 0), (8, 2, 1), (256, 2, 1), (40, 2, 0)])
+def test_unsupported_group_width(lib, C, G, dt):
+    assert _fwd(lib, _dims(num_embeds=C, num_groups=G, feat_dtype=dt)) == DA_ERR_UNSUPPORTED
+    assert b"group width" in lib.da_last_error()
+
+
+def test_too_many_maps(lib):
+    ss = (ctypes.c_int32 * (2 * 65))(*([1, 1] * 65))
+    ls = (ctypes.c_int32 * 65)(*range(65))
+    d = _dims(num_cams=65, num_feat_rows=65)
+    assert _fwd(lib, d, ss, ls) == DA_ERR_UNSUPPORTED
+
+
+def test_null_pointers(lib):
+    assert _fwd(lib, _dims(), feat=None) == DA_ERR_NULL
+    assert _fwd(lib, _dims(), loc=None) == DA_ERR_NULL
+    assert _fwd(lib, _dims(), out=None) == DA_ERR_NULL
+    assert _bwd(lib, _dims(), go=None) == DA_ERR_NULL
+    assert _bwd(lib, _dims(), gf=None) == DA_ERR_NULL
+    assert _bwd(lib, _dims(), gl=None) == DA_ERR_NULL
+    assert _bwd(lib, _dims(), gw=None) == DA_ERR_NULL
+    ss, ls = _tables()
+    assert lib.da_forward(ctypes.byref(_dims()), FAKE, None, ls, FAKE, FAKE, FAKE, None) == DA_ERR_NULL
+
+
+def test_misaligned_pointers(lib):
+    assert _fwd(lib, _dims(), feat=FAKE + 4) == DA_ERR_ALIGN
+    assert _fwd(lib, _dims(), loc=FAKE + 4) == DA_ERR_ALIGN
+    assert _fwd(lib, _dims(), w=FAKE + 2) == DA_ERR_ALIGN
+    assert _fwd(lib, _dims(), out=FAKE + 8) == DA_ERR_ALIGN
+    assert _bwd(lib, _dims(), go=FAKE + 8) == DA_ERR_ALIGN
+    assert _bwd(lib, _dims(), gf=FAKE + 8) == DA_ERR_ALIGN
+    assert _bwd(lib, _dims(), gl=FAKE + 2) == DA_ERR_ALIGN
+    assert _bwd(lib, _dims(), gw=FAKE + 1) == DA_ERR_ALIGN
+
+
+def test_empty_problem_needs_no_pointers(lib):
+    """With B = 0 every tensor is empty: NULL pointers are fine and nothing is
+    enqueued (no CUDA call is made, so this passes without a GPU)."""
+    d = _dims(batch=0)
+    assert _fwd(lib, d, feat=None, loc=None, w=None, out=None) == DA_OK
+    assert _bwd(lib, d, feat=None, loc=None, w=None, go=None, gf=None, gl=None, gw=None) == DA_OK
+
+
+def test_binding_rejects_host_tensors():
+    import torch
+    feat = torch.zeros(1, 16, 32)
+    loc = torch.zeros(1, 4, 2, 1, 2)
+    w = torch.zeros(1, 4, 2, 1, 1, 1)
+    with pytest.raises((ValueError, RuntimeError)):
+        da.da_forward(feat, [[[4, 4]]], [[0]], loc, w, out=torch.zeros(1, 4, 32))

@@ -1,0 +1,206 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+All five workloads run at full size, and every output element is compared
+with the oracle on the same seeded inputs. The launch configuration is the
+one the bench times. Smaller cases cover:
+  * every supported group width (D*elem = 16/32/64/128 bytes, fp32 and bf16);
+  * ragged sample counts and anchor counts that are not a multiple of a CTA's
+    share;
+  * 1x1 maps, wide location ranges, empty inputs and non-finite locations;
+  * output guard bands, the autograd wrapper and a non-default stream.
+"""
+import numpy as np
+import pytest
+import torch
+
+import da_inputs
+import oracle
+from parity_util import TOL, assert_close, max_rel, to_np, violations
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def da():
+    import deformable_view_feature_gb300 as m
+    m.build.build()
+    m.load_library()
+    assert torch.cuda.is_available(), "the parity tests need a CUDA GPU"
+    return m
+
+
+def _run_gpu(da, inp, backward=True, stream=None):
+    dev = torch.device("cuda")
+    feat = inp.feat.to(dev)
+    loc = inp.loc.to(dev)
+    w = inp.weights.to(dev)
+    out = da.da_forward(feat, inp.spatial_shape, inp.level_start_index, loc, w, stream=stream)
+    res = {"out": out}
+    if backward:
+        go = inp.grad_out.to(dev)
+        gf, gl, gw = da.da_backward(feat, inp.spatial_shape, inp.level_start_index, loc, w, go,
+                                    stream=stream)
+        res.update(grad_feat=gf, grad_loc=gl, grad_weight=gw)
+    torch.cuda.synchronize()
+    return {k: to_np(v) for k, v in res.items()}
+
+
+def _compare(inp, got, ref):
+    kind = inp.wl.feat_dtype
+    msgs = []
+    for name in ref:
+        rtol, atol = TOL[kind][name]
+        n, msg = violations(got[name], ref[name], rtol, atol, name)
+        if n:
+            msgs.append(msg)
+    assert not msgs, f"{inp.wl.name}: " + " | ".join(msgs)
+
+
+@pytest.mark.parametrize("name", da_inputs.WORKLOAD_ORDER)
+def test_parity_full_size(da, name):
+    inp = da_inputs.make_inputs(name)
+    backward = inp.wl.backward or name == "sp4d_inf"
+    got = _run_gpu(da, inp, backward=backward)
+    ref = oracle.run_inputs(inp, backward_pass=backward)
+    for k in ref:
+        print(f"{name}.{k}: max_rel={max_rel(got[k], ref[k]):.3e}")
+    _compare(inp, got, ref)
+
+
+def _custom(seed, shapes_ks, B, C, G, A, P, dtype="f32", lo=-0.3, hi=1.3, wscale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    K, S = len(shapes_ks), len(shapes_ks[0])
+    ss = torch.zeros(K, S, 2, dtype=torch.int32)
+    ls = torch.zeros(K, S, dtype=torch.int32)
+    row = 0
+    for k in range(K):
+        for s in range(S):
+            ss[k, s, 0], ss[k, s, 1] = shapes_ks[k][s]
+            ls[k, s] = row
+            row += shapes_ks[k][s][0] * shapes_ks[k][s][1]
+    feat = torch.randn(B, row, C, generator=g)
+    if dtype == "bf16":
+        feat = feat.to(torch.bfloat16)
+    loc = lo + (hi - lo) * torch.rand(B, A, P, K, 2, generator=g)
+    w = torch.randn(B, A, P, K, S, G, generator=g) * wscale
+    go = torch.randn(B, A, C, generator=g)
+    wl = da_inputs.WORKLOADS["tiny"].replace(name=f"custom{seed}", feat_dtype=dtype)
+    return da_inputs.Inputs(wl, feat, ss, ls, loc, w, go)
+
+
+CASES = [
+    # (seed, shapes [K][S], B, C, G, A, P, dtype)
+    (1, [[(7, 9), (3, 5)], [(6, 11), (2, 2)]], 2, 32, 1, 5, 3, "f32"),    # D=32 (8 chunks), G=1
+    (2, [[(7, 9), (3, 5)], [(6, 11), (2, 2)]], 2, 64, 4, 7, 5, "f32"),    # D=16
+    (3, [[(13, 4)], [(1, 1)], [(5, 17)]], 3, 24, 3, 11, 7, "f32"),        # D=8, G=3, 1x1 map
+    (4, [[(9, 9), (4, 4), (2, 2)]], 2, 64, 16, 9, 4, "f32"),              # D=4, G=16
+    (5, [[(10, 12), (5, 6)], [(8, 8), (4, 4)]], 2, 256, 8, 13, 13, "f32"),  # Sparse4D-like groups
+    (6, [[(7, 9), (3, 5)], [(6, 11), (2, 2)]], 2, 128, 2, 6, 3, "bf16"),  # D=64 bf16
+    (7, [[(7, 9), (3, 5)], [(6, 11), (2, 2)]], 2, 64, 2, 6, 3, "bf16"),   # D=32 bf16
+    (8, [[(7, 9)], [(3, 5)]], 1, 32, 2, 9, 5, "bf16"),                     # D=16 bf16
+    (9, [[(7, 9)], [(3, 5)]], 1, 32, 4, 10, 6, "bf16"),                    # D=8 bf16
+    (10, [[(31, 47), (16, 24), (8, 12)]] * 3, 1, 64, 2, 37, 11, "f32"),    # many chunks per warp
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"case{c[0]}" for c in CASES])
+def test_parity_shapes(da, case):
+    seed, shapes, B, C, G, A, P, dt = case
+    inp = _custom(seed, shapes, B, C, G, A, P, dt)
+    got = _run_gpu(da, inp)
+    ref = oracle.run_inputs(inp)
+    _compare(inp, got, ref)
+
+
+@pytest.mark.parametrize("B,A,P", [(0, 5, 3), (2, 0, 3), (2, 5, 0)])
+def test_empty(da, B, A, P):
+    inp = _custom(20, [[(6, 7)]], max(B, 1), 32, 2, max(A, 1), max(P, 1))
+    inp.feat = inp.feat[:B].contiguous()
+    inp.loc = inp.loc[:B, :A, :P].contiguous()
+    inp.weights = inp.weights[:B, :A, :P].contiguous()
+    inp.grad_out = inp.grad_out[:B, :A].contiguous()
+    got = _run_gpu(da, inp)
+    assert got["out"].shape == (B, A, 32) and np.all(got["out"] == 0)
+    assert got["grad_feat"].shape == tuple(inp.feat.shape) and np.all(got["grad_feat"] == 0)
+    assert got["grad_loc"].shape == tuple(inp.loc.shape) and np.all(got["grad_loc"] == 0)
+    assert got["grad_weight"].shape == tuple(inp.weights.shape)
+
+
+def test_nonfinite_and_far_locations(da):
+    inp = _custom(21, [[(6, 7), (3, 3)]], 1, 32, 2, 8, 4)
+    loc = inp.loc.clone()
+    loc[0, 0, 0, 0, 0] = float("nan")
+    loc[0, 1, 1, 0, 1] = float("inf")
+    loc[0, 2, 2, 0, 0] = -float("inf")
+    loc[0, 3, :, 0, :] = 1e30
+    loc[0, 4, :, 0, :] = -1e30
+    loc[0, 5, 0, 0, :] = torch.tensor([-0.49, 1.49])
+    inp.loc = loc
+    got = _run_gpu(da, inp)
+    ref = oracle.run_inputs(inp)
+    _compare(inp, got, ref)
+
+
+def test_output_guard_bands(da):
+    """Outputs are written in place inside NaN-filled buffers: nothing outside
+    the tensor may change."""
+    inp = _custom(22, [[(9, 10), (4, 5)]], 2, 64, 4, 9, 5)
+    dev = torch.device("cuda")
+    pad = 64
+
+    def guarded(shape):
+        n = int(np.prod(shape))
+        buf = torch.full((n + 2 * pad,), float("nan"), device=dev)
+        return buf, buf[pad:pad + n].view(shape)
+
+    feat, loc, w, go = (t.to(dev) for t in (inp.feat, inp.loc, inp.weights, inp.grad_out))
+    ob, out = guarded(tuple(go.shape))
+    fb, gf = guarded(tuple(feat.shape))
+    lb, gl = guarded(tuple(loc.shape))
+    wb, gw = guarded(tuple(w.shape))
+    da.da_forward(feat, inp.spatial_shape, inp.level_start_index, loc, w, out=out)
+    da.da_backward(feat, inp.spatial_shape, inp.level_start_index, loc, w, go,
+                   grad_feat=gf, grad_loc=gl, grad_weight=gw)
+    torch.cuda.synchronize()
+    for buf in (ob, fb, lb, wb):
+        assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[-pad:]).all()
+    ref = oracle.run_inputs(inp)
+    _compare(inp, {"out": to_np(out), "grad_feat": to_np(gf), "grad_loc": to_np(gl),
+                   "grad_weight": to_np(gw)}, ref)
+
+
+def test_forward_is_deterministic(da):
+    inp = da_inputs.make_inputs(da_inputs.small_variant("sp4d_train", batch=2, num_anchors=64))
+    a = _run_gpu(da, inp, backward=False)["out"]
+    b = _run_gpu(da, inp, backward=False)["out"]
+    np.testing.assert_array_equal(a, b)
+
+
+def test_autograd_function_and_side_stream(da):
+    inp = _custom(23, [[(8, 9), (4, 5)], [(7, 6), (3, 3)]], 2, 64, 4, 6, 3)
+    dev = torch.device("cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        feat = inp.feat.to(dev).requires_grad_(True)
+        loc = inp.loc.to(dev).requires_grad_(True)
+        w = inp.weights.to(dev).requires_grad_(True)
+        out = da.DeformableAggregationFunction.apply(feat, inp.spatial_shape,
+                                                     inp.level_start_index, loc, w)
+        out.backward(inp.grad_out.to(dev))
+    s.synchronize()
+    ref = oracle.run_inputs(inp)
+    got = {"out": to_np(out), "grad_feat": to_np(feat.grad), "grad_loc": to_np(loc.grad),
+           "grad_weight": to_np(w.grad)}
+    _compare(inp, got, ref)
+
+
+def test_invalid_arguments_raise_before_launch(da):
+    inp = _custom(24, [[(6, 7)]], 1, 32, 2, 4, 3)
+    dev = torch.device("cuda")
+    feat, loc, w = inp.feat.to(dev), inp.loc.to(dev), inp.weights.to(dev)
+    bad_ls = inp.level_start_index + 1  # the map would overrun the feature rows
+    with pytest.raises(da.DaError, match="DA_ERR_SHAPE"):
+        da.da_forward(feat, inp.spatial_shape, bad_ls, loc, w)
+    with pytest.raises(ValueError):
+        da.da_forward(feat.cpu(), inp.spatial_shape, inp.level_start_index, loc, w)
+    torch.cuda.synchronize()
