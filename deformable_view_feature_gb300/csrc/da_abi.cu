@@ -153,10 +153,13 @@ da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t
     if (!aligned(grad_feat, 16)) return fail(DA_ERR_ALIGN, "grad_feat must be 16-byte aligned");
     if (!aligned(grad_loc, 4)) return fail(DA_ERR_ALIGN, "grad_loc must be 4-byte aligned");
     if (!aligned(grad_weight, 4)) return fail(DA_ERR_ALIGN, "grad_weight must be 4-byte aligned");
-    // The per-CTA grad_loc staging area must fit in shared memory.
-    const int64_t smem = static_cast<int64_t>(pb.anchors_per_cta) * pb.pk * 2 * 4;
+    // The backward walks (b, k, a) views; the grid must cover them, and the
+    // per-CTA grad_loc staging area must fit in shared memory.
+    if (static_cast<int64_t>(pb.num_ba) * pb.K > INT32_MAX)
+        return fail(DA_ERR_UNSUPPORTED, "batch*anchors*cams exceeds int32");
+    const int64_t smem = static_cast<int64_t>(pb.anchors_per_cta) * pb.P * 2 * 4;
     if (smem > 200 * 1024)
-        return fail(DA_ERR_UNSUPPORTED, "pts*cams = %d too large for the grad_loc staging area", pb.pk);
+        return fail(DA_ERR_UNSUPPORTED, "num_pts = %d too large for the grad_loc staging area", pb.P);
     a.grad_out = grad_out;
     a.grad_feat = grad_feat;
     a.grad_loc = grad_loc;

@@ -8,8 +8,9 @@
 //   grad_weight += grad_out * (w1*v1 + w2*v2 + w3*v3 + w4*v4)
 // each summed over the group's D channels.
 //
-// Decomposition (same as the forward: a warp owns (b*A+a, g), lanes split
-// into sample slot, corner and 16-byte chunk):
+// Decomposition: a warp owns one (b, k, a, g) task, i.e. the P*S samples of
+// one anchor in one camera for one group. Lanes split into sample slot,
+// corner and 16-byte chunk, as in the forward.
 //   * d_i = sum_c grad_out[c] * v_i[c] is the only per-channel reduction the
 //     three gradients need: grad_weight = sum_i w_i d_i, grad_x =
 //     W*w*(lh*(d4-d3) + hh*(d2-d1)), grad_y = H*w*(lw*(d4-d2) + hw*(d3-d1)). Each
@@ -20,8 +21,9 @@
 //     16-byte vector reduction (red.global.add.v4.f32). The scatter is the one
 //     place where samples of different anchors meet, so it must be atomic.
 //   * grad_weight: every (b,a,p,k,s,g) belongs to one warp: a plain store.
-//   * grad_loc: sums over s and g, all inside the CTA (it owns whole
-//     anchors). It is accumulated with shared-memory atomics and stored once.
+//   * grad_loc[b,a,p,k] sums over s and g, all inside the CTA that owns view
+//     (b, k, a). It is accumulated with shared-memory atomics and stored
+//     once.
 #include "da_internal.cuh"
 
 namespace da {
@@ -34,8 +36,16 @@ __global__ void zero_fill_kernel(float4 *__restrict__ p, int64_t n4)
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// The backward walks the problem camera-major: CTA i owns the views
+// v = (b*K + k)*A + a in [i*views_per_cta, (i+1)*views_per_cta), all groups
+// of each. At any moment the resident CTAs touch the maps of one or two
+// cameras of one batch item (feat and grad_feat slices of NPIX*C values each).
+// That working set stays in L2, so the grad_feat reductions hit lines that
+// are already there. Every output element still has one owner:
+//   * grad_weight and grad_loc are per camera;
+//   * grad_feat rows belong to one camera's maps.
 template <typename T, int CH>
-__global__ void __launch_bounds__(kThreads) bwd_kernel(const BwdArgs args)
+__global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
 {
     using Ck = Chunk<T>;
     constexpr int VEC = Ck::kVec;
@@ -44,7 +54,10 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(const BwdArgs args)
 
     __shared__ __align__(16) int2 tab[kWarps][32][4];   // {row, w * corner weight}
     __shared__ __align__(16) float dtab[kWarps][32][4]; // per-corner d_i
-    extern __shared__ float gl_s[];                      // [anchors_per_cta][P*K][2]
+    // Epilogue coefficients per sample: grad_weight = sum cw_i d_i,
+    // grad_x = sum ax_i d_i, grad_y = sum ay_i d_i.
+    __shared__ __align__(16) float4 etab[kWarps][32][3];
+    extern __shared__ float gl_s[];                      // [views_per_cta][P][2]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -52,21 +65,27 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(const BwdArgs args)
     const int corner = (lane / CH) & 3;
     const int slot = lane / (4 * CH);
 
-    const int64_t ba0 = static_cast<int64_t>(blockIdx.x) * pb.anchors_per_cta;
-    const int64_t na = min(static_cast<int64_t>(pb.anchors_per_cta), pb.num_ba - ba0);
-    const int ntask = static_cast<int>(na) * pb.G;
+    const int64_t num_views = static_cast<int64_t>(pb.num_ba) * pb.K;
+    const int64_t v0 = static_cast<int64_t>(blockIdx.x) * pb.anchors_per_cta;
+    const int64_t nv = min(static_cast<int64_t>(pb.anchors_per_cta), num_views - v0);
+    const int ntask = static_cast<int>(nv) * pb.G;
+    const int ps = pb.P * pb.S;  // samples per task
     const int64_t row_bytes = static_cast<int64_t>(pb.C) * static_cast<int64_t>(16 / VEC);
     const int64_t grow = pb.C;  // grad_feat row stride, in floats
 
-    const int nloc = static_cast<int>(na) * pb.pk * 2;
+    const int nloc = static_cast<int>(nv) * pb.P * 2;
     for (int i = threadIdx.x; i < nloc; i += kThreads) gl_s[i] = 0.f;
     __syncthreads();
 
     for (int task = warp; task < ntask; task += kWarps) {
-        const int64_t ba = ba0 + task / pb.G;
-        const int aloc = task / pb.G;
+        const int vloc = task / pb.G;
         const int g = task % pb.G;
-        const int64_t b = ba / pb.A;
+        const int64_t view = v0 + vloc;
+        const int64_t a = view % pb.A;
+        const int64_t bk = view / pb.A;
+        const int k = static_cast<int>(bk % pb.K);
+        const int64_t b = bk / pb.K;
+        const int64_t ba = b * pb.A + a;
         const int64_t coff = static_cast<int64_t>(g) * pb.D + chunk * VEC;  // channel offset
         const char *base = static_cast<const char *>(pb.feat) +
                            (b * pb.rows * pb.C + coff) * (16 / VEC);
@@ -85,27 +104,32 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(const BwdArgs args)
             }
         }
 
-        for (int j0 = 0; j0 < pb.pks; j0 += 32) {
-            const int n = min(32, pb.pks - j0);
-            // Footprint of sample j0 + lane; kept in registers for the epilogue.
-            Footprint f;
-            float w = 0.f;
-            int jk = 0;
-            MapInfo m{};
+        for (int j0 = 0; j0 < ps; j0 += 32) {
+            const int n = min(32, ps - j0);
+            // Footprint of sample j0 + lane: the gather table, and the
+            // coefficients that turn the four d_i into the three gradients
+            // (page §4.1: grad_w = lh*(v4-v3) + hh*(v2-v1) times W*w, and
+            // grad_h = lw*(v4-v2) + hw*(v3-v1) times H*w).
             if (lane < n) {
                 const int j = j0 + lane;
-                jk = j / pb.S;
-                const int s = j - jk * pb.S;
-                const int k = jk % pb.K;
-                const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + (ba * pb.pk + jk) * 2);
-                w = pb.weights[(ba * pb.pks + j) * pb.G + g];
-                m = pb.maps[k * pb.S + s];
+                const int p = j / pb.S;
+                const int s = j - p * pb.S;
+                const int64_t bapk = (ba * pb.P + p) * pb.K + k;
+                const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + bapk * 2);
+                const float w = pb.weights[(bapk * pb.S + s) * pb.G + g];
+                const MapInfo m = pb.maps[k * pb.S + s];
+                Footprint f;
                 footprint(xy.x, xy.y, m, f);
                 int4 *dst = reinterpret_cast<int4 *>(&tab[warp][lane][0]);
                 dst[0] = make_int4(f.row[0], __float_as_int(w * f.cw[0]),
                                    f.row[1], __float_as_int(w * f.cw[1]));
                 dst[1] = make_int4(f.row[2], __float_as_int(w * f.cw[2]),
                                    f.row[3], __float_as_int(w * f.cw[3]));
+                const float wx = static_cast<float>(m.W) * w;
+                const float wy = static_cast<float>(m.H) * w;
+                etab[warp][lane][0] = make_float4(f.cw[0], f.cw[1], f.cw[2], f.cw[3]);
+                etab[warp][lane][1] = make_float4(-wx * f.hh, wx * f.hh, -wx * f.lh, wx * f.lh);
+                etab[warp][lane][2] = make_float4(-wy * f.hw, -wy * f.lw, wy * f.hw, wy * f.lw);
             }
             __syncwarp();
 
@@ -156,29 +180,45 @@ __global__ void __launch_bounds__(kThreads) bwd_kernel(const BwdArgs args)
             __syncwarp();
 
             if (lane < n) {
-                const float4 dd = *reinterpret_cast<const float4 *>(&dtab[warp][lane][0]);
                 const int j = j0 + lane;
-                const float gweight = f.cw[0] * dd.x + f.cw[1] * dd.y + f.cw[2] * dd.z + f.cw[3] * dd.w;
-                args.grad_weight[(ba * pb.pks + j) * pb.G + g] = gweight;
-                const float gx = static_cast<float>(m.W) * w * (f.lh * (dd.w - dd.z) + f.hh * (dd.y - dd.x));
-                const float gy = static_cast<float>(m.H) * w * (f.lw * (dd.w - dd.y) + f.hw * (dd.z - dd.x));
-                atomicAdd(&gl_s[(aloc * pb.pk + jk) * 2 + 0], gx);
-                atomicAdd(&gl_s[(aloc * pb.pk + jk) * 2 + 1], gy);
+                const int p = j / pb.S;
+                const int s = j - p * pb.S;
+                const float4 dd = *reinterpret_cast<const float4 *>(&dtab[warp][lane][0]);
+                const float4 cw = etab[warp][lane][0];
+                const float4 ax = etab[warp][lane][1];
+                const float4 ay = etab[warp][lane][2];
+                const float gweight = cw.x * dd.x + cw.y * dd.y + cw.z * dd.z + cw.w * dd.w;
+                args.grad_weight[(((ba * pb.P + p) * pb.K + k) * pb.S + s) * pb.G + g] = gweight;
+                const float gx = ax.x * dd.x + ax.y * dd.y + ax.z * dd.z + ax.w * dd.w;
+                const float gy = ay.x * dd.x + ay.y * dd.y + ay.z * dd.z + ay.w * dd.w;
+                atomicAdd(&gl_s[(vloc * pb.P + p) * 2 + 0], gx);
+                atomicAdd(&gl_s[(vloc * pb.P + p) * 2 + 1], gy);
             }
             __syncwarp();
         }
     }
     __syncthreads();
-    float *gdst = args.grad_loc + ba0 * pb.pk * 2;
-    for (int i = threadIdx.x; i < nloc; i += kThreads) gdst[i] = gl_s[i];
+    // grad_loc[b,a,p,k,:] for the CTA's views: a stride of K pairs between p.
+    for (int i = threadIdx.x; i < nloc; i += kThreads) {
+        const int vloc = i / (pb.P * 2);
+        const int r = i - vloc * pb.P * 2;
+        const int p = r >> 1;
+        const int64_t view = v0 + vloc;
+        const int64_t a = view % pb.A;
+        const int64_t bk = view / pb.A;
+        const int64_t k = bk % pb.K;
+        const int64_t b = bk / pb.K;
+        args.grad_loc[(((b * pb.A + a) * pb.P + p) * pb.K + k) * 2 + (r & 1)] = gl_s[i];
+    }
 }
 
 template <typename T, int CH>
 cudaError_t launch(const BwdArgs &a, cudaStream_t st)
 {
-    const int64_t grid = sampling_grid(a.pb);
+    const int64_t views = static_cast<int64_t>(a.pb.num_ba) * a.pb.K;
+    const int64_t grid = (views + a.pb.anchors_per_cta - 1) / a.pb.anchors_per_cta;
     if (grid == 0) return cudaSuccess;
-    const size_t smem = static_cast<size_t>(a.pb.anchors_per_cta) * a.pb.pk * 2 * sizeof(float);
+    const size_t smem = static_cast<size_t>(a.pb.anchors_per_cta) * a.pb.P * 2 * sizeof(float);
     if (smem > 48 * 1024) {
         cudaError_t e = cudaFuncSetAttribute(bwd_kernel<T, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));

@@ -52,6 +52,9 @@ def _load():
         lib.dao_backward.argtypes = ([i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp, i64, i64,
                                                   vp, vp, vp])
         lib.dao_backward.restype = i32
+        lib.dao_grad_loc_magnitude.argtypes = ([i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp,
+                                                            i64, i64, vp])
+        lib.dao_grad_loc_magnitude.restype = i32
         lib.dao_bilinear.argtypes = [vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float]
         lib.dao_bilinear.restype = ctypes.c_double
         _lib = lib
@@ -124,6 +127,22 @@ def backward(feat, spatial_shape, level_start_index, loc, weights, grad_out,
         gl = gl.reshape(B, A, P, K, 2)
         gw = gw.reshape(B, A, P, K, S, G)
     return gf, gl, gw
+
+
+def grad_loc_magnitude(feat, spatial_shape, level_start_index, loc, weights, grad_out):
+    """Sum of |terms| of every grad_loc element (an error-bound helper for the
+    parity tests; see dao_grad_loc_magnitude in da_oracle.c)."""
+    feat, bf16, ss, ls, loc, weights, dims = _prep(feat, spatial_shape, level_start_index,
+                                                   loc, weights)
+    B, K, S, C, G, A, P, rows = dims
+    grad_out = np.ascontiguousarray(grad_out, dtype=np.float32)
+    mag = np.empty((B, A, P, K, 2), dtype=np.float32)
+    rc = _load().dao_grad_loc_magnitude(B, K, S, C, G, A, P, rows, _ptr(ss), _ptr(ls), _ptr(feat),
+                                        bf16, _ptr(loc), _ptr(weights), _ptr(grad_out), 0, B * A,
+                                        _ptr(mag))
+    if rc != 0:
+        raise ValueError(f"oracle magnitude rejected its arguments (code {rc})")
+    return mag
 
 
 def bilinear(fmap: np.ndarray, c: int, x: float, y: float) -> float:

@@ -265,3 +265,58 @@ double dao_bilinear(const float *map, int32_t H, int32_t W, int32_t C, int32_t c
         if (f.row[i] >= 0) v += cw[i] * (double)map[f.row[i] * C + c];
     return v;
 }
+
+/*
+ * Error-bound helper for the parity tests, not part of the operator.
+ *
+ * For each location (b,a,p,k) it returns the sum, over s, g and the group's
+ * channels, of the absolute values of the products that make up grad_loc in
+ * §4.1. mag[..,0] is that sum for the width component, mag[..,1] for the
+ * height component:
+ *   mag[..,0] = sum W * |top_grad| * (lh*(|v4|+|v3|) + hh*(|v2|+|v1|))
+ *   mag[..,1] = sum H * |top_grad| * (lw*(|v4|+|v2|) + hw*(|v3|+|v1|))
+ * A floating-point sum of these terms cannot be off by more than (number of
+ * sequential roundings) * unit roundoff * mag.
+ */
+int dao_grad_loc_magnitude(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
+                           const int32_t *shape, const int32_t *start,
+                           const void *feat, int feat_bf16,
+                           const float *loc, const float *weights, const float *grad_out,
+                           int64_t ba_begin, int64_t ba_end, float *mag)
+{
+    if (!check_dims(B, K, S, C, G, A, P, rows, shape, start)) return DAO_ERR_ARGS;
+    if (ba_begin < 0 || ba_end < ba_begin || ba_end > (int64_t)B * A) return DAO_ERR_ARGS;
+    const int D = C / G;
+    int64_t ba;
+    for (ba = ba_begin; ba < ba_end; ++ba) {
+        const int64_t b = ba / A;
+        int p, k, s, g, c, i;
+        for (p = 0; p < P; ++p)
+            for (k = 0; k < K; ++k) {
+                const float *xy = loc + ((ba * P + p) * K + k) * 2;
+                double mx = 0.0, my = 0.0;
+                for (s = 0; s < S; ++s) {
+                    const int32_t H = shape[(k * S + s) * 2];
+                    const int32_t W = shape[(k * S + s) * 2 + 1];
+                    footprint f;
+                    make_footprint(xy[0], xy[1], H, W, start[k * S + s], &f);
+                    for (g = 0; g < G; ++g) {
+                        const double w = fabs((double)weights[(((ba * P + p) * K + k) * S + s) * G + g]);
+                        for (c = 0; c < D; ++c) {
+                            const double tg = fabs((double)grad_out[ba * C + (int64_t)g * D + c]) * w;
+                            double v[4] = {0.0, 0.0, 0.0, 0.0};
+                            for (i = 0; i < 4; ++i)
+                                if (f.row[i] >= 0)
+                                    v[i] = fabs(feat_value(feat, feat_bf16,
+                                                           (b * rows + f.row[i]) * C + (int64_t)g * D + c));
+                            mx += (double)W * tg * (f.lh * (v[3] + v[2]) + f.hh * (v[1] + v[0]));
+                            my += (double)H * tg * (f.lw * (v[3] + v[1]) + f.hw * (v[2] + v[0]));
+                        }
+                    }
+                }
+                mag[(((ba - ba_begin) * P + p) * K + k) * 2 + 0] = (float)mx;
+                mag[(((ba - ba_begin) * P + p) * K + k) * 2 + 1] = (float)my;
+            }
+    }
+    return DAO_OK;
+}

@@ -429,3 +429,28 @@ def test_workload_shapes():
     assert W["large_bf16"].num_samples == 4_492_800
     assert W["dcnv4"].num_samples == 903_168
     assert W["tiny"].num_samples == 64
+
+
+# --------------------------------------------------------------------------- tolerance helper
+
+def test_grad_loc_magnitude_bounds_and_hand_value():
+    """The error-bound helper: it bounds |grad_loc|, and on the 2x2 centre
+    case it equals the hand-worked sum of |terms|. With W = H = 2,
+    |top_grad| = 2 and lh = lw = hh = hw = 0.5:
+    x: 2*2*(0.5*(4+3) + 0.5*(2+1)) = 20; y: 2*2*(0.5*(4+2) + 0.5*(3+1)) = 20."""
+    feat = np.array([1.0, 2.0, 3.0, 4.0], np.float32).reshape(1, 4, 1)
+    ss = np.array([[[2, 2]]], np.int32)
+    ls = np.zeros((1, 1), np.int32)
+    loc = np.array([0.5, 0.5], np.float32).reshape(1, 1, 1, 1, 2)
+    w = np.full((1, 1, 1, 1, 1, 1), 2.0, np.float32)
+    go = np.ones((1, 1, 1), np.float32)
+    m = oracle.grad_loc_magnitude(feat, ss, ls, loc, w, go)
+    np.testing.assert_array_equal(m.ravel(), np.array([20.0, 20.0], np.float32))
+    rng = np.random.default_rng(22)
+    feat, ss, ls, loc, w, go = _rand_problem(rng, 2, [[(7, 9), (3, 4)], [(5, 6), (2, 2)]],
+                                             C=8, G=2, A=5, P=3)
+    _, gl, _ = oracle.backward(feat, ss, ls, loc, w, go)
+    m = oracle.grad_loc_magnitude(feat, ss, ls, loc, w, go)
+    assert np.all(np.abs(gl) <= m * (1 + 1e-6) + 1e-30)
+    m2 = oracle.grad_loc_magnitude(feat, ss, ls, loc, w, (-3.0 * go).astype(np.float32))
+    np.testing.assert_allclose(m2, 3.0 * m, rtol=1e-6)
