@@ -99,6 +99,11 @@ da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_
     pb.pk = d.num_pts * d.num_cams;
     pb.num_ba = static_cast<int32_t>(num_ba);
     pb.anchors_per_cta = d.num_groups < da::kWarps ? da::kWarps / d.num_groups : 1;
+    pb.nmaps = static_cast<int32_t>(nmaps);
+    pb.div_S = da::FastDiv::make(d.num_scales > 0 ? d.num_scales : 1);
+    pb.div_K = da::FastDiv::make(d.num_cams > 0 ? d.num_cams : 1);
+    pb.div_G = da::FastDiv::make(d.num_groups);
+    pb.div_A = da::FastDiv::make(d.num_anchors > 0 ? d.num_anchors : 1);
     return DA_OK;
 }
 

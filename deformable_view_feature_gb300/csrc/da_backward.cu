@@ -36,6 +36,43 @@ __global__ void zero_fill_kernel(float4 *__restrict__ p, int64_t n4)
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// Sums each of a lane's four per-sample values d[0..3] over the CH lanes of
+// its corner row (the lanes that differ only in the chunk bits). Instead of
+// reducing each value on its own (4*log2(CH) shuffles), the lanes split the
+// work: each halving step sends half of the values still held. After the
+// last step each sum sits in CH/4 lanes (CH >= 4), or 2 or 4 sums per lane
+// (CH = 2 or 1). Then one lane per sum stores it to dst[u * 4], the table
+// entry of sample i + u.
+template <int CH>
+__device__ __forceinline__ void row_sum_store(const float (&d)[4], int chunk, float *dst)
+{
+    if constexpr (CH >= 4) {
+        const bool hA = (chunk & (CH / 2)) != 0;
+        float a0 = hA ? d[2] : d[0], a1 = hA ? d[3] : d[1];
+        const float s0 = hA ? d[0] : d[2], s1 = hA ? d[1] : d[3];
+        a0 += __shfl_xor_sync(0xffffffffu, s0, CH / 2);
+        a1 += __shfl_xor_sync(0xffffffffu, s1, CH / 2);
+        const bool hB = (chunk & (CH / 4)) != 0;
+        float r = hB ? a1 : a0;
+        const float t = hB ? a0 : a1;
+        r += __shfl_xor_sync(0xffffffffu, t, CH / 4);
+#pragma unroll
+        for (int m = CH / 8; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+        if ((chunk & (CH / 4 - 1)) == 0) dst[((hA ? 2 : 0) + (hB ? 1 : 0)) * 4] = r;
+    } else if constexpr (CH == 2) {
+        const bool h = (chunk & 1) != 0;
+        float a0 = h ? d[2] : d[0], a1 = h ? d[3] : d[1];
+        const float s0 = h ? d[0] : d[2], s1 = h ? d[1] : d[3];
+        a0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        a1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        dst[(h ? 2 : 0) * 4] = a0;
+        dst[(h ? 3 : 1) * 4] = a1;
+    } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) dst[u * 4] = d[u];
+    }
+}
+
 // The backward walks the problem camera-major: CTA i owns the views
 // v = (b*K + k)*A + a in [i*views_per_cta, (i+1)*views_per_cta), all groups
 // of each. At any moment the resident CTAs touch the maps of one or two
@@ -49,15 +86,17 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
 {
     using Ck = Chunk<T>;
     constexpr int VEC = Ck::kVec;
+    constexpr int ESZ = 16 / VEC;
     constexpr int SPP = 8 / CH;
     const Problem &pb = args.pb;
 
-    __shared__ __align__(16) int2 tab[kWarps][32][4];   // {row, w * corner weight}
-    __shared__ __align__(16) float dtab[kWarps][32][4]; // per-corner d_i
+    __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];  // {row, w * corner weight}
+    __shared__ __align__(16) float dtab[kWarps][32][4];        // per-corner d_i of each sample
     // Epilogue coefficients per sample: grad_weight = sum cw_i d_i,
     // grad_x = sum ax_i d_i, grad_y = sum ay_i d_i.
     __shared__ __align__(16) float4 etab[kWarps][32][3];
-    extern __shared__ float gl_s[];                      // [views_per_cta][P][2]
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    extern __shared__ float gl_s[];                             // [views_per_cta][P][2]
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -65,31 +104,31 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
     const int corner = (lane / CH) & 3;
     const int slot = lane / (4 * CH);
 
-    const int64_t num_views = static_cast<int64_t>(pb.num_ba) * pb.K;
-    const int64_t v0 = static_cast<int64_t>(blockIdx.x) * pb.anchors_per_cta;
-    const int64_t nv = min(static_cast<int64_t>(pb.anchors_per_cta), num_views - v0);
-    const int ntask = static_cast<int>(nv) * pb.G;
+    const int num_views = pb.num_ba * pb.K;
+    const int v0 = static_cast<int>(blockIdx.x) * pb.anchors_per_cta;
+    const int nv = min(pb.anchors_per_cta, num_views - v0);
+    const int ntask = nv * pb.G;
     const int ps = pb.P * pb.S;  // samples per task
-    const int64_t row_bytes = static_cast<int64_t>(pb.C) * static_cast<int64_t>(16 / VEC);
-    const int64_t grow = pb.C;  // grad_feat row stride, in floats
+    const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
+    const uint32_t grow_bytes = static_cast<uint32_t>(pb.C) * 4;  // grad_feat row pitch
 
-    const int nloc = static_cast<int>(nv) * pb.P * 2;
+    stage_maps(pb, maps_s);
+    const int nloc = nv * pb.P * 2;
     for (int i = threadIdx.x; i < nloc; i += kThreads) gl_s[i] = 0.f;
     __syncthreads();
 
     for (int task = warp; task < ntask; task += kWarps) {
-        const int vloc = task / pb.G;
-        const int g = task % pb.G;
-        const int64_t view = v0 + vloc;
-        const int64_t a = view % pb.A;
-        const int64_t bk = view / pb.A;
-        const int k = static_cast<int>(bk % pb.K);
-        const int64_t b = bk / pb.K;
-        const int64_t ba = b * pb.A + a;
+        const int vloc = static_cast<int>(pb.div_G.div(task));
+        const int g = task - vloc * pb.G;
+        const int view = v0 + vloc;
+        const int bk = static_cast<int>(pb.div_A.div(view));
+        const int a = view - bk * pb.A;
+        const int b = static_cast<int>(pb.div_K.div(bk));
+        const int k = bk - b * pb.K;
+        const int64_t ba = static_cast<int64_t>(b) * pb.A + a;
         const int64_t coff = static_cast<int64_t>(g) * pb.D + chunk * VEC;  // channel offset
-        const char *base = static_cast<const char *>(pb.feat) +
-                           (b * pb.rows * pb.C + coff) * (16 / VEC);
-        float *gbase = args.grad_feat + b * pb.rows * pb.C + coff;
+        const char *base = static_cast<const char *>(pb.feat) + (b * pb.rows * pb.C + coff) * ESZ;
+        char *gbase = reinterpret_cast<char *>(args.grad_feat + b * pb.rows * pb.C + coff);
 
         float go[VEC];
         {
@@ -110,43 +149,46 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
             // coefficients that turn the four d_i into the three gradients
             // (page §4.1: grad_w = lh*(v4-v3) + hh*(v2-v1) times W*w, and
             // grad_h = lw*(v4-v2) + hw*(v3-v1) times H*w).
-            if (lane < n) {
-                const int j = j0 + lane;
-                const int p = j / pb.S;
-                const int s = j - p * pb.S;
-                const int64_t bapk = (ba * pb.P + p) * pb.K + k;
-                const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + bapk * 2);
-                const float w = pb.weights[(bapk * pb.S + s) * pb.G + g];
-                const MapInfo m = pb.maps[k * pb.S + s];
-                Footprint f;
-                footprint(xy.x, xy.y, m, f);
-                int4 *dst = reinterpret_cast<int4 *>(&tab[warp][lane][0]);
-                dst[0] = make_int4(f.row[0], __float_as_int(w * f.cw[0]),
-                                   f.row[1], __float_as_int(w * f.cw[1]));
-                dst[1] = make_int4(f.row[2], __float_as_int(w * f.cw[2]),
-                                   f.row[3], __float_as_int(w * f.cw[3]));
-                const float wx = static_cast<float>(m.W) * w;
-                const float wy = static_cast<float>(m.H) * w;
-                etab[warp][lane][0] = make_float4(f.cw[0], f.cw[1], f.cw[2], f.cw[3]);
-                etab[warp][lane][1] = make_float4(-wx * f.hh, wx * f.hh, -wx * f.lh, wx * f.lh);
-                etab[warp][lane][2] = make_float4(-wy * f.hw, -wy * f.lw, wy * f.hw, wy * f.lw);
+            {
+                int row[4] = {-1, -1, -1, -1};
+                float tw[4] = {0.f, 0.f, 0.f, 0.f};
+                if (lane < n) {
+                    const int j = j0 + lane;
+                    const int p = static_cast<int>(pb.div_S.div(j));
+                    const int s = j - p * pb.S;
+                    const int64_t bapk = (ba * pb.P + p) * pb.K + k;
+                    const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + bapk * 2);
+                    const float w = pb.weights[(bapk * pb.S + s) * pb.G + g];
+                    const MapInfo m = maps_s[k * pb.S + s];
+                    Footprint f;
+                    footprint(xy.x, xy.y, m, f);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        row[c] = f.row[c];
+                        tw[c] = w * f.cw[c];
+                    }
+                    const float wx = static_cast<float>(m.W) * w;
+                    const float wy = static_cast<float>(m.H) * w;
+                    etab[warp][lane][0] = make_float4(f.cw[0], f.cw[1], f.cw[2], f.cw[3]);
+                    etab[warp][lane][1] = make_float4(-wx * f.hh, wx * f.hh, -wx * f.lh, wx * f.lh);
+                    etab[warp][lane][2] = make_float4(-wy * f.hw, -wy * f.lw, wy * f.hw, wy * f.lw);
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tab[warp][c][lane] = make_int2(row[c], __float_as_int(tw[c]));
             }
             __syncwarp();
 
             for (int i0 = 0; i0 < n; i0 += 4 * SPP) {
-                int2 e[4];
+                const int i = i0 + 4 * slot;
+                const int4 e01 = *reinterpret_cast<const int4 *>(&tab[warp][corner][i]);
+                const int4 e23 = *reinterpret_cast<const int4 *>(&tab[warp][corner][i + 2]);
+                const int r[4] = {e01.x, e01.z, e23.x, e23.z};
+                const float tw[4] = {__int_as_float(e01.y), __int_as_float(e01.w), __int_as_float(e23.y),
+                                     __int_as_float(e23.w)};
                 uint4 raw[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
                 float d[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int i = i0 + slot + u * SPP;
-                    e[u] = (i < n) ? tab[warp][i][corner] : make_int2(-1, 0);
-                }
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    raw[u] = make_uint4(0u, 0u, 0u, 0u);
-                    if (e[u].x >= 0) raw[u] = ldg16(base + static_cast<int64_t>(e[u].x) * row_bytes);
-                }
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     float v[VEC];
@@ -155,33 +197,20 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
 #pragma unroll
                     for (int q = 0; q < VEC; ++q) acc = fmaf(go[q], v[q], acc);
                     d[u] = acc;
-                    if (e[u].x >= 0) {
-                        const float tw = __int_as_float(e[u].y);
-                        float *dst = gbase + static_cast<int64_t>(e[u].x) * grow;
+                    float *dst = reinterpret_cast<float *>(gbase + static_cast<uint64_t>(static_cast<uint32_t>(r[u])) *
+                                                                       grow_bytes);
 #pragma unroll
-                        for (int q = 0; q < VEC / 4; ++q)
-                            red_add_v4(dst + 4 * q, tw * go[4 * q], tw * go[4 * q + 1],
-                                       tw * go[4 * q + 2], tw * go[4 * q + 3]);
-                    }
+                    for (int q = 0; q < VEC / 4; ++q)
+                        red_add_v4_if(r[u] >= 0, dst + 4 * q, tw[u] * go[4 * q], tw[u] * go[4 * q + 1],
+                                      tw[u] * go[4 * q + 2], tw[u] * go[4 * q + 3]);
                 }
-#pragma unroll
-                for (int m2 = 1; m2 < CH; m2 <<= 1) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) d[u] += __shfl_xor_sync(0xffffffffu, d[u], m2);
-                }
-                if (chunk == 0) {
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const int i = i0 + slot + u * SPP;
-                        if (i < n) dtab[warp][i][corner] = d[u];
-                    }
-                }
+                row_sum_store<CH>(d, chunk, &dtab[warp][i][corner]);
             }
             __syncwarp();
 
             if (lane < n) {
                 const int j = j0 + lane;
-                const int p = j / pb.S;
+                const int p = static_cast<int>(pb.div_S.div(j));
                 const int s = j - p * pb.S;
                 const float4 dd = *reinterpret_cast<const float4 *>(&dtab[warp][lane][0]);
                 const float4 cw = etab[warp][lane][0];
@@ -203,12 +232,12 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
         const int vloc = i / (pb.P * 2);
         const int r = i - vloc * pb.P * 2;
         const int p = r >> 1;
-        const int64_t view = v0 + vloc;
-        const int64_t a = view % pb.A;
-        const int64_t bk = view / pb.A;
-        const int64_t k = bk % pb.K;
-        const int64_t b = bk / pb.K;
-        args.grad_loc[(((b * pb.A + a) * pb.P + p) * pb.K + k) * 2 + (r & 1)] = gl_s[i];
+        const int view = v0 + vloc;
+        const int bk = static_cast<int>(pb.div_A.div(view));
+        const int a = view - bk * pb.A;
+        const int b = static_cast<int>(pb.div_K.div(bk));
+        const int k = bk - b * pb.K;
+        args.grad_loc[(((static_cast<int64_t>(b) * pb.A + a) * pb.P + p) * pb.K + k) * 2 + (r & 1)] = gl_s[i];
     }
 }
 

@@ -8,17 +8,19 @@
 // warp owns one (b*A+a, g) task and its P*K*S samples):
 //   * A CTA of 8 warps owns `anchors_per_cta` whole anchors: all their groups.
 //   * Footprints: 32 samples at a time, one per lane. Each lane writes its
-//     sample's four {row, weight * corner weight} pairs to a per-warp table in
-//     shared memory.
+//     sample's four {row, weight * corner weight} pairs to a per-warp,
+//     corner-major table in shared memory.
 //   * Gather: the D channels of one corner row are D*sizeof(T) bytes, i.e.
-//     CH 16-byte chunks. Lane l reads chunk l % CH of corner (l / CH) % 4 of
-//     sample slot l / (4*CH). So one warp-wide 16-byte load reads the four
-//     corner rows of 8/CH samples, every row as one coalesced segment (the
-//     vectorised channel-last access of the DCNv4 page, "Solving the problem:
-//     2. let the GPU move less data").
+//     CH 16-byte chunks. Lane l reads chunk l % CH of corner (l / CH) % 4 for
+//     the samples of slot l / (4*CH). So one warp-wide 16-byte load reads the
+//     four corner rows of 8/CH samples, every row as one coalesced segment
+//     (the vectorised channel-last access of the DCNv4 page, "Solving the
+//     problem: 2. let the GPU move less data"). Each lane walks four
+//     consecutive samples per step, so four loads are in flight per lane.
+//     Their table entries arrive in two 16-byte shared loads.
 //   * Each lane accumulates its chunk in fp32 registers. At the end, shuffles
 //     sum over corners and slots, and the CH lanes of slot 0 write the group's
-//     D outputs with 16-byte stores.
+//     D outputs with 16-byte stores. No atomics: the result is deterministic.
 #include "da_internal.cuh"
 
 namespace da {
@@ -29,10 +31,14 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 {
     using Ck = Chunk<T>;
     constexpr int VEC = Ck::kVec;   // channels per 16-byte chunk
+    constexpr int ESZ = 16 / VEC;   // bytes per feature element
     constexpr int SPP = 8 / CH;     // samples per warp-wide load
     const Problem &pb = args.pb;
 
-    __shared__ __align__(16) int2 tab[kWarps][32][4];
+    __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    stage_maps(pb, maps_s);
+    __syncthreads();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -40,17 +46,18 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     const int corner = (lane / CH) & 3;
     const int slot = lane / (4 * CH);
 
-    const int64_t ba0 = static_cast<int64_t>(blockIdx.x) * pb.anchors_per_cta;
-    const int64_t na = min(static_cast<int64_t>(pb.anchors_per_cta), pb.num_ba - ba0);
-    const int ntask = static_cast<int>(na) * pb.G;
-    const int64_t row_bytes = static_cast<int64_t>(pb.C) * static_cast<int64_t>(16 / VEC);
+    const int ba0 = static_cast<int>(blockIdx.x) * pb.anchors_per_cta;
+    const int na = min(pb.anchors_per_cta, pb.num_ba - ba0);
+    const int ntask = na * pb.G;
+    const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
 
     for (int task = warp; task < ntask; task += kWarps) {
-        const int64_t ba = ba0 + task / pb.G;
-        const int g = task % pb.G;
-        const int64_t b = ba / pb.A;
+        const int tq = static_cast<int>(pb.div_G.div(task));
+        const int g = task - tq * pb.G;
+        const int ba = ba0 + tq;
+        const int b = static_cast<int>(pb.div_A.div(ba));
         const char *base = static_cast<const char *>(pb.feat) +
-                           (b * pb.rows * pb.C + static_cast<int64_t>(g) * pb.D) * (16 / VEC) +
+                           (static_cast<int64_t>(b) * pb.rows * pb.C + static_cast<int64_t>(g) * pb.D) * ESZ +
                            chunk * 16;
         float acc[VEC];
 #pragma unroll
@@ -58,52 +65,47 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 
         for (int j0 = 0; j0 < pb.pks; j0 += 32) {
             const int n = min(32, pb.pks - j0);
-            if (lane < n) {
-                const int j = j0 + lane;
-                const int jk = j / pb.S;  // p*K + k
-                const int s = j - jk * pb.S;
-                const int k = jk % pb.K;
-                const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + (ba * pb.pk + jk) * 2);
-                const float w = pb.weights[(ba * pb.pks + j) * pb.G + g];
-                Footprint f;
-                footprint(xy.x, xy.y, pb.maps[k * pb.S + s], f);
-                int4 *dst = reinterpret_cast<int4 *>(&tab[warp][lane][0]);
-                dst[0] = make_int4(f.row[0], __float_as_int(w * f.cw[0]),
-                                   f.row[1], __float_as_int(w * f.cw[1]));
-                dst[1] = make_int4(f.row[2], __float_as_int(w * f.cw[2]),
-                                   f.row[3], __float_as_int(w * f.cw[3]));
+            {
+                int row[4] = {-1, -1, -1, -1};
+                float tw[4] = {0.f, 0.f, 0.f, 0.f};
+                if (lane < n) {
+                    const int j = j0 + lane;
+                    const int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k
+                    const int s = j - jk * pb.S;
+                    const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
+                    const float2 xy =
+                        *reinterpret_cast<const float2 *>(pb.loc + (static_cast<int64_t>(ba) * pb.pk + jk) * 2);
+                    const float w = pb.weights[(static_cast<int64_t>(ba) * pb.pks + j) * pb.G + g];
+                    Footprint f;
+                    footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        row[c] = f.row[c];
+                        tw[c] = w * f.cw[c];
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tab[warp][c][lane] = make_int2(row[c], __float_as_int(tw[c]));
             }
             __syncwarp();
 
-            int i = slot;
-            for (; i + 3 * SPP < n; i += 4 * SPP) {
-                int2 e[4];
+            for (int i0 = 0; i0 < n; i0 += 4 * SPP) {
+                const int i = i0 + 4 * slot;
+                const int4 e01 = *reinterpret_cast<const int4 *>(&tab[warp][corner][i]);
+                const int4 e23 = *reinterpret_cast<const int4 *>(&tab[warp][corner][i + 2]);
+                const int r[4] = {e01.x, e01.z, e23.x, e23.z};
+                const float cw[4] = {__int_as_float(e01.y), __int_as_float(e01.w), __int_as_float(e23.y),
+                                     __int_as_float(e23.w)};
                 uint4 raw[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) e[u] = tab[warp][i + u * SPP][corner];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    raw[u] = make_uint4(0u, 0u, 0u, 0u);
-                    if (e[u].x >= 0) raw[u] = ldg16(base + static_cast<int64_t>(e[u].x) * row_bytes);
-                }
+                for (int u = 0; u < 4; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     float v[VEC];
                     Ck::unpack(raw[u], v);
-                    const float cw = __int_as_float(e[u].y);
 #pragma unroll
-                    for (int q = 0; q < VEC; ++q) acc[q] = fmaf(cw, v[q], acc[q]);
+                    for (int q = 0; q < VEC; ++q) acc[q] = fmaf(cw[u], v[q], acc[q]);
                 }
-            }
-            for (; i < n; i += SPP) {
-                const int2 e = tab[warp][i][corner];
-                uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-                if (e.x >= 0) raw = ldg16(base + static_cast<int64_t>(e.x) * row_bytes);
-                float v[VEC];
-                Ck::unpack(raw, v);
-                const float cw = __int_as_float(e.y);
-#pragma unroll
-                for (int q = 0; q < VEC; ++q) acc[q] = fmaf(cw, v[q], acc[q]);
             }
             __syncwarp();
         }
@@ -116,8 +118,8 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
             for (int q = 0; q < VEC; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], m);
         }
         if (lane < CH) {
-            float4 *o = reinterpret_cast<float4 *>(args.out + ba * pb.C + static_cast<int64_t>(g) * pb.D +
-                                                   chunk * VEC);
+            float4 *o = reinterpret_cast<float4 *>(args.out + static_cast<int64_t>(ba) * pb.C +
+                                                   static_cast<int64_t>(g) * pb.D + chunk * VEC);
 #pragma unroll
             for (int q = 0; q < VEC / 4; ++q)
                 o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);

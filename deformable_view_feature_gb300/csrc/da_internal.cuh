@@ -17,8 +17,28 @@ struct MapInfo {
     int32_t H, W, start, pad;
 };
 
+// Division by a runtime divisor d >= 1 through a multiply and a shift:
+// n / d == (n * m) >> sh for every 0 <= n < 2^31, with l = ceil(log2 d),
+// m = ceil(2^(31+l) / d) < 2^32 and sh = 31 + l. It holds because
+// m*d - 2^(31+l) < d <= 2^l, so n*(m*d - 2^(31+l)) < 2^(31+l) and the
+// error term stays below 1/d.
+struct FastDiv {
+    uint32_t d, m, sh;
+    static FastDiv make(uint32_t divisor)
+    {
+        uint32_t l = 0;
+        while ((1ull << l) < divisor) ++l;
+        const uint64_t num = (1ull << (31 + l)) + divisor - 1;
+        return FastDiv{divisor, static_cast<uint32_t>(num / divisor), 31 + l};
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t n) const
+    {
+        return static_cast<uint32_t>((static_cast<uint64_t>(n) * m) >> sh);
+    }
+};
+
 // Everything a sampling kernel needs about the problem. It is passed by value
-// as a kernel parameter, so the map table lives in the constant bank.
+// as a kernel parameter; the kernels copy the map table to shared memory.
 struct Problem {
     const void *feat;
     const float *loc;
@@ -28,7 +48,9 @@ struct Problem {
     int32_t pks;              // P*K*S samples per (b, a, g)
     int32_t pk;               // P*K locations per (b, a)
     int32_t num_ba;           // B*A
-    int32_t anchors_per_cta;  // anchors (all groups) owned by one CTA
+    int32_t anchors_per_cta;  // anchors (or views) owned by one CTA, all groups
+    int32_t nmaps;            // K*S
+    FastDiv div_S, div_K, div_G, div_A;
     MapInfo maps[DA_MAX_MAPS];
 };
 
@@ -113,10 +135,24 @@ __device__ __forceinline__ void footprint(float x, float y, const MapInfo &m, Fo
     f.cw[3] = f.lh * f.lw;
 }
 
-// 16-byte read-only load of one chunk of a feature row.
-__device__ __forceinline__ uint4 ldg16(const void *p)
+// 16-byte read-only load of one chunk of a feature row, or zeros when `pred`
+// is false (then nothing is read, whatever the address).
+__device__ __forceinline__ uint4 ldg16_if(bool pred, const void *p)
 {
-    return __ldg(reinterpret_cast<const uint4 *>(p));
+    uint4 r;
+    asm("{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %5, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "@q ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];\n\t}"
+        : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+        : "l"(p), "r"(static_cast<int>(pred)));
+    return r;
+}
+
+// Address of feature row `row` (>= 0 when used): one 32x32->64 multiply-add.
+__device__ __forceinline__ const char *row_addr(const char *base, int32_t row, uint32_t row_bytes)
+{
+    return base + static_cast<uint64_t>(static_cast<uint32_t>(row)) * row_bytes;
 }
 
 // The 16 bytes as floats: 4 fp32 values, or 8 bf16 values widened exactly.
@@ -153,13 +189,30 @@ struct Chunk<Bf16Tag> {
     }
 };
 
-// Vector reduction of four floats into global memory (sm_90+).
-__device__ __forceinline__ void red_add_v4(float *p, float a, float b, float c, float d)
+// Vector reduction of four floats into global memory (sm_90+), issued only
+// when `pred` holds (no branch; the address is not touched otherwise).
+__device__ __forceinline__ void red_add_v4_if(bool pred, float *p, float a, float b, float c, float d)
 {
-    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+    asm volatile("{\n\t.reg .pred q;\n\t"
+                 "setp.ne.b32 q, %5, 0;\n\t"
+                 "@q red.global.add.v4.f32 [%0], {%1, %2, %3, %4};\n\t}"
                  :
-                 : "l"(p), "f"(a), "f"(b), "f"(c), "f"(d)
+                 : "l"(p), "f"(a), "f"(b), "f"(c), "f"(d), "r"(static_cast<int>(pred))
                  : "memory");
+}
+
+// Per-warp table of the four corners of 32 samples: tab[corner][sample] =
+// {feature row or -1, weight}. Corner-major, so a lane reads the entries of
+// its corner for four consecutive samples with two 16-byte loads. The row
+// pitch of 36 entries (288 B) staggers the four corners by 8 banks, so the
+// four corner groups of a warp read conflict-free.
+constexpr int kTabPitch = 36;
+
+// Stage the map table of the kernel parameters in shared memory: lanes index
+// it with divergent (k, s), which the constant bank would serialise.
+__device__ __forceinline__ void stage_maps(const Problem &pb, MapInfo *maps_s)
+{
+    for (int i = threadIdx.x; i < pb.nmaps; i += blockDim.x) maps_s[i] = pb.maps[i];
 }
 
 }  // namespace da
