@@ -47,6 +47,9 @@ sys.path.insert(0, ROOT)
 import da_inputs  # noqa: E402
 
 METRIC = "fwd+bwd bilinear samples/sec at 6-cam Sparse4D shape; GB/s vs HBM peak"
+# Kernels da_backward launches: binned = row-count zero-fill, count, 3 scan
+# steps, fill, pull, epilogue; scatter = grad_feat zero-fill, gather-scatter.
+BWD_LAUNCHES = {"binned": 8, "scatter": 2}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -252,6 +255,10 @@ def run_ours(a, wl):
     gw = torch.empty(w.shape, device=dev)
     stream = torch.cuda.Stream(device=dev)
     fwd_bytes, bwd_bytes = algorithmic_bytes(inp)
+    ws = None
+    if a.bwd_path == "binned":
+        dims = da._dims(feat, da._host_i32(ss), loc, w)
+        ws = torch.empty(max(da.backward_workspace_size(dims), 256), dtype=torch.uint8, device=dev)
 
     def step(ev=None):
         if ev is not None:
@@ -261,7 +268,7 @@ def run_ours(a, wl):
             ev[1].record(stream)
         if wl.backward:
             da.da_backward(feat, ss, ls, loc, w, go, grad_feat=gf, grad_loc=gl, grad_weight=gw,
-                           stream=stream)
+                           stream=stream, path=a.bwd_path, workspace=ws)
             if ev is not None:
                 ev[2].record(stream)
 
@@ -345,13 +352,15 @@ def run_ours(a, wl):
                                 f"{inp.feat.numel() * inp.feat.element_size() / 1e6:.0f} MB), no flush"),
         "gbs_step": (fwd_bytes + (bwd_bytes if wl.backward else 0)) / (step_ms / 1e3) / 1e9,
         "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms) if bwd_ms else None,
-        "roofline": {"bound": "hbm", "kernel": dom + (" (grad_feat zero-fill + gradient kernel)"
+        "roofline": {"bound": "hbm", "kernel": dom + (f" ({a.bwd_path} path, all its kernels)"
                                                        if dom == "da_backward" else ""),
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
                      "algorithmic_bytes": dom_bytes, "traffic": None},
         "e2e": e2e,
-        "gpu_launches": a.steps * (1 + (2 if wl.backward else 0)),
+        "gpu_launches": a.steps * (1 + (BWD_LAUNCHES[a.bwd_path] if wl.backward else 0)),
+        "bwd_path": a.bwd_path,
+        "workspace_bytes": int(ws.numel()) if ws is not None else 0,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
     if world == 1 and not a.no_cpu_baseline:
@@ -372,6 +381,8 @@ def main():
     ap.add_argument("--ref-anchors", type=int, default=300,
                     help="anchors per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bwd-path", choices=["binned", "scatter"], default="binned",
+                    help="backward algorithm (binned needs a device workspace)")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -20,18 +20,18 @@ from __future__ import annotations
 
 import ctypes
 import os
-from typing import Optional, Sequence, Tuple
+from typing import Optional, Tuple
 
 import torch
 
 from . import build as _build
 
-__all__ = ["da_forward", "da_backward", "DeformableAggregationFunction", "DaError",
-           "library_path", "load_library", "da_version"]
+__all__ = ["da_forward", "da_backward", "backward_workspace_size", "DeformableAggregationFunction",
+           "DaError", "library_path", "load_library", "da_version"]
 
 DA_F32, DA_BF16 = 0, 1
 _STATUS = {0: "DA_OK", 1: "DA_ERR_NULL", 2: "DA_ERR_SHAPE", 3: "DA_ERR_ALIGN",
-           4: "DA_ERR_UNSUPPORTED", 5: "DA_ERR_CUDA"}
+           4: "DA_ERR_UNSUPPORTED", 5: "DA_ERR_CUDA", 6: "DA_ERR_WORKSPACE"}
 
 
 class DaError(RuntimeError):
@@ -70,8 +70,11 @@ def load_library():
     vp = ctypes.c_void_p
     lib.da_forward.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp]
     lib.da_forward.restype = ctypes.c_int
-    lib.da_backward.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+    lib.da_backward.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                ctypes.c_size_t, vp]
     lib.da_backward.restype = ctypes.c_int
+    lib.da_backward_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
+    lib.da_backward_workspace_size.restype = ctypes.c_int
     lib.da_status_string.argtypes = [ctypes.c_int]
     lib.da_status_string.restype = ctypes.c_char_p
     lib.da_last_error.argtypes = []
@@ -157,12 +160,39 @@ def da_forward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
     return out
 
 
+def backward_workspace_size(dims: DaDims) -> int:
+    """Bytes of device scratch the binned backward needs (da_backward_workspace_size)."""
+    n = ctypes.c_size_t(0)
+    _check(load_library().da_backward_workspace_size(ctypes.byref(dims), ctypes.byref(n)))
+    return n.value
+
+
+# One reusable workspace per (device, stream): calls on one stream are ordered,
+# so they may share it.
+_workspaces = {}
+
+
+def _workspace(device: torch.device, stream_handle, nbytes: int) -> torch.Tensor:
+    key = (device.index, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
 def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
                 sampling_location: torch.Tensor, weights: torch.Tensor, grad_out: torch.Tensor,
                 grad_feat: Optional[torch.Tensor] = None, grad_loc: Optional[torch.Tensor] = None,
-                grad_weight: Optional[torch.Tensor] = None,
-                stream=None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
-    """Backward pass; returns (grad_feat fp32, grad_loc, grad_weight)."""
+                grad_weight: Optional[torch.Tensor] = None, stream=None, path: str = "binned",
+                workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+    """Backward pass; returns (grad_feat fp32, grad_loc, grad_weight).
+
+    path="binned" (default) sorts corner contributions by feature row in a
+    device workspace (allocated through torch and reused, or passed in);
+    path="scatter" needs no workspace and scatters grad_feat with vector
+    reductions.
+    """
     lib = load_library()
     ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
     d = _dims(mc_ms_feat, ss, sampling_location, weights)
@@ -180,10 +210,22 @@ def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
                            ("grad_weight", grad_weight, weights.shape)):
         if t.shape != shape or t.dtype != torch.float32:
             raise ValueError(f"{name} must be float32 {tuple(shape)}")
+    sh = _stream_handle(stream)
+    ws_ptr, ws_bytes = None, 0
+    if path == "binned":
+        need = backward_workspace_size(d)
+        if workspace is None:
+            workspace = _workspace(mc_ms_feat.device, sh, need)
+        ws_bytes = workspace.numel() * workspace.element_size()
+        if ws_bytes < need:
+            raise ValueError(f"workspace holds {ws_bytes} bytes; {need} are needed")
+        ws_ptr = _dptr(workspace)
+    elif path != "scatter":
+        raise ValueError("path must be 'binned' or 'scatter'")
     _check(lib.da_backward(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
                            ls.data_ptr() if ls.numel() else None, _dptr(sampling_location),
                            _dptr(weights), _dptr(grad_out), _dptr(grad_feat), _dptr(grad_loc),
-                           _dptr(grad_weight), _stream_handle(stream)))
+                           _dptr(grad_weight), ws_ptr, ws_bytes, sh))
     return grad_feat, grad_loc, grad_weight
 
 

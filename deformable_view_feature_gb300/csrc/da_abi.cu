@@ -104,12 +104,26 @@ da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_
     pb.div_K = da::FastDiv::make(d.num_cams > 0 ? d.num_cams : 1);
     pb.div_G = da::FastDiv::make(d.num_groups);
     pb.div_A = da::FastDiv::make(d.num_anchors > 0 ? d.num_anchors : 1);
+    pb.div_P = da::FastDiv::make(d.num_pts > 0 ? d.num_pts : 1);
+    pb.div_PKS = da::FastDiv::make(pks > 0 ? static_cast<uint32_t>(pks) : 1);
     return DA_OK;
 }
 
 da_status cuda_fail(cudaError_t e, const char *what)
 {
     return fail(DA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Layout of the binned backward's workspace; DA_ERR_UNSUPPORTED when its
+// record indices would not fit in int32.
+da_status binned_layout(const da_dims &d, da::BinLayout &L)
+{
+    L = da::bin_layout(d.batch, d.num_feat_rows, d.num_anchors, d.num_pts, d.num_cams, d.num_scales,
+                       d.num_groups);
+    if (L.ncap > INT32_MAX || L.rows_total + da::kScanTile > INT32_MAX)
+        return fail(DA_ERR_UNSUPPORTED, "binned backward: 4*B*A*P*K*S = %lld or B*rows = %lld exceeds int32",
+                    static_cast<long long>(L.ncap), static_cast<long long>(L.rows_total));
+    return DA_OK;
 }
 
 }  // namespace
@@ -135,10 +149,25 @@ da_status da_forward(const da_dims *dims, const void *mc_ms_feat, const int32_t 
     return DA_OK;
 }
 
+da_status da_backward_workspace_size(const da_dims *dims, size_t *bytes)
+{
+    if (!dims || !bytes) return fail(DA_ERR_NULL, "dims / bytes is NULL");
+    const da_dims d = *dims;
+    if (d.batch < 0 || d.num_cams < 0 || d.num_scales < 0 || d.num_anchors < 0 || d.num_pts < 0 ||
+        d.num_embeds < 1 || d.num_groups < 1 || d.num_embeds % d.num_groups != 0 || d.num_feat_rows < 0 ||
+        d.num_feat_rows > DA_MAX_ROWS)
+        return fail(DA_ERR_SHAPE, "invalid dims");
+    da::BinLayout L;
+    const da_status st = binned_layout(d, L);
+    if (st != DA_OK) return st;
+    *bytes = L.bytes;
+    return DA_OK;
+}
+
 da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
                       const int32_t *level_start_index, const float *sampling_location,
                       const float *weights, const float *grad_out, float *grad_feat, float *grad_loc,
-                      float *grad_weight, da_stream_t stream)
+                      float *grad_weight, void *workspace, size_t workspace_bytes, da_stream_t stream)
 {
     da::BwdArgs a{};
     int chunks = 0;
@@ -170,6 +199,29 @@ da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t
     a.grad_loc = grad_loc;
     a.grad_weight = grad_weight;
     const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (workspace || workspace_bytes) {
+        da::BinLayout L;
+        st = binned_layout(*dims, L);
+        if (st != DA_OK) return st;
+        if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.bytes)
+            return fail(DA_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)",
+                        L.bytes, workspace_bytes);
+        char *ws = static_cast<char *>(workspace);
+        da::BinArgs w{};
+        w.row_off = reinterpret_cast<int32_t *>(ws + L.off_row_off);
+        w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
+        w.rec_cid = reinterpret_cast<int32_t *>(ws + L.off_rec_cid);
+        w.rec_cw = reinterpret_cast<float *>(ws + L.off_rec_cw);
+        w.pos4 = reinterpret_cast<int32_t *>(ws + L.off_pos4);
+        w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
+        w.rows_total = L.rows_total;
+        w.nsid = L.nsid;
+        w.ncap = L.ncap;
+        w.ntiles = L.ntiles;
+        const cudaError_t e = da::launch_backward_binned(a, w, dims->feat_dtype, s);
+        if (e != cudaSuccess) return cuda_fail(e, "binned backward launch");
+        return DA_OK;
+    }
     cudaError_t e = da::launch_zero_fill(grad_feat, n_gf, s);
     if (e != cudaSuccess) return cuda_fail(e, "grad_feat zero-fill");
     if (n_out == 0) return DA_OK;
@@ -187,6 +239,7 @@ const char *da_status_string(da_status status)
         case DA_ERR_ALIGN: return "DA_ERR_ALIGN";
         case DA_ERR_UNSUPPORTED: return "DA_ERR_UNSUPPORTED";
         case DA_ERR_CUDA: return "DA_ERR_CUDA";
+        case DA_ERR_WORKSPACE: return "DA_ERR_WORKSPACE";
     }
     return "DA_ERR_UNKNOWN";
 }

@@ -50,7 +50,7 @@ struct Problem {
     int32_t num_ba;           // B*A
     int32_t anchors_per_cta;  // anchors (or views) owned by one CTA, all groups
     int32_t nmaps;            // K*S
-    FastDiv div_S, div_K, div_G, div_A;
+    FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS;
     MapInfo maps[DA_MAX_MAPS];
 };
 
@@ -67,9 +67,42 @@ struct BwdArgs {
     float *grad_weight;
 };
 
+// Device scratch of the binned backward, carved out of one caller-provided
+// buffer. Every region starts on a 256-byte boundary.
+//   row_off  [ntiles*kScanTile + 4] int32: per feature row (over all B*rows
+//            rows): the corner count, then its exclusive prefix sum, then
+//            (after the fill) the end of the row's record range
+//   tile_sum [ntiles + 4] int32: per-tile totals of the scan
+//   rec_cid  [ncap] int32: sample id * 4 + corner, grouped by feature row
+//   rec_cw   [ncap] fp32: the corner's bilinear weight
+//   pos4     [nsid * 4] int32: record index of each (sample, corner), or -1
+//   dpix     [G * ncap] fp32: d = grad_out . feat of each (record, group)
+// A sample id here is ((b*A + a)*P + p)*K + k)*S + s: a sample of all groups.
+constexpr int kScanTile = 4096;
+
+struct BinLayout {
+    int64_t rows_total;  // B * rows
+    int64_t nsid;        // B*A*P*K*S
+    int64_t ncap;        // 4 * nsid
+    int64_t ntiles;
+    size_t off_row_off, off_tile_sum, off_rec_cid, off_rec_cw, off_pos4, off_dpix, bytes;
+};
+BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, int64_t S, int64_t G);
+
+struct BinArgs {
+    int32_t *row_off;
+    int32_t *tile_sum;
+    int32_t *rec_cid;
+    float *rec_cw;
+    int32_t *pos4;
+    float *dpix;
+    int64_t rows_total, nsid, ncap, ntiles;
+};
+
 // `chunks` = D * sizeof(feature) / 16, one of 1, 2, 4, 8.
 cudaError_t launch_forward(const FwdArgs &a, int feat_dtype, int chunks, cudaStream_t st);
 cudaError_t launch_backward(const BwdArgs &a, int feat_dtype, int chunks, cudaStream_t st);
+cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st);
 cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st);
 
 // Grid size that covers num_ba anchors, anchors_per_cta at a time.

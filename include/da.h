@@ -46,6 +46,7 @@
 #ifndef DA_H_
 #define DA_H_
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -61,7 +62,8 @@ typedef enum da_status {
     DA_ERR_SHAPE = 2,       /* sizes negative, inconsistent, or a map outside the feature rows */
     DA_ERR_ALIGN = 3,       /* a pointer is not aligned as required below */
     DA_ERR_UNSUPPORTED = 4, /* valid sizes this build has no kernel for (see da_forward) */
-    DA_ERR_CUDA = 5         /* a CUDA launch or runtime call failed */
+    DA_ERR_CUDA = 5,        /* a CUDA launch or runtime call failed */
+    DA_ERR_WORKSPACE = 6    /* workspace too small or not 256-byte aligned */
 } da_status;
 
 typedef enum da_dtype {
@@ -117,6 +119,16 @@ da_status da_forward(const da_dims *dims,
                      da_stream_t stream);
 
 /*
+ * Size in bytes of the device workspace that the binned path of da_backward
+ * needs for `dims` (stored in *bytes). It depends on the sizes only:
+ * about 4*B*A*P*K*S*(12 + 4*G) bytes plus 4 bytes per feature row. This is
+ * about 300 MB for B=6, A=900, P=13, K=6, S=4, G=8.
+ * Returns DA_ERR_UNSUPPORTED when 4*B*A*P*K*S or B*num_feat_rows does not
+ * fit in int32. The scatter path (no workspace) still serves such sizes.
+ */
+da_status da_backward_workspace_size(const da_dims *dims, size_t *bytes);
+
+/*
  * Backward pass: the three gradients of page §4.1, for a loss L with
  * dL/d out = grad_out.
  *
@@ -124,14 +136,23 @@ da_status da_forward(const da_dims *dims,
  *   grad_out    device [B, A, C] fp32, 16-byte aligned.
  *   grad_feat   device [B, num_feat_rows, C] fp32 for both feature types,
  *               16-byte aligned; overwritten. Rows outside every map get 0.
- *               The scatter-add order is unspecified, so the bits may differ
- *               from run to run.
+ *               Contributions are summed in an unspecified order, so the
+ *               bits may differ from run to run.
  *   grad_loc    device [B, A, P, K, 2] fp32, 4-byte aligned; overwritten.
  *               [...,0] is dL/dx (scaled by W), [...,1] is dL/dy (scaled by H).
  *   grad_weight device [B, A, P, K, S, G] fp32, 4-byte aligned; overwritten.
+ *   workspace   device scratch of at least da_backward_workspace_size bytes,
+ *               256-byte aligned, owned by the caller and not read
+ *               afterwards; or NULL with workspace_bytes = 0.
  *
- * The call zero-fills grad_feat and then scatters into it. grad_loc and
- * grad_weight are written exactly once per element.
+ * With a workspace (the binned path), the corner contributions are sorted by
+ * feature row, and every grad_feat row is computed once by the lanes that
+ * own it. There is no zero-fill and no atomic scatter.
+ * Without one (the scatter path), grad_feat is zero-filled and then scattered
+ * into with 16-byte vector reductions. That path is slower at large sizes
+ * but needs no scratch.
+ * Both paths write grad_loc and grad_weight exactly once per element.
+ * Calls that share one workspace must not overlap on the GPU.
  */
 da_status da_backward(const da_dims *dims,
                       const void *mc_ms_feat,
@@ -143,6 +164,8 @@ da_status da_backward(const da_dims *dims,
                       float *grad_feat,
                       float *grad_loc,
                       float *grad_weight,
+                      void *workspace,
+                      size_t workspace_bytes,
                       da_stream_t stream);
 
 /* Static name of a status code. */

@@ -79,9 +79,10 @@ def _fwd(lib, dims, ss=None, ls=None, feat=FAKE, loc=FAKE, w=FAKE, out=FAKE):
                           out, None)
 
 
-def _bwd(lib, dims, feat=FAKE, loc=FAKE, w=FAKE, go=FAKE, gf=FAKE, gl=FAKE, gw=FAKE):
+def _bwd(lib, dims, feat=FAKE, loc=FAKE, w=FAKE, go=FAKE, gf=FAKE, gl=FAKE, gw=FAKE, ws=None,
+         ws_bytes=0):
     ss, ls = _tables()
-    return lib.da_backward(ctypes.byref(dims), feat, ss, ls, loc, w, go, gf, gl, gw, None)
+    return lib.da_backward(ctypes.byref(dims), feat, ss, ls, loc, w, go, gf, gl, gw, ws, ws_bytes, None)
 
 
 def test_null_dims(lib):
@@ -139,6 +140,24 @@ def test_misaligned_pointers(lib):
     assert _bwd(lib, _dims(), gf=FAKE + 8) == DA_ERR_ALIGN
     assert _bwd(lib, _dims(), gl=FAKE + 2) == DA_ERR_ALIGN
     assert _bwd(lib, _dims(), gw=FAKE + 1) == DA_ERR_ALIGN
+
+
+def test_workspace_size_and_errors(lib):
+    n = ctypes.c_size_t(0)
+    d = _dims(batch=6, num_cams=6, num_scales=4, num_embeds=256, num_groups=8, num_anchors=900,
+              num_pts=13, num_feat_rows=6 * 14960)
+    assert lib.da_backward_workspace_size(ctypes.byref(d), ctypes.byref(n)) == DA_OK
+    nsid = 6 * 900 * 13 * 6 * 4
+    # records (cid + weight), pos4, dpix for 8 groups: 4*nsid*(4+4) + 16*nsid + 4*nsid*8*4
+    assert n.value >= nsid * (32 + 16 + 128)
+    assert n.value < nsid * (32 + 16 + 128) + 8 * 1024 * 1024
+    assert lib.da_backward_workspace_size(None, ctypes.byref(n)) == DA_ERR_NULL
+    big = _dims(batch=1 << 20, num_anchors=1 << 10, num_pts=4)
+    assert lib.da_backward_workspace_size(ctypes.byref(big), ctypes.byref(n)) == DA_ERR_UNSUPPORTED
+    # too small / misaligned workspace: rejected before any launch
+    assert _bwd(lib, _dims(), ws=FAKE, ws_bytes=16) == 6
+    assert _bwd(lib, _dims(), ws=FAKE + 16, ws_bytes=1 << 30) == 6
+    assert lib.da_status_string(6) == b"DA_ERR_WORKSPACE"
 
 
 def test_empty_problem_needs_no_pointers(lib):

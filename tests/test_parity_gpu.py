@@ -29,7 +29,10 @@ def da():
     return m
 
 
-def _run_gpu(da, inp, backward=True, stream=None):
+PATHS = ("binned", "scatter")
+
+
+def _run_gpu(da, inp, backward=True, stream=None, path="binned"):
     dev = torch.device("cuda")
     feat = inp.feat.to(dev)
     loc = inp.loc.to(dev)
@@ -39,7 +42,7 @@ def _run_gpu(da, inp, backward=True, stream=None):
     if backward:
         go = inp.grad_out.to(dev)
         gf, gl, gw = da.da_backward(feat, inp.spatial_shape, inp.level_start_index, loc, w, go,
-                                    stream=stream)
+                                    stream=stream, path=path)
         res.update(grad_feat=gf, grad_loc=gl, grad_weight=gw)
     torch.cuda.synchronize()
     return {k: to_np(v) for k, v in res.items()}
@@ -59,14 +62,27 @@ def _compare(inp, got, ref):
     assert not msgs, f"{inp.wl.name}: " + " | ".join(msgs)
 
 
+@pytest.fixture(scope="module")
+def full_refs():
+    """Oracle results of the five workloads, computed once per module."""
+    cache = {}
+
+    def get(name):
+        if name not in cache:
+            inp = da_inputs.make_inputs(name)
+            backward = inp.wl.backward or name == "sp4d_inf"
+            cache[name] = (inp, backward, oracle.run_inputs(inp, backward_pass=backward))
+        return cache[name]
+    return get
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("name", da_inputs.WORKLOAD_ORDER)
-def test_parity_full_size(da, name):
-    inp = da_inputs.make_inputs(name)
-    backward = inp.wl.backward or name == "sp4d_inf"
-    got = _run_gpu(da, inp, backward=backward)
-    ref = oracle.run_inputs(inp, backward_pass=backward)
+def test_parity_full_size(da, full_refs, name, path):
+    inp, backward, ref = full_refs(name)
+    got = _run_gpu(da, inp, backward=backward, path=path)
     for k in ref:
-        print(f"{name}.{k}: max_rel={max_rel(got[k], ref[k]):.3e}")
+        print(f"{name}[{path}].{k}: max_rel={max_rel(got[k], ref[k]):.3e}")
     _compare(inp, got, ref)
 
 
@@ -106,30 +122,47 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", CASES, ids=[f"case{c[0]}" for c in CASES])
-def test_parity_shapes(da, case):
+def test_parity_shapes(da, case, path):
     seed, shapes, B, C, G, A, P, dt = case
     inp = _custom(seed, shapes, B, C, G, A, P, dt)
-    got = _run_gpu(da, inp)
+    got = _run_gpu(da, inp, path=path)
     ref = oracle.run_inputs(inp)
     _compare(inp, got, ref)
 
 
+def test_binned_skewed_locations(da):
+    """Many samples on a few pixels (long per-row record lists, uneven row
+    ranges across CTAs) and anchors with no in-map corner at all."""
+    inp = _custom(25, [[(12, 14), (6, 7)], [(9, 9), (3, 3)]], 2, 64, 2, 40, 9)
+    loc = inp.loc.clone()
+    loc[:, :20] = 0.31  # half of the anchors sample one spot in every map
+    loc[:, 20:24] = 7.0  # outside every map
+    inp.loc = loc
+    for path in PATHS:
+        got = _run_gpu(da, inp, path=path)
+        ref = oracle.run_inputs(inp)
+        _compare(inp, got, ref)
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("B,A,P", [(0, 5, 3), (2, 0, 3), (2, 5, 0)])
-def test_empty(da, B, A, P):
+def test_empty(da, B, A, P, path):
     inp = _custom(20, [[(6, 7)]], max(B, 1), 32, 2, max(A, 1), max(P, 1))
     inp.feat = inp.feat[:B].contiguous()
     inp.loc = inp.loc[:B, :A, :P].contiguous()
     inp.weights = inp.weights[:B, :A, :P].contiguous()
     inp.grad_out = inp.grad_out[:B, :A].contiguous()
-    got = _run_gpu(da, inp)
+    got = _run_gpu(da, inp, path=path)
     assert got["out"].shape == (B, A, 32) and np.all(got["out"] == 0)
     assert got["grad_feat"].shape == tuple(inp.feat.shape) and np.all(got["grad_feat"] == 0)
     assert got["grad_loc"].shape == tuple(inp.loc.shape) and np.all(got["grad_loc"] == 0)
     assert got["grad_weight"].shape == tuple(inp.weights.shape)
 
 
-def test_nonfinite_and_far_locations(da):
+@pytest.mark.parametrize("path", PATHS)
+def test_nonfinite_and_far_locations(da, path):
     inp = _custom(21, [[(6, 7), (3, 3)]], 1, 32, 2, 8, 4)
     loc = inp.loc.clone()
     loc[0, 0, 0, 0, 0] = float("nan")
@@ -139,12 +172,13 @@ def test_nonfinite_and_far_locations(da):
     loc[0, 4, :, 0, :] = -1e30
     loc[0, 5, 0, 0, :] = torch.tensor([-0.49, 1.49])
     inp.loc = loc
-    got = _run_gpu(da, inp)
+    got = _run_gpu(da, inp, path=path)
     ref = oracle.run_inputs(inp)
     _compare(inp, got, ref)
 
 
-def test_output_guard_bands(da):
+@pytest.mark.parametrize("path", PATHS)
+def test_output_guard_bands(da, path):
     """Outputs are written in place inside NaN-filled buffers: nothing outside
     the tensor may change."""
     inp = _custom(22, [[(9, 10), (4, 5)]], 2, 64, 4, 9, 5)
@@ -163,7 +197,7 @@ def test_output_guard_bands(da):
     wb, gw = guarded(tuple(w.shape))
     da.da_forward(feat, inp.spatial_shape, inp.level_start_index, loc, w, out=out)
     da.da_backward(feat, inp.spatial_shape, inp.level_start_index, loc, w, go,
-                   grad_feat=gf, grad_loc=gl, grad_weight=gw)
+                   grad_feat=gf, grad_loc=gl, grad_weight=gw, path=path)
     torch.cuda.synchronize()
     for buf in (ob, fb, lb, wb):
         assert torch.isnan(buf[:pad]).all() and torch.isnan(buf[-pad:]).all()
