@@ -184,14 +184,14 @@ def _workspace(device: torch.device, stream_handle, nbytes: int) -> torch.Tensor
 def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
                 sampling_location: torch.Tensor, weights: torch.Tensor, grad_out: torch.Tensor,
                 grad_feat: Optional[torch.Tensor] = None, grad_loc: Optional[torch.Tensor] = None,
-                grad_weight: Optional[torch.Tensor] = None, stream=None, path: str = "binned",
+                grad_weight: Optional[torch.Tensor] = None, stream=None, path: str = "scatter",
                 workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Backward pass; returns (grad_feat fp32, grad_loc, grad_weight).
 
-    path="binned" (default) sorts corner contributions by feature row in a
-    device workspace (allocated through torch and reused, or passed in);
-    path="scatter" needs no workspace and scatters grad_feat with vector
-    reductions.
+    path="scatter" (default) needs no workspace and scatters grad_feat with
+    vector reductions; path="binned" sorts the corner contributions by
+    feature row in a device workspace (allocated through torch and reused, or
+    passed in) and writes every grad_feat row once.
     """
     lib = load_library()
     ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
