@@ -10,8 +10,15 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 
 #include "da_internal.cuh"
+
+// Scratch of da_backward_noalloc: a fixed array in device memory, present
+// on every device that loads the library. In host code its name only stands
+// in for it; the device address comes from cudaGetSymbolAddress, looked up
+// once per device with that device current.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[DA_NOALLOC_SCRATCH_BYTES];
 
 namespace {
 
@@ -126,6 +133,28 @@ da_status binned_layout(const da_dims &d, da::BinLayout &L)
     return DA_OK;
 }
 
+// Device address of g_noalloc_scratch on the current device.
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+
+da_status noalloc_scratch(void **out)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(DA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    if (!g_noalloc_ptr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return DA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -228,6 +257,26 @@ da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t
     e = da::launch_backward(a, dims->feat_dtype, chunks, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return DA_OK;
+}
+
+da_status da_backward_noalloc(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                              const int32_t *level_start_index, const float *sampling_location,
+                              const float *weights, const float *grad_out, float *grad_feat, float *grad_loc,
+                              float *grad_weight, da_stream_t stream)
+{
+    size_t need = 0;
+    da_status st = da_backward_workspace_size(dims, &need);
+    if (st != DA_OK) return st;
+    if (need > DA_NOALLOC_SCRATCH_BYTES)
+        return fail(DA_ERR_WORKSPACE,
+                    "da_backward_noalloc: this problem needs %zu bytes of scratch; the built-in array holds %u "
+                    "(use da_backward with a workspace)",
+                    need, DA_NOALLOC_SCRATCH_BYTES);
+    void *scratch = nullptr;
+    st = noalloc_scratch(&scratch);
+    if (st != DA_OK) return st;
+    return da_backward(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location, weights, grad_out,
+                       grad_feat, grad_loc, grad_weight, scratch, DA_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 const char *da_status_string(da_status status)

@@ -168,6 +168,47 @@ da_status da_backward(const da_dims *dims,
                       size_t workspace_bytes,
                       da_stream_t stream);
 
+/*
+ * da_backward_noalloc: the binned backward, with its scratch in a fixed
+ * array of DA_NOALLOC_SCRATCH_BYTES that the library carries in device
+ * memory. No call allocates anything.
+ *
+ * The pages have no counterpart to this entry point. It exists for callers
+ * that cannot call cudaMalloc. Examples: a runtime that fixes its device
+ * memory at start-up and forbids later allocation; a plug-in whose host
+ * framework owns all device memory and hands it no allocator; code that
+ * cannot accept the device-wide synchronisation an allocation may cause.
+ * They still pass their own inputs and outputs, exactly as for da_backward.
+ *
+ * Arguments, layouts and results are those of da_backward. Rules:
+ *   - The scratch array exists once per device that loads the library and is
+ *     held until the process exits.
+ *   - The first call on a device looks up the array's device address (a
+ *     one-time set-up per device). Make that first call before any stream
+ *     capture.
+ *   - Problems whose workspace (da_backward_workspace_size) exceeds
+ *     DA_NOALLOC_SCRATCH_BYTES are rejected with DA_ERR_WORKSPACE. The limit
+ *     fits e.g. the 6-camera Sparse4D shape at B = 1 (about 50 MB); the
+ *     B = 6 training shape needs about 300 MB and must use da_backward.
+ *   - Every call uses the same array. Each call clears what must start at
+ *     zero, so a call does not depend on what the last one left there.
+ *   - Calls that overlap on the GPU (on different streams, or from
+ *     different threads without ordering) race on the array and give wrong
+ *     results. Order them on one stream.
+ */
+#define DA_NOALLOC_SCRATCH_BYTES (64u << 20)
+da_status da_backward_noalloc(const da_dims *dims,
+                              const void *mc_ms_feat,
+                              const int32_t *spatial_shape,
+                              const int32_t *level_start_index,
+                              const float *sampling_location,
+                              const float *weights,
+                              const float *grad_out,
+                              float *grad_feat,
+                              float *grad_loc,
+                              float *grad_weight,
+                              da_stream_t stream);
+
 /* Static name of a status code. */
 const char *da_status_string(da_status status);
 
