@@ -381,7 +381,7 @@ def main():
     ap.add_argument("--ref-anchors", type=int, default=300,
                     help="anchors per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--bwd-path", choices=["binned", "scatter"], default="scatter",
+    ap.add_argument("--bwd-path", choices=["binned", "scatter"], default="binned",
                     help="backward algorithm (binned needs a device workspace)")
     a = ap.parse_args()
     if a.warmup < 3:

@@ -113,6 +113,7 @@ da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_
     pb.div_A = da::FastDiv::make(d.num_anchors > 0 ? d.num_anchors : 1);
     pb.div_P = da::FastDiv::make(d.num_pts > 0 ? d.num_pts : 1);
     pb.div_PKS = da::FastDiv::make(pks > 0 ? static_cast<uint32_t>(pks) : 1);
+    pb.div_rows = da::FastDiv::make(d.num_feat_rows > 0 ? static_cast<uint32_t>(d.num_feat_rows) : 1);
     return DA_OK;
 }
 
@@ -130,6 +131,11 @@ da_status binned_layout(const da_dims &d, da::BinLayout &L)
     if (L.ncap > INT32_MAX || L.rows_total + da::kScanTile > INT32_MAX)
         return fail(DA_ERR_UNSUPPORTED, "binned backward: 4*B*A*P*K*S = %lld or B*rows = %lld exceeds int32",
                     static_cast<long long>(L.ncap), static_cast<long long>(L.rows_total));
+    if (!da::binned_supported(d.num_embeds, d.num_embeds / d.num_groups))
+        return fail(DA_ERR_UNSUPPORTED,
+                    "binned backward: needs num_embeds a power of two in [8, 256] and num_embeds/num_groups "
+                    "a multiple of 8 (got %d, %d)",
+                    d.num_embeds, d.num_embeds / d.num_groups);
     return DA_OK;
 }
 
@@ -239,8 +245,7 @@ da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t
         da::BinArgs w{};
         w.row_off = reinterpret_cast<int32_t *>(ws + L.off_row_off);
         w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
-        w.rec_cid = reinterpret_cast<int32_t *>(ws + L.off_rec_cid);
-        w.rec_cw = reinterpret_cast<float *>(ws + L.off_rec_cw);
+        w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
         w.pos4 = reinterpret_cast<int32_t *>(ws + L.off_pos4);
         w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
         w.rows_total = L.rows_total;

@@ -15,13 +15,19 @@
 //     the samples of slot l / (4*CH). So one warp-wide 16-byte load reads the
 //     four corner rows of 8/CH samples, every row as one coalesced segment
 //     (the vectorised channel-last access of the DCNv4 page, "Solving the
-//     problem: 2. let the GPU move less data"). Each lane walks four
-//     consecutive samples per step, so four loads are in flight per lane.
-//     Their table entries arrive in two 16-byte shared loads.
+//     problem: 2. let the GPU move less data"). Each lane walks U consecutive
+//     samples per step, so U loads are in flight per lane. Their table
+//     entries arrive in U/2 16-byte shared loads.
 //   * Each lane accumulates its chunk in fp32 registers. At the end, shuffles
 //     sum over corners and slots, and the CH lanes of slot 0 write the group's
 //     D outputs with 16-byte stores. No atomics: the result is deterministic.
 #include "da_internal.cuh"
+
+// Samples a lane walks per step (loads in flight per lane), at most 32 per
+// warp-wide step.
+#ifndef DA_FWD_UNROLL
+#define DA_FWD_UNROLL 8
+#endif
 
 namespace da {
 namespace {
@@ -33,6 +39,8 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     constexpr int VEC = Ck::kVec;   // channels per 16-byte chunk
     constexpr int ESZ = 16 / VEC;   // bytes per feature element
     constexpr int SPP = 8 / CH;     // samples per warp-wide load
+    // Samples per lane per step; a warp-wide step covers U * SPP <= 32.
+    constexpr int U = DA_FWD_UNROLL * SPP <= 32 ? DA_FWD_UNROLL : 32 / SPP;
     const Problem &pb = args.pb;
 
     __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
@@ -89,18 +97,23 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
             }
             __syncwarp();
 
-            for (int i0 = 0; i0 < n; i0 += 4 * SPP) {
-                const int i = i0 + 4 * slot;
-                const int4 e01 = *reinterpret_cast<const int4 *>(&tab[warp][corner][i]);
-                const int4 e23 = *reinterpret_cast<const int4 *>(&tab[warp][corner][i + 2]);
-                const int r[4] = {e01.x, e01.z, e23.x, e23.z};
-                const float cw[4] = {__int_as_float(e01.y), __int_as_float(e01.w), __int_as_float(e23.y),
-                                     __int_as_float(e23.w)};
-                uint4 raw[4];
+            for (int i0 = 0; i0 < n; i0 += U * SPP) {
+                const int i = i0 + U * slot;
+                int r[U];
+                float cw[U];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
+                for (int h = 0; h < U / 2; ++h) {
+                    const int4 e = *reinterpret_cast<const int4 *>(&tab[warp][corner][i + 2 * h]);
+                    r[2 * h] = e.x;
+                    cw[2 * h] = __int_as_float(e.y);
+                    r[2 * h + 1] = e.z;
+                    cw[2 * h + 1] = __int_as_float(e.w);
+                }
+                uint4 raw[U];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
+                for (int u = 0; u < U; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
                     float v[VEC];
                     Ck::unpack(raw[u], v);
 #pragma unroll

@@ -50,7 +50,7 @@ struct Problem {
     int32_t num_ba;           // B*A
     int32_t anchors_per_cta;  // anchors (or views) owned by one CTA, all groups
     int32_t nmaps;            // K*S
-    FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS;
+    FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS, div_rows;
     MapInfo maps[DA_MAX_MAPS];
 };
 
@@ -73,10 +73,10 @@ struct BwdArgs {
 //            rows): the corner count, then its exclusive prefix sum, then
 //            (after the fill) the end of the row's record range
 //   tile_sum [ntiles + 4] int32: per-tile totals of the scan
-//   rec_cid  [ncap] int32: sample id * 4 + corner, grouped by feature row
-//   rec_cw   [ncap] fp32: the corner's bilinear weight
+//   rec      [ncap] int2: {sample id * 4 + corner, corner weight bits},
+//            grouped by feature row
 //   pos4     [nsid * 4] int32: record index of each (sample, corner), or -1
-//   dpix     [G * ncap] fp32: d = grad_out . feat of each (record, group)
+//   dpix     [ncap * G] fp32: d = grad_out . feat of each (record, group)
 // A sample id here is ((b*A + a)*P + p)*K + k)*S + s: a sample of all groups.
 constexpr int kScanTile = 4096;
 
@@ -85,15 +85,22 @@ struct BinLayout {
     int64_t nsid;        // B*A*P*K*S
     int64_t ncap;        // 4 * nsid
     int64_t ntiles;
-    size_t off_row_off, off_tile_sum, off_rec_cid, off_rec_cw, off_pos4, off_dpix, bytes;
+    size_t off_row_off, off_tile_sum, off_rec, off_pos4, off_dpix, bytes;
 };
 BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, int64_t S, int64_t G);
+
+// Whether the binned backward has a kernel for these channel counts: C in
+// {8, 16, ..., 256} (a power of two times 8, at most one warp per row) and
+// D a multiple of 8.
+inline bool binned_supported(int C, int D)
+{
+    return C >= 8 && C <= 256 && (C & (C - 1)) == 0 && D % 8 == 0;
+}
 
 struct BinArgs {
     int32_t *row_off;
     int32_t *tile_sum;
-    int32_t *rec_cid;
-    float *rec_cw;
+    int2 *rec;
     int32_t *pos4;
     float *dpix;
     int64_t rows_total, nsid, ncap, ntiles;

@@ -124,7 +124,9 @@ da_status da_forward(const da_dims *dims,
  * about 4*B*A*P*K*S*(12 + 4*G) bytes plus 4 bytes per feature row. This is
  * about 300 MB for B=6, A=900, P=13, K=6, S=4, G=8.
  * Returns DA_ERR_UNSUPPORTED when 4*B*A*P*K*S or B*num_feat_rows does not
- * fit in int32. The scatter path (no workspace) still serves such sizes.
+ * fit in int32. It also returns DA_ERR_UNSUPPORTED unless C is a power of
+ * two in [8, 256] and D is a multiple of 8. The scatter path (no workspace)
+ * still serves such sizes.
  */
 da_status da_backward_workspace_size(const da_dims *dims, size_t *bytes);
 
