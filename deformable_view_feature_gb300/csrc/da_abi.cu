@@ -66,8 +66,9 @@ da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_
 
     const int64_t num_ba = static_cast<int64_t>(d.batch) * d.num_anchors;
     const int64_t pks = static_cast<int64_t>(d.num_pts) * nmaps;
-    if (num_ba > INT32_MAX || pks > INT32_MAX || static_cast<int64_t>(d.num_pts) * d.num_cams > INT32_MAX)
-        return fail(DA_ERR_UNSUPPORTED, "batch*anchors or pts*cams*scales exceeds int32");
+    if (num_ba > INT32_MAX || pks > INT32_MAX || num_ba * d.num_cams > INT32_MAX ||
+        static_cast<int64_t>(d.num_pts) * d.num_cams > INT32_MAX)
+        return fail(DA_ERR_UNSUPPORTED, "batch*anchors*cams or pts*cams*scales exceeds int32");
 
     if (nmaps > 0 && (!spatial_shape || !level_start_index))
         return fail(DA_ERR_NULL, "spatial_shape / level_start_index is NULL");
@@ -222,10 +223,8 @@ da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t
     if (!aligned(grad_feat, 16)) return fail(DA_ERR_ALIGN, "grad_feat must be 16-byte aligned");
     if (!aligned(grad_loc, 4)) return fail(DA_ERR_ALIGN, "grad_loc must be 4-byte aligned");
     if (!aligned(grad_weight, 4)) return fail(DA_ERR_ALIGN, "grad_weight must be 4-byte aligned");
-    // The backward walks (b, k, a) views; the grid must cover them, and the
-    // per-CTA grad_loc staging area must fit in shared memory.
-    if (static_cast<int64_t>(pb.num_ba) * pb.K > INT32_MAX)
-        return fail(DA_ERR_UNSUPPORTED, "batch*anchors*cams exceeds int32");
+    // The per-CTA grad_loc staging area of the scatter path must fit in
+    // shared memory.
     const int64_t smem = static_cast<int64_t>(pb.anchors_per_cta) * pb.P * 2 * 4;
     if (smem > 200 * 1024)
         return fail(DA_ERR_UNSUPPORTED, "num_pts = %d too large for the grad_loc staging area", pb.P);

@@ -320,32 +320,44 @@ __global__ void __launch_bounds__(kPullThreads) pull_kernel(const PullArgs args)
     float *dp = w.dpix + static_cast<int64_t>(jb) * pb.G + g;
 
     for (int k0 = 0; k0 < nmax; k0 += 4) {
-        // Every lane decodes the four records itself (the loads of a row's
-        // lanes hit the same addresses), so the four records' load chains
-        // stay independent of each other.
-        int a[4];
+        // Every lane decodes the four records itself (the lanes of a row load
+        // the same addresses). The four record loads issue together, then the
+        // four weight loads, then the grad_out rows: three waits per batch of
+        // four records, not twelve.
+        int2 r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) r[u] = (k0 + u < n) ? __ldg(&w.rec[jb + k0 + u]) : make_int2(0, 0);
         float tw[4];
+        const float *gp[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            a[u] = 0;
-            tw[u] = 0.f;
-            if (k0 + u < n) {
-                const int2 r = __ldg(&w.rec[jb + k0 + u]);
-                const int sid = r.x >> 2;
-                a[u] = static_cast<int>(pb.div_PKS.div(sid)) - abase;
-                tw[u] = __int_as_float(r.y) * __ldg(&pb.weights[static_cast<int64_t>(sid) * pb.G + g]);
-            }
+            const int sid = r[u].x >> 2;
+            const int a = static_cast<int>(pb.div_PKS.div(sid)) - abase;
+            const bool valid = k0 + u < n;
+            const float wt = valid ? __ldg(&pb.weights[static_cast<int64_t>(sid) * pb.G + g]) : 0.f;
+            tw[u] = __int_as_float(r[u].y) * wt;
+            gp[u] = go_b + static_cast<int64_t>(valid ? a : 0) * pb.C;
         }
         float d[4];
+        if (RPW == 1 && k0 + 4 <= n) {  // a full batch, the same for the whole warp
+            float4 x[4], y[4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-            if (k0 + u < n) {
-                const float4 *gp = reinterpret_cast<const float4 *>(go_b + static_cast<int64_t>(a[u]) * pb.C);
-                x = __ldg(gp);
-                y = __ldg(gp + 1);
+            for (int u = 0; u < 4; ++u) {
+                x[u] = __ldg(reinterpret_cast<const float4 *>(gp[u]));
+                y[u] = __ldg(reinterpret_cast<const float4 *>(gp[u]) + 1);
             }
-            d[u] = record_fma(v, x, y, tw[u], acc);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) d[u] = record_fma(v, x[u], y[u], tw[u], acc);
+        } else {
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+                if (k0 + u < n) {
+                    x = __ldg(reinterpret_cast<const float4 *>(gp[u]));
+                    y = __ldg(reinterpret_cast<const float4 *>(gp[u]) + 1);
+                }
+                d[u] = record_fma(v, x, y, tw[u], acc);
+            }
         }
         group_sum_store<LPG>(d, gsub, n - k0, dp + static_cast<int64_t>(k0) * pb.G, pb.G);
     }

@@ -81,9 +81,9 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                     const int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k
                     const int s = j - jk * pb.S;
                     const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
-                    const float2 xy =
-                        *reinterpret_cast<const float2 *>(pb.loc + (static_cast<int64_t>(ba) * pb.pk + jk) * 2);
-                    const float w = pb.weights[(static_cast<int64_t>(ba) * pb.pks + j) * pb.G + g];
+                    const int64_t locid = static_cast<int64_t>(ba) * pb.pk + jk;  // (b,a,p,k)
+                    const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + locid * 2);
+                    const float w = pb.weights[(locid * pb.S + s) * pb.G + g];
                     Footprint f;
                     footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
 #pragma unroll
