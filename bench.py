@@ -49,9 +49,9 @@ import da_inputs  # noqa: E402
 METRIC = "fwd+bwd bilinear samples/sec at 6-cam Sparse4D shape; GB/s vs HBM peak"
 
 # DRAM bytes per call (dram__bytes_read.sum + dram__bytes_write.sum, summed over
-# the call's kernels) from one ncu capture of this bench at sp4d_train; see
-# profiles/kernels_sp4d_train.md. They describe the kernels whose sources hash
-# to "digest" and are reported as null once the sources change.
+# the call's kernels), from one ncu capture of this bench at sp4d_train. They
+# describe the kernels whose sources hash to "digest", and are reported as null
+# once the sources change.
 NCU_TRAFFIC = {
     "digest": "093ff1202a8b591a",
     "workload": "sp4d_train",
