@@ -193,12 +193,20 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """Largest x over all ranks (a CUDA tensor under NCCL, a CPU one under gloo)."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], device="cuda", dtype=torch.float64)
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], device=dev, dtype=torch.float64)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(samples_per_rank_step: int, steps: int, world: int, ms_max: float) -> float:
+    """Whole-job samples/s: every rank runs its own replica of the workload,
+    and the job's time is the slowest rank's."""
+    return samples_per_rank_step * steps * world / (ms_max / 1e3)
 
 
 # ----------------------------------------------------------------------------- CPU oracle legs
@@ -330,8 +338,7 @@ def run_ours(a, wl):
     fwd_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(a.steps)]
     bwd_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(a.steps)] if wl.backward else []
 
-    samples_total = wl.num_samples * a.steps * world
-    value = samples_total / (ms_max / 1e3)
+    value = job_throughput(wl.num_samples, a.steps, world, ms_max)
 
     # End to end through the public API: pinned host inputs, copies in the timed region.
     h_in = [t.pin_memory() for t in (inp.feat, inp.loc, inp.weights, inp.grad_out)]

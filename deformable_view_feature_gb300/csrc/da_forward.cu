@@ -26,7 +26,7 @@
 // Samples a lane walks per step (loads in flight per lane), at most 32 per
 // warp-wide step.
 #ifndef DA_FWD_UNROLL
-#define DA_FWD_UNROLL 8
+#define DA_FWD_UNROLL 16
 #endif
 
 namespace da {
