@@ -10,14 +10,16 @@
 // contributions by feature row, and every row is computed once by the lanes
 // that own it:
 //
-//   1. count   one thread per location (b, a, p, k) counts the in-map
-//              corners of its S samples per feature row (row_off; one
-//              integer red per corner);
+//   1. count   one thread per location (b, a, p, k), camera-major, counts the
+//              in-map corners of its S samples per feature row (row_off):
+//              in shared memory for the maps that fit, then one global
+//              atomic per touched row; per corner for larger maps;
 //   2. scan    exclusive prefix sum of the counts (three small kernels);
-//   3. fill    the same threads claim a slot in their rows (atomic add with
-//              return) and store the record {sample*4 + corner, corner
-//              weight} (one 8-byte store), plus the slot of each corner
-//              (pos4);
+//   3. fill    the same threads claim their slots (one global range per
+//              touched row per CTA for the small maps, one global atomic per
+//              corner for the large ones) and store the record
+//              {sample*4 + corner, corner weight} (one 8-byte store), plus
+//              the slot of each corner (pos4);
 //   4. pull    C/8 lanes own one feature row (8 channels each, all groups;
 //              a whole warp when C = 256). Per record they read the
 //              anchor's grad_out row, accumulate (w * w_i) * grad_out into
@@ -64,35 +66,103 @@ BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, i
 
 namespace {
 
-// Location id pk = ((b*A + a)*P + p)*K + k -> camera k and batch item b.
-__device__ __forceinline__ void split_location(const Problem &pb, int pk, int &k, int &b)
-{
-    const int bap = static_cast<int>(pb.div_K.div(pk));
-    k = pk - bap * pb.K;
-    const int ba = static_cast<int>(pb.div_P.div(bap));
-    b = static_cast<int>(pb.div_A.div(ba));
-}
-
 // ---------------------------------------------------------------- 1. count
 
-__global__ void __launch_bounds__(256) bin_count_kernel(const Problem pb, const BinArgs w, int64_t npk)
+// Binning threads run camera-major: CTA (b, k, chunk) takes 256 consecutive
+// (a, p) pairs of camera k of batch item b, so all its corners fall in the
+// maps of that one camera. The maps of camera k that fit kBinSmemRows
+// entries are counted in shared memory first, and each touched row then gets
+// one global atomic per CTA. That removes the pile-up of atomics on the rows
+// of the coarse maps. Larger maps are counted with a global atomic per
+// corner.
+constexpr int kBinThreads = 256;
+constexpr int kBinSmemRows = 4096;
+
+struct BinCta {
+    int b, k, q;         // batch item, camera, (a*P + p) of this thread
+    bool valid;          // q < A*P
+    int64_t pk;          // location id ((b*A + a)*P + p)*K + k
+};
+
+__device__ __forceinline__ BinCta bin_cta(const Problem &pb, int ctas_per_view)
+{
+    BinCta c;
+    const int bk = static_cast<int>(blockIdx.x) / ctas_per_view;
+    const int chunk = static_cast<int>(blockIdx.x) - bk * ctas_per_view;
+    c.b = static_cast<int>(pb.div_K.div(bk));
+    c.k = bk - c.b * pb.K;
+    c.q = chunk * kBinThreads + threadIdx.x;
+    c.valid = c.q < pb.A * pb.P;
+    const int a = c.valid ? static_cast<int>(pb.div_P.div(c.q)) : 0;
+    const int p = c.q - a * pb.P;
+    c.pk = ((static_cast<int64_t>(c.b) * pb.A + a) * pb.P + p) * pb.K + c.k;
+    return c;
+}
+
+// Shared-memory offsets of the small maps of camera k (-1: counted globally).
+__device__ __forceinline__ void small_map_offsets(const Problem &pb, const MapInfo *maps_s, int k, int *hoff,
+                                                  int &nsmall)
+{
+    int off = 0;
+    for (int s = 0; s < pb.S; ++s) {
+        const int n = maps_s[k * pb.S + s].H * maps_s[k * pb.S + s].W;
+        if (off + n <= kBinSmemRows) {
+            hoff[s] = off;
+            off += n;
+        } else {
+            hoff[s] = -1;
+        }
+    }
+    nsmall = off;
+}
+
+// Adds the shared counts of the small maps into row_off: one global atomic
+// per touched row. Needs a __syncthreads() before it.
+__device__ __forceinline__ void flush_small_counts(const Problem &pb, const MapInfo *maps_s, const int *hoff,
+                                                   int k, const int *hist, int32_t *row_base)
+{
+    for (int s = 0; s < pb.S; ++s) {
+        if (hoff[s] < 0) continue;
+        const MapInfo m = maps_s[k * pb.S + s];
+        for (int r = threadIdx.x; r < m.H * m.W; r += kBinThreads) {
+            const int v = hist[hoff[s] + r];
+            if (v) atomicAdd(row_base + m.start + r, v);
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb, const BinArgs w,
+                                                                 int ctas_per_view)
 {
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    __shared__ int hist[kBinSmemRows];
+    __shared__ int hoff[DA_MAX_MAPS];
+    __shared__ int nsmall_s;
     stage_maps(pb, maps_s);
+    const BinCta c = bin_cta(pb, ctas_per_view);
     __syncthreads();
-    const int64_t pk64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (pk64 >= npk) return;
-    int k, b;
-    split_location(pb, static_cast<int>(pk64), k, b);
-    const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + pk64 * 2);
-    int32_t *cnt = w.row_off + static_cast<int64_t>(b) * pb.rows;
-    for (int s = 0; s < pb.S; ++s) {
-        Footprint f;
-        footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
+    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
+    __syncthreads();
+    int32_t *cnt = w.row_off + static_cast<int64_t>(c.b) * pb.rows;
+    if (c.valid) {
+        const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + c.pk * 2);
+        for (int s = 0; s < pb.S; ++s) {
+            const MapInfo m = maps_s[c.k * pb.S + s];
+            Footprint f;
+            footprint(xy.x, xy.y, m, f);
+            const int ho = hoff[s];
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (f.row[c] >= 0) atomicAdd(cnt + f.row[c], 1);
+            for (int cc = 0; cc < 4; ++cc) {
+                if (f.row[cc] < 0) continue;
+                if (ho >= 0) atomicAdd(&hist[ho + f.row[cc] - m.start], 1);
+                else atomicAdd(cnt + f.row[cc], 1);
+            }
+        }
     }
+    __syncthreads();
+    flush_small_counts(pb, maps_s, hoff, c.k, hist, cnt);
 }
 
 // ---------------------------------------------------------------- 2. scan
@@ -170,28 +240,70 @@ __global__ void __launch_bounds__(256) scan_add_kernel(int32_t *data, const int3
 
 // ---------------------------------------------------------------- 3. fill
 
-__global__ void __launch_bounds__(256) bin_fill_kernel(const Problem pb, const BinArgs w, int64_t npk)
+// The fill runs the same threads. For the small maps it counts again in
+// shared memory, claims one contiguous range per touched row with a single
+// global atomic, and then hands out slots inside the range with shared
+// atomics. Every corner of a large map claims its slot with a global atomic.
+// pos4 is stored view-major: index ((b*K + k)*A*P + a*P + p)*S + s.
+__global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb, const BinArgs w,
+                                                                int ctas_per_view)
 {
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    __shared__ int hist[kBinSmemRows];
+    __shared__ int hoff[DA_MAX_MAPS];
+    __shared__ int nsmall_s;
     stage_maps(pb, maps_s);
+    const BinCta c = bin_cta(pb, ctas_per_view);
     __syncthreads();
-    const int64_t pk64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (pk64 >= npk) return;
-    int k, b;
-    split_location(pb, static_cast<int>(pk64), k, b);
-    const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + pk64 * 2);
-    int32_t *cursor = w.row_off + static_cast<int64_t>(b) * pb.rows;
+    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s);
+    __syncthreads();
+    for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
+    __syncthreads();
+    float2 xy = make_float2(0.f, 0.f);
+    if (c.valid) {
+        xy = *reinterpret_cast<const float2 *>(pb.loc + c.pk * 2);
+        for (int s = 0; s < pb.S; ++s) {
+            const int ho = hoff[s];
+            if (ho < 0) continue;
+            const MapInfo m = maps_s[c.k * pb.S + s];
+            Footprint f;
+            footprint(xy.x, xy.y, m, f);
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+                if (f.row[cc] >= 0) atomicAdd(&hist[ho + f.row[cc] - m.start], 1);
+        }
+    }
+    __syncthreads();
+    // Claim each touched row's range: hist[] switches from counts to bases.
+    int32_t *cursor = w.row_off + static_cast<int64_t>(c.b) * pb.rows;
     for (int s = 0; s < pb.S; ++s) {
+        if (hoff[s] < 0) continue;
+        const MapInfo m = maps_s[c.k * pb.S + s];
+        for (int r = threadIdx.x; r < m.H * m.W; r += kBinThreads) {
+            const int v = hist[hoff[s] + r];
+            if (v) hist[hoff[s] + r] = atomicAdd(cursor + m.start + r, v);
+        }
+    }
+    __syncthreads();
+    if (!c.valid) return;
+    const int64_t vsid0 = ((static_cast<int64_t>(c.b) * pb.K + c.k) * pb.A * pb.P + c.q) * pb.S;
+    for (int s = 0; s < pb.S; ++s) {
+        const MapInfo m = maps_s[c.k * pb.S + s];
         Footprint f;
-        footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
-        const int64_t sid = pk64 * pb.S + s;
+        footprint(xy.x, xy.y, m, f);
+        const int ho = hoff[s];
+        const int64_t sid = c.pk * pb.S + s;
         int pos[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) pos[c] = f.row[c] >= 0 ? atomicAdd(cursor + f.row[c], 1) : -1;
+        for (int cc = 0; cc < 4; ++cc) {
+            pos[cc] = -1;
+            if (f.row[cc] >= 0)
+                pos[cc] = ho >= 0 ? atomicAdd(&hist[ho + f.row[cc] - m.start], 1) : atomicAdd(cursor + f.row[cc], 1);
+        }
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            if (pos[c] >= 0) w.rec[pos[c]] = make_int2(static_cast<int>(sid) * 4 + c, __float_as_int(f.cw[c]));
-        reinterpret_cast<int4 *>(w.pos4)[sid] = make_int4(pos[0], pos[1], pos[2], pos[3]);
+        for (int cc = 0; cc < 4; ++cc)
+            if (pos[cc] >= 0) w.rec[pos[cc]] = make_int2(static_cast<int>(sid) * 4 + cc, __float_as_int(f.cw[cc]));
+        reinterpret_cast<int4 *>(w.pos4)[vsid0 + s] = make_int4(pos[0], pos[1], pos[2], pos[3]);
     }
 }
 
@@ -381,7 +493,12 @@ __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const B
     const int lane = threadIdx.x & 31;
     if (pk64 >= pk_end) return;  // whole warps leave together
     const int pk = static_cast<int>(pk64);
-    const int k = pk - static_cast<int>(pb.div_K.div(pk)) * pb.K;
+    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
+    const int k = pk - bap * pb.K;
+    const int bq = static_cast<int>(pb.div_P.div(bap));  // b*A + a
+    const int b = static_cast<int>(pb.div_A.div(bq));
+    const int q = bap - b * pb.A * pb.P;  // a*P + p
+    const int64_t vsid0 = ((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * pb.S;
     const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + pk64 * 2);
     float gx = 0.f, gy = 0.f;
     const int sg = pb.S * pb.G;
@@ -393,7 +510,7 @@ __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const B
         Footprint f;
         footprint(xy.x, xy.y, m, f);
         const float wt = pb.weights[sid * pb.G + g];
-        const int4 pos = reinterpret_cast<const int4 *>(w.pos4)[sid];
+        const int4 pos = reinterpret_cast<const int4 *>(w.pos4)[vsid0 + s];
         const float *dp = w.dpix + g;  // row of record j: dpix[j*G .. j*G + G)
         const float d0 = pos.x >= 0 ? dp[static_cast<int64_t>(pos.x) * pb.G] : 0.f;
         const float d1 = pos.y >= 0 ? dp[static_cast<int64_t>(pos.y) * pb.G] : 0.f;
@@ -469,8 +586,10 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
         if (e != cudaSuccess) return e;
     }
     const int64_t npk = static_cast<int64_t>(pb.num_ba) * pb.P * pb.K;
+    const int ctas_per_view = (pb.A * pb.P + kBinThreads - 1) / kBinThreads;
+    const int64_t bin_grid = static_cast<int64_t>(pb.B) * pb.K * ctas_per_view;
     if (w.nsid > 0) {
-        bin_count_kernel<<<static_cast<unsigned>((npk + 255) / 256), 256, 0, st>>>(pb, w, npk);
+        bin_count_kernel<<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 2. offsets
@@ -485,7 +604,7 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     }
     // 3. records
     if (w.nsid > 0) {
-        bin_fill_kernel<<<static_cast<unsigned>((npk + 255) / 256), 256, 0, st>>>(pb, w, npk);
+        bin_fill_kernel<<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 4. grad_feat and d

@@ -75,7 +75,8 @@ struct BwdArgs {
 //   tile_sum [ntiles + 4] int32: per-tile totals of the scan
 //   rec      [ncap] int2: {sample id * 4 + corner, corner weight bits},
 //            grouped by feature row
-//   pos4     [nsid * 4] int32: record index of each (sample, corner), or -1
+//   pos4     [nsid * 4] int32: record index of each (sample, corner), or -1;
+//            samples in view-major order ((b*K + k)*A*P + a*P + p)*S + s
 //   dpix     [ncap * G] fp32: d = grad_out . feat of each (record, group)
 // A sample id here is ((b*A + a)*P + p)*K + k)*S + s: a sample of all groups.
 constexpr int kScanTile = 4096;
