@@ -27,7 +27,7 @@ import torch
 from . import build as _build
 
 __all__ = ["da_forward", "da_backward", "backward_workspace_size", "DeformableAggregationFunction",
-           "DaError", "library_path", "load_library", "da_version"]
+           "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
 
 DA_F32, DA_BF16 = 0, 1
 _STATUS = {0: "DA_OK", 1: "DA_ERR_NULL", 2: "DA_ERR_SHAPE", 3: "DA_ERR_ALIGN",
@@ -81,6 +81,15 @@ def load_library():
     lib.da_last_error.restype = ctypes.c_char_p
     lib.da_version.argtypes = []
     lib.da_version.restype = ctypes.c_int32
+    lib.da_pipeline_create.argtypes = [ctypes.POINTER(DaDims), vp, vp, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.POINTER(vp)]
+    lib.da_pipeline_create.restype = ctypes.c_int
+    lib.da_pipeline_submit.argtypes = [vp] * 9
+    lib.da_pipeline_submit.restype = ctypes.c_int
+    lib.da_pipeline_sync.argtypes = [vp]
+    lib.da_pipeline_sync.restype = ctypes.c_int
+    lib.da_pipeline_destroy.argtypes = [vp]
+    lib.da_pipeline_destroy.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -227,6 +236,102 @@ def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
                            _dptr(weights), _dptr(grad_out), _dptr(grad_feat), _dptr(grad_loc),
                            _dptr(grad_weight), ws_ptr, ws_bytes, sh))
     return grad_feat, grad_loc, grad_weight
+
+
+def _hptr(t: Optional[torch.Tensor], name: str, shape, dtype) -> Optional[int]:
+    if t is None:
+        if int(torch.Size(shape).numel()) == 0:
+            return None
+        raise ValueError(f"{name} is required")
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host tensor")
+    if not t.is_contiguous() or tuple(t.shape) != tuple(shape) or t.dtype != dtype:
+        raise ValueError(f"{name} must be a contiguous {dtype} host tensor of shape {tuple(shape)}")
+    return t.data_ptr() if t.numel() else None
+
+
+class HostPipeline:
+    """da_pipeline_* (include/da.h): steps whose tensors are HOST tensors.
+
+    Each ``submit`` copies a step's inputs to the device, runs the forward
+    (and backward), and copies the outputs back into the given host tensors.
+    Copies in, kernels and copies out of consecutive steps overlap on three
+    streams. Host tensors should be pinned (``tensor.pin_memory()``); the
+    outputs are valid, and the inputs may change, after ``sync()``.
+    """
+
+    def __init__(self, dims: DaDims, spatial_shape, level_start_index, backward: bool = True,
+                 depth: int = 2, device: Optional[torch.device] = None):
+        lib = load_library()
+        self._ss, self._ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+        self.dims = dims
+        self.backward = backward
+        self._handle = ctypes.c_void_p(None)
+        self._inflight = []
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+        with torch.cuda.device(dev):
+            _check(lib.da_pipeline_create(ctypes.byref(dims), self._ss.data_ptr() if self._ss.numel() else None,
+                                          self._ls.data_ptr() if self._ls.numel() else None,
+                                          int(backward), depth, ctypes.byref(self._handle)))
+        self.device = dev
+
+    def shapes(self):
+        d = self.dims
+        fdt = torch.bfloat16 if d.feat_dtype == DA_BF16 else torch.float32
+        S, G = d.num_scales, d.num_groups
+        B, A, P, K, C = d.batch, d.num_anchors, d.num_pts, d.num_cams, d.num_embeds
+        return {"mc_ms_feat": ((B, d.num_feat_rows, C), fdt),
+                "sampling_location": ((B, A, P, K, 2), torch.float32),
+                "weights": ((B, A, P, K, S, G), torch.float32),
+                "grad_out": ((B, A, C), torch.float32), "out": ((B, A, C), torch.float32),
+                "grad_feat": ((B, d.num_feat_rows, C), torch.float32),
+                "grad_loc": ((B, A, P, K, 2), torch.float32),
+                "grad_weight": ((B, A, P, K, S, G), torch.float32)}
+
+    def submit(self, mc_ms_feat, sampling_location, weights, out, grad_out=None, grad_feat=None,
+               grad_loc=None, grad_weight=None):
+        if not self._handle:
+            raise RuntimeError("pipeline is closed")
+        sh = self.shapes()
+        args = {"mc_ms_feat": mc_ms_feat, "sampling_location": sampling_location, "weights": weights,
+                "grad_out": grad_out, "out": out, "grad_feat": grad_feat, "grad_loc": grad_loc,
+                "grad_weight": grad_weight}
+        grads = ("grad_out", "grad_feat", "grad_loc", "grad_weight")
+        ptrs = {}
+        for name, t in args.items():
+            if name in grads and not self.backward:
+                ptrs[name] = None
+                continue
+            ptrs[name] = _hptr(t, name, *sh[name])
+        _check(load_library().da_pipeline_submit(
+            self._handle, ptrs["mc_ms_feat"], ptrs["sampling_location"], ptrs["weights"], ptrs["grad_out"],
+            ptrs["out"], ptrs["grad_feat"], ptrs["grad_loc"], ptrs["grad_weight"]))
+        # The copies read and write these tensors until the next sync.
+        self._inflight.append(tuple(t for t in args.values() if t is not None))
+
+    def sync(self):
+        if self._handle:
+            _check(load_library().da_pipeline_sync(self._handle))
+        self._inflight.clear()
+
+    def close(self):
+        if self._handle:
+            st = load_library().da_pipeline_destroy(self._handle)
+            self._handle = ctypes.c_void_p(None)
+            self._inflight.clear()
+            _check(st)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class DeformableAggregationFunction(torch.autograd.Function):

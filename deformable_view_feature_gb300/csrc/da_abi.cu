@@ -20,9 +20,11 @@
 // once per device with that device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DA_NOALLOC_SCRATCH_BYTES];
 
-namespace {
+namespace da {
 
+namespace {
 thread_local char g_err[256] = "";
+}  // namespace
 
 da_status fail(da_status st, const char *fmt, ...)
 {
@@ -33,12 +35,17 @@ da_status fail(da_status st, const char *fmt, ...)
     return st;
 }
 
+const char *last_error() { return g_err; }
+
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
-// Checks shared by both passes; fills the kernel's Problem and the chunk count.
-da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_shape,
-                  const int32_t *level_start_index, const float *loc, const float *weights,
-                  da::Problem &pb, int &chunks)
+da_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(DA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const int32_t *level_start_index,
+                        Problem &pb, int &chunks)
 {
     if (!dims) return fail(DA_ERR_NULL, "dims is NULL");
     const da_dims d = *dims;
@@ -82,18 +89,6 @@ da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_
                         static_cast<long long>(i), st, H, W, static_cast<long long>(d.num_feat_rows));
         pb.maps[i] = da::MapInfo{H, W, st, 0};
     }
-
-    const int64_t n_feat = static_cast<int64_t>(d.batch) * d.num_feat_rows * d.num_embeds;
-    const int64_t n_samp = num_ba * pks;
-    if (n_feat > 0 && !feat) return fail(DA_ERR_NULL, "mc_ms_feat is NULL");
-    if (n_samp > 0 && (!loc || !weights)) return fail(DA_ERR_NULL, "sampling_location / weights is NULL");
-    if (!aligned(feat, 16)) return fail(DA_ERR_ALIGN, "mc_ms_feat must be 16-byte aligned");
-    if (!aligned(loc, 8)) return fail(DA_ERR_ALIGN, "sampling_location must be 8-byte aligned");
-    if (!aligned(weights, 4)) return fail(DA_ERR_ALIGN, "weights must be 4-byte aligned");
-
-    pb.feat = feat;
-    pb.loc = loc;
-    pb.weights = weights;
     pb.rows = d.num_feat_rows;
     pb.B = d.batch;
     pb.A = d.num_anchors;
@@ -118,9 +113,36 @@ da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_
     return DA_OK;
 }
 
-da_status cuda_fail(cudaError_t e, const char *what)
+}  // namespace da
+
+namespace {
+
+using da::aligned;
+using da::cuda_fail;
+using da::fail;
+
+// Checks shared by both passes; fills the kernel's Problem and the chunk count.
+da_status prepare(const da_dims *dims, const void *feat, const int32_t *spatial_shape,
+                  const int32_t *level_start_index, const float *loc, const float *weights,
+                  da::Problem &pb, int &chunks)
 {
-    return fail(DA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+    da_status st = da::prepare_shape(dims, spatial_shape, level_start_index, pb, chunks);
+    if (st != DA_OK) return st;
+    const da_dims d = *dims;
+    const int64_t num_ba = pb.num_ba;
+    const int64_t pks = pb.pks;
+    const int64_t n_feat = static_cast<int64_t>(d.batch) * d.num_feat_rows * d.num_embeds;
+    const int64_t n_samp = num_ba * pks;
+    if (n_feat > 0 && !feat) return fail(DA_ERR_NULL, "mc_ms_feat is NULL");
+    if (n_samp > 0 && (!loc || !weights)) return fail(DA_ERR_NULL, "sampling_location / weights is NULL");
+    if (!aligned(feat, 16)) return fail(DA_ERR_ALIGN, "mc_ms_feat must be 16-byte aligned");
+    if (!aligned(loc, 8)) return fail(DA_ERR_ALIGN, "sampling_location must be 8-byte aligned");
+    if (!aligned(weights, 4)) return fail(DA_ERR_ALIGN, "weights must be 4-byte aligned");
+
+    pb.feat = feat;
+    pb.loc = loc;
+    pb.weights = weights;
+    return DA_OK;
 }
 
 // Layout of the binned backward's workspace; DA_ERR_UNSUPPORTED when its
@@ -297,7 +319,7 @@ const char *da_status_string(da_status status)
     return "DA_ERR_UNKNOWN";
 }
 
-const char *da_last_error(void) { return g_err; }
+const char *da_last_error(void) { return da::last_error(); }
 
 int32_t da_version(void) { return 100; }
 

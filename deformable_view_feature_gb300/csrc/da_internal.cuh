@@ -113,6 +113,17 @@ cudaError_t launch_backward(const BwdArgs &a, int feat_dtype, int chunks, cudaSt
 cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st);
 cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st);
 
+// Host-side helpers of the entry points (da_abi.cu).
+// fail: records a one-line reason for da_last_error() and returns st.
+da_status fail(da_status st, const char *fmt, ...);
+const char *last_error();
+da_status cuda_fail(cudaError_t e, const char *what);
+bool aligned(const void *p, uintptr_t a);
+// Validates dims and the two host map tables and fills every field of pb
+// except the tensor pointers. Makes no CUDA call.
+da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const int32_t *level_start_index,
+                        Problem &pb, int &chunks);
+
 // Grid size that covers num_ba anchors, anchors_per_cta at a time.
 inline int64_t sampling_grid(const Problem &pb)
 {

@@ -28,7 +28,9 @@
  *   - Pointers marked "device" point to memory the calling CUDA context can
  *     read or write from kernels. Pointers marked "host" point to ordinary
  *     host memory, read during the call only.
- *   - The caller owns every buffer; the library allocates nothing.
+ *   - The caller owns every buffer; the library allocates nothing. The one
+ *     exception is a da_pipeline (below): it owns the device buffers it
+ *     allocates when it is created.
  *   - Work is enqueued on `stream`, or on the legacy default stream when it is
  *     NULL. The call returns without synchronising. Outputs are valid once the
  *     stream reaches that point.
@@ -210,6 +212,77 @@ da_status da_backward_noalloc(const da_dims *dims,
                               float *grad_loc,
                               float *grad_weight,
                               da_stream_t stream);
+
+/*
+ * Host pipeline: the forward (and backward) of a sequence of problems of one
+ * shape whose tensors live in HOST memory.
+ *
+ * The pages do not describe this part. It is the path for callers whose data
+ * sits in host memory: every step copies its inputs to the device, runs
+ * da_forward (and da_backward), and copies the outputs back. The pipeline
+ * keeps `depth` sets of device buffers and three CUDA streams (copy in,
+ * compute, copy out). Step n uses buffer set n % depth, so step n's input
+ * copy and step n-1's output copy run while a third step computes, and the
+ * two copy directions share the host link at once.
+ *
+ * da_pipeline_create
+ *   dims, spatial_shape, level_start_index: as for da_forward (host arrays,
+ *     copied; the caller may free them afterwards).
+ *   with_backward: 0 = forward only; 1 = forward, then backward.
+ *   depth: buffer sets, 1 to 4. depth 1 serialises copies and compute; 2 is
+ *     enough to overlap them.
+ *   *pipeline receives the new pipeline.
+ *   Works on the CUDA device that is current when it is called. It allocates
+ *   depth * (inputs + outputs + backward workspace) bytes of device memory
+ *   with cudaMalloc. With a backward, the binned path of da_backward is used
+ *   when the sizes allow it (see da_backward_workspace_size), and the scatter
+ *   path otherwise. Sizes are validated before any CUDA call.
+ *
+ * da_pipeline_submit
+ *   Host pointers with the layouts of da_forward and da_backward:
+ *   mc_ms_feat, sampling_location, weights, grad_out (inputs) and out,
+ *   grad_feat, grad_loc, grad_weight (outputs). Without a backward, grad_out
+ *   and the three gradients are ignored and may be NULL. A pointer may be
+ *   NULL only when its tensor has no elements.
+ *   Enqueues one step and returns. It does not wait when every host buffer
+ *   is page-locked (cudaHostAlloc, cudaHostRegister); with pageable memory
+ *   the copies may block the caller. Do not change the step's input buffers
+ *   or read its output buffers until da_pipeline_sync returns.
+ *
+ * da_pipeline_sync
+ *   Waits until every submitted step has finished and its outputs are in host
+ *   memory.
+ *
+ * da_pipeline_destroy
+ *   Waits like da_pipeline_sync, then frees the device buffers, streams and
+ *   events. NULL is accepted and ignored.
+ *
+ * A pipeline is not thread-safe: one thread at a time. After DA_ERR_CUDA
+ * from submit or sync, the pipeline refuses further steps with DA_ERR_CUDA;
+ * destroy it.
+ */
+typedef struct da_pipeline da_pipeline;
+
+da_status da_pipeline_create(const da_dims *dims,
+                             const int32_t *spatial_shape,
+                             const int32_t *level_start_index,
+                             int32_t with_backward,
+                             int32_t depth,
+                             da_pipeline **pipeline);
+
+da_status da_pipeline_submit(da_pipeline *pipeline,
+                             const void *mc_ms_feat,
+                             const float *sampling_location,
+                             const float *weights,
+                             const float *grad_out,
+                             float *out,
+                             float *grad_feat,
+                             float *grad_loc,
+                             float *grad_weight);
+
+da_status da_pipeline_sync(da_pipeline *pipeline);
+
+da_status da_pipeline_destroy(da_pipeline *pipeline);
 
 /* Static name of a status code. */
 const char *da_status_string(da_status status);

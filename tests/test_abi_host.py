@@ -175,3 +175,39 @@ def test_binding_rejects_host_tensors():
     w = torch.zeros(1, 4, 2, 1, 1, 1)
     with pytest.raises((ValueError, RuntimeError)):
         da.da_forward(feat, [[[4, 4]]], [[0]], loc, w, out=torch.zeros(1, 4, 32))
+
+
+def test_pipeline_validation_before_any_cuda_call(lib):
+    vp = ctypes.c_void_p
+    lib.da_pipeline_create.argtypes = [ctypes.POINTER(da.DaDims), vp, vp, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.POINTER(vp)]
+    lib.da_pipeline_submit.argtypes = [vp] * 9
+    lib.da_pipeline_sync.argtypes = [vp]
+    lib.da_pipeline_destroy.argtypes = [vp]
+    ss, ls = _tables()
+    h = vp(None)
+    assert lib.da_pipeline_create(ctypes.byref(_dims()), ss, ls, 1, 2, None) == DA_ERR_NULL
+    assert lib.da_pipeline_create(ctypes.byref(_dims()), ss, ls, 1, 0, ctypes.byref(h)) == DA_ERR_SHAPE
+    assert lib.da_pipeline_create(ctypes.byref(_dims()), ss, ls, 1, 5, ctypes.byref(h)) == DA_ERR_SHAPE
+    assert lib.da_pipeline_create(ctypes.byref(_dims()), ss, ls, 2, 2, ctypes.byref(h)) == DA_ERR_SHAPE
+    assert lib.da_pipeline_create(ctypes.byref(_dims(num_groups=3)), ss, ls, 1, 2, ctypes.byref(h)) == DA_ERR_SHAPE
+    big_ss, big_ls = _tables(H=4, W=5)  # 20 rows > 16
+    assert lib.da_pipeline_create(ctypes.byref(_dims()), big_ss, big_ls, 0, 2, ctypes.byref(h)) == DA_ERR_SHAPE
+    assert lib.da_pipeline_create(ctypes.byref(_dims(num_embeds=12)), ss, ls, 0, 2,
+                                  ctypes.byref(h)) == DA_ERR_UNSUPPORTED
+    assert not h.value  # nothing was created
+    assert lib.da_pipeline_submit(None, *([None] * 8)) == DA_ERR_NULL
+    assert lib.da_pipeline_sync(None) == DA_ERR_NULL
+    assert lib.da_pipeline_destroy(None) == DA_OK
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="checks the behaviour without a GPU")
+def test_pipeline_create_without_gpu_fails_cleanly(lib):
+    vp = ctypes.c_void_p
+    lib.da_pipeline_create.argtypes = [ctypes.POINTER(da.DaDims), vp, vp, ctypes.c_int32, ctypes.c_int32,
+                                       ctypes.POINTER(vp)]
+    ss, ls = _tables()
+    h = vp(None)
+    assert lib.da_pipeline_create(ctypes.byref(_dims()), ss, ls, 1, 2, ctypes.byref(h)) == 5  # DA_ERR_CUDA
+    assert not h.value
+    assert b"pipeline set-up" in lib.da_last_error()
