@@ -85,7 +85,8 @@ def ncu_traffic(workload: str, call: str):
     return NCU_TRAFFIC.get(call)
 # Kernels da_backward launches: binned = row-count zero-fill, count, 3 scan
 # steps, fill, pull, epilogue; scatter = grad_feat zero-fill, gather-scatter.
-BWD_LAUNCHES = {"binned": 8, "scatter": 2}
+# binned-det adds the four kernels of the per-row sort (DA_BACKWARD_DETERMINISTIC).
+BWD_LAUNCHES = {"binned": 8, "binned-det": 12, "scatter": 2}
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -300,7 +301,8 @@ def run_ours(a, wl):
     stream = torch.cuda.Stream(device=dev)
     fwd_bytes, bwd_bytes = algorithmic_bytes(inp)
     ws = None
-    if a.bwd_path == "binned":
+    path = "scatter" if a.bwd_path == "scatter" else "binned"
+    if path == "binned":
         dims = da._dims(feat, da._host_i32(ss), loc, w)
         ws = torch.empty(max(da.backward_workspace_size(dims), 256), dtype=torch.uint8, device=dev)
 
@@ -312,7 +314,8 @@ def run_ours(a, wl):
             ev[1].record(stream)
         if wl.backward:
             da.da_backward(feat, ss, ls, loc, w, go, grad_feat=gf, grad_loc=gl, grad_weight=gw,
-                           stream=stream, path=a.bwd_path, workspace=ws)
+                           stream=stream, path=path, workspace=ws,
+                           deterministic=a.bwd_path == "binned-det")
             if ev is not None:
                 ev[2].record(stream)
 
@@ -432,8 +435,9 @@ def main():
     ap.add_argument("--ref-anchors", type=int, default=300,
                     help="anchors per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--bwd-path", choices=["binned", "scatter"], default="binned",
-                    help="backward algorithm (binned needs a device workspace)")
+    ap.add_argument("--bwd-path", choices=["binned", "binned-det", "scatter"], default="binned",
+                    help="backward algorithm (binned needs a device workspace; binned-det is its "
+                         "deterministic mode)")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -73,6 +73,9 @@ def load_library():
     lib.da_backward.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                 ctypes.c_size_t, vp]
     lib.da_backward.restype = ctypes.c_int
+    lib.da_backward_ex.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                   ctypes.c_size_t, ctypes.c_uint32, vp]
+    lib.da_backward_ex.restype = ctypes.c_int
     lib.da_backward_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
     lib.da_backward_workspace_size.restype = ctypes.c_int
     lib.da_status_string.argtypes = [ctypes.c_int]
@@ -194,14 +197,19 @@ def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
                 sampling_location: torch.Tensor, weights: torch.Tensor, grad_out: torch.Tensor,
                 grad_feat: Optional[torch.Tensor] = None, grad_loc: Optional[torch.Tensor] = None,
                 grad_weight: Optional[torch.Tensor] = None, stream=None, path: str = "scatter",
-                workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                workspace: Optional[torch.Tensor] = None,
+                deterministic: bool = False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Backward pass; returns (grad_feat fp32, grad_loc, grad_weight).
 
     path="scatter" (default) needs no workspace and scatters grad_feat with
     vector reductions; path="binned" sorts the corner contributions by
     feature row in a device workspace (allocated through torch and reused, or
-    passed in) and writes every grad_feat row once.
+    passed in) and writes every grad_feat row once. deterministic=True
+    (binned only) fixes the order of every row's contributions, so the
+    gradients are the same bit for bit on every run (DA_BACKWARD_DETERMINISTIC).
     """
+    if deterministic and path != "binned":
+        raise ValueError("deterministic=True needs path='binned'")
     lib = load_library()
     ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
     d = _dims(mc_ms_feat, ss, sampling_location, weights)
@@ -231,10 +239,10 @@ def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
         ws_ptr = _dptr(workspace)
     elif path != "scatter":
         raise ValueError("path must be 'binned' or 'scatter'")
-    _check(lib.da_backward(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
-                           ls.data_ptr() if ls.numel() else None, _dptr(sampling_location),
-                           _dptr(weights), _dptr(grad_out), _dptr(grad_feat), _dptr(grad_loc),
-                           _dptr(grad_weight), ws_ptr, ws_bytes, sh))
+    _check(lib.da_backward_ex(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
+                              ls.data_ptr() if ls.numel() else None, _dptr(sampling_location),
+                              _dptr(weights), _dptr(grad_out), _dptr(grad_feat), _dptr(grad_loc),
+                              _dptr(grad_weight), ws_ptr, ws_bytes, 1 if deterministic else 0, sh))
     return grad_feat, grad_loc, grad_weight
 
 

@@ -227,6 +227,21 @@ da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t
                       const float *weights, const float *grad_out, float *grad_feat, float *grad_loc,
                       float *grad_weight, void *workspace, size_t workspace_bytes, da_stream_t stream)
 {
+    return da_backward_ex(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location, weights,
+                          grad_out, grad_feat, grad_loc, grad_weight, workspace, workspace_bytes, 0u, stream);
+}
+
+da_status da_backward_ex(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                         const int32_t *level_start_index, const float *sampling_location,
+                         const float *weights, const float *grad_out, float *grad_feat, float *grad_loc,
+                         float *grad_weight, void *workspace, size_t workspace_bytes, uint32_t flags,
+                         da_stream_t stream)
+{
+    if (flags & ~static_cast<uint32_t>(DA_BACKWARD_DETERMINISTIC))
+        return fail(DA_ERR_SHAPE, "unknown flags 0x%x", flags);
+    const bool deterministic = (flags & DA_BACKWARD_DETERMINISTIC) != 0;
+    if (deterministic && !workspace && !workspace_bytes)
+        return fail(DA_ERR_WORKSPACE, "DA_BACKWARD_DETERMINISTIC needs the binned path's workspace");
     da::BwdArgs a{};
     int chunks = 0;
     da_status st = prepare(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location,
@@ -273,6 +288,13 @@ da_status da_backward(const da_dims *dims, const void *mc_ms_feat, const int32_t
         w.nsid = L.nsid;
         w.ncap = L.ncap;
         w.ntiles = L.ntiles;
+        if (deterministic) {
+            w.sort_lists = reinterpret_cast<int32_t *>(ws + L.off_lists);
+            w.sort_counts = w.row_off + L.ntiles * da::kScanTile + 4;
+            w.cap_m = L.cap_m;
+            w.cap_s = L.cap_s;
+            w.cap_g = L.cap_g;
+        }
         const cudaError_t e = da::launch_backward_binned(a, w, dims->feat_dtype, s);
         if (e != cudaSuccess) return cuda_fail(e, "binned backward launch");
         return DA_OK;

@@ -33,6 +33,7 @@
 //              reduced by shuffles. Every output has one owner, so there
 //              are no atomics.
 #include <algorithm>
+#include <climits>
 
 #include "da_internal.cuh"
 
@@ -51,7 +52,9 @@ BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, i
     L.ntiles = (L.rows_total + kScanTile - 1) / kScanTile;
     size_t o = 0;
     L.off_row_off = o;
-    o = align256(o + static_cast<size_t>(L.ntiles * kScanTile + 4) * 4);
+    // Row offsets, the scan's end value, then the sort's three list counters:
+    // one zero-fill clears them all.
+    o = align256(o + static_cast<size_t>(L.ntiles * kScanTile + kRowOffTail) * 4);
     L.off_tile_sum = o;
     o = align256(o + static_cast<size_t>(L.ntiles + 4) * 4);
     L.off_rec = o;
@@ -60,6 +63,13 @@ BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, i
     o = align256(o + static_cast<size_t>(L.nsid) * 16);
     L.off_dpix = o;
     o = align256(o + static_cast<size_t>(L.ncap) * static_cast<size_t>(G) * 4);
+    // A row holds more than 8 (128, 2048) records in at most ncap/9
+    // (ncap/129, ncap/2049) rows.
+    L.cap_m = L.ncap / 9 + 1;
+    L.cap_s = L.ncap / 129 + 1;
+    L.cap_g = L.ncap / 2049 + 1;
+    L.off_lists = o;
+    o = align256(o + static_cast<size_t>(L.cap_m + L.cap_s + L.cap_g) * 4);
     L.bytes = o;
     return L;
 }
@@ -304,6 +314,195 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
         for (int cc = 0; cc < 4; ++cc)
             if (pos[cc] >= 0) w.rec[pos[cc]] = make_int2(static_cast<int>(sid) * 4 + cc, __float_as_int(f.cw[cc]));
         reinterpret_cast<int4 *>(w.pos4)[vsid0 + s] = make_int4(pos[0], pos[1], pos[2], pos[3]);
+    }
+}
+
+// ------------------------------------------- 3b. sort (deterministic mode)
+
+// The fill hands out slots inside a row with atomics, so the order of a
+// row's records, and with it the rounding of the pull's sums, changes from
+// run to run. In deterministic mode the records of every row are put in
+// ascending order of their first field (sample id * 4 + corner, unique per
+// record) before the pull, and pos4 is rewritten to match. The sum over a
+// row then always runs in the same order, so grad_feat (and everything
+// computed from it) is the same bit for bit on every run.
+//
+// A row's records all come from the A*P locations of one view at one scale,
+// and a location puts at most one corner in a row, so a row holds at most
+// A*P records. Three tiers, by row length n:
+//   n <= 8      one thread per row: rank = number of smaller keys;
+//   n <= 128    one warp per row, records staged in shared memory, ranks;
+//   n <= 2048   one CTA per row, bitonic sort in shared memory;
+//   larger      one CTA per row, bitonic sort in place in global memory.
+// The first kernel runs over all rows and lists the longer ones for the
+// other three.
+
+constexpr int kSortThreads = 256;
+constexpr int kSortWarpMax = 128;
+constexpr int kSortSmemMax = 2048;
+
+// Index into pos4 (int32 entries) of record key sid*4 + corner.
+__device__ __forceinline__ int64_t pos4_entry(const Problem &pb, int key)
+{
+    const int sid = key >> 2;
+    const int pk = static_cast<int>(pb.div_S.div(sid));
+    const int s = sid - pk * pb.S;
+    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
+    const int k = pk - bap * pb.K;
+    const int bq = static_cast<int>(pb.div_P.div(bap));
+    const int b = static_cast<int>(pb.div_A.div(bq));
+    const int q = bap - b * pb.A * pb.P;
+    return (((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * pb.S + s) * 4 + (key & 3);
+}
+
+__device__ __forceinline__ int row_begin(const BinArgs &w, int64_t r) { return r > 0 ? w.row_off[r - 1] : 0; }
+
+__global__ void __launch_bounds__(kSortThreads) sort_short_rows_kernel(const Problem pb, const BinArgs w)
+{
+    __shared__ int n_list[3], base[3];
+    if (threadIdx.x < 3) n_list[threadIdx.x] = 0;
+    __syncthreads();
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * kSortThreads + threadIdx.x;
+    int n = 0, jb = 0;
+    if (r < w.rows_total) {
+        jb = row_begin(w, r);
+        n = w.row_off[r] - jb;
+    }
+    const int tier = n <= 8 ? -1 : n <= kSortWarpMax ? 0 : n <= kSortSmemMax ? 1 : 2;
+    int slot = 0;
+    if (tier >= 0) slot = atomicAdd(&n_list[tier], 1);
+    __syncthreads();
+    if (threadIdx.x < 3 && n_list[threadIdx.x] > 0)
+        base[threadIdx.x] = atomicAdd(w.sort_counts + threadIdx.x, n_list[threadIdx.x]);
+    __syncthreads();
+    if (tier >= 0) {
+        const int64_t off = tier == 0 ? 0 : tier == 1 ? w.cap_m : w.cap_m + w.cap_s;
+        w.sort_lists[off + base[tier] + slot] = static_cast<int32_t>(r);
+        return;
+    }
+    if (n < 2) return;
+    int2 e[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) e[u] = u < n ? w.rec[jb + u] : make_int2(INT_MAX, 0);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+        if (u >= n) break;
+        int rank = 0;
+#pragma unroll
+        for (int v = 0; v < 8; ++v) rank += (e[v].x < e[u].x) ? 1 : 0;  // padding keys are never smaller
+        if (rank != u) {
+            w.rec[jb + rank] = e[u];
+            w.pos4[pos4_entry(pb, e[u].x)] = jb + rank;
+        }
+    }
+}
+
+// Rows of 9..128 records: one warp per row. The records are staged in
+// shared memory; each lane ranks its records against all of them.
+__global__ void __launch_bounds__(kSortThreads) sort_warp_rows_kernel(const Problem pb, const BinArgs w)
+{
+    __shared__ int2 buf[kSortThreads / 32][kSortWarpMax];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int count = w.sort_counts[0];
+    const int nwarps = gridDim.x * (kSortThreads / 32);
+    for (int i = blockIdx.x * (kSortThreads / 32) + warp; i < count; i += nwarps) {
+        const int64_t r = w.sort_lists[i];
+        const int jb = row_begin(w, r);
+        const int n = w.row_off[r] - jb;
+        for (int j = lane; j < n; j += 32) buf[warp][j] = w.rec[jb + j];
+        __syncwarp();
+        for (int j = lane; j < n; j += 32) {
+            const int2 e = buf[warp][j];
+            int rank = 0;
+            for (int v = 0; v < n; ++v) rank += (buf[warp][v].x < e.x) ? 1 : 0;
+            if (rank != j) {
+                w.rec[jb + rank] = e;
+                w.pos4[pos4_entry(pb, e.x)] = jb + rank;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// Compare-exchange of a bitonic network: the smaller key goes to index lo.
+template <typename Ptr>
+__device__ __forceinline__ void cmp_swap(Ptr a, int lo, int hi)
+{
+    const int2 x = a[lo], y = a[hi];
+    if (x.x > y.x) {
+        a[lo] = y;
+        a[hi] = x;
+    }
+}
+
+// Ascending bitonic sort of a[0..n) by the block's threads, in the variant
+// whose first step of every merge compares mirrored elements: every
+// comparator then points the same way, and positions past n act as +inf
+// that no comparator moves, so n need not be a power of two. `sync` is
+// __syncthreads; a[] is shared or global memory.
+template <typename Ptr>
+__device__ void block_bitonic_sort(Ptr a, int n)
+{
+    int64_t np = 1;
+    while (np < n) np <<= 1;
+    const int half = static_cast<int>(np >> 1);
+    for (int64_t k = 2; k <= np; k <<= 1) {
+        const int lk = __ffsll(k) - 2;  // log2(k / 2)
+        const int hk = static_cast<int>(k >> 1);
+        for (int i = threadIdx.x; i < half; i += blockDim.x) {
+            const int blk = i >> lk, o = i & (hk - 1);
+            const int64_t lo = static_cast<int64_t>(blk) * k + o, hi = static_cast<int64_t>(blk) * k + k - 1 - o;
+            if (hi < n) cmp_swap(a, static_cast<int>(lo), static_cast<int>(hi));
+        }
+        __syncthreads();
+        for (int j = hk >> 1; j > 0; j >>= 1) {
+            const int lj = __ffs(j) - 1;
+            for (int i = threadIdx.x; i < half; i += blockDim.x) {
+                const int blk = i >> lj, o = i & (j - 1);
+                const int64_t lo = (static_cast<int64_t>(blk) << (lj + 1)) + o, hi = lo + j;
+                if (hi < n) cmp_swap(a, static_cast<int>(lo), static_cast<int>(hi));
+            }
+            __syncthreads();
+        }
+    }
+}
+
+// Rows of 129..2048 records: one CTA per row, sorted in shared memory.
+__global__ void __launch_bounds__(kSortThreads) sort_cta_rows_kernel(const Problem pb, const BinArgs w)
+{
+    __shared__ int2 buf[kSortSmemMax];
+    const int count = w.sort_counts[1];
+    const int32_t *list = w.sort_lists + w.cap_m;
+    for (int i = blockIdx.x; i < count; i += gridDim.x) {
+        const int64_t r = list[i];
+        const int jb = row_begin(w, r);
+        const int n = w.row_off[r] - jb;
+        for (int j = threadIdx.x; j < n; j += kSortThreads) buf[j] = w.rec[jb + j];
+        __syncthreads();
+        block_bitonic_sort(static_cast<int2 *>(buf), n);
+        for (int j = threadIdx.x; j < n; j += kSortThreads) {
+            const int2 e = buf[j];
+            w.rec[jb + j] = e;
+            w.pos4[pos4_entry(pb, e.x)] = jb + j;
+        }
+        __syncthreads();
+    }
+}
+
+// Rows of more than 2048 records (crowded pixels): one CTA per row, sorted
+// in place in global memory (plain loads: the data changes under the
+// kernel, so no read-only cache path).
+__global__ void __launch_bounds__(1024) sort_long_rows_kernel(const Problem pb, const BinArgs w)
+{
+    const int count = w.sort_counts[2];
+    const int32_t *list = w.sort_lists + w.cap_m + w.cap_s;
+    for (int i = blockIdx.x; i < count; i += gridDim.x) {
+        const int64_t r = list[i];
+        const int jb = row_begin(w, r);
+        const int n = w.row_off[r] - jb;
+        block_bitonic_sort(w.rec + jb, n);
+        for (int j = threadIdx.x; j < n; j += blockDim.x) w.pos4[pos4_entry(pb, w.rec[jb + j].x)] = jb + j;
+        __syncthreads();
     }
 }
 
@@ -582,7 +781,7 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     cudaError_t e;
     // 1. counts
     if (w.ntiles > 0) {
-        e = launch_zero_fill(reinterpret_cast<float *>(w.row_off), w.ntiles * kScanTile + 4, st);
+        e = launch_zero_fill(reinterpret_cast<float *>(w.row_off), w.ntiles * kScanTile + kRowOffTail, st);
         if (e != cudaSuccess) return e;
     }
     const int64_t npk = static_cast<int64_t>(pb.num_ba) * pb.P * pb.K;
@@ -605,6 +804,22 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     // 3. records
     if (w.nsid > 0) {
         bin_fill_kernel<<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    // 3b. deterministic order inside every row
+    if (w.sort_lists && w.nsid > 0 && w.rows_total > 0) {
+        const int64_t g1 = (w.rows_total + kSortThreads - 1) / kSortThreads;
+        sort_short_rows_kernel<<<static_cast<unsigned>(g1), kSortThreads, 0, st>>>(pb, w);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        int dev = 0, sms = 0;
+        if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        // Persistent grids over the row lists (their lengths are on the device).
+        sort_warp_rows_kernel<<<static_cast<unsigned>(sms * 8), kSortThreads, 0, st>>>(pb, w);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        sort_cta_rows_kernel<<<static_cast<unsigned>(sms * 4), kSortThreads, 0, st>>>(pb, w);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        sort_long_rows_kernel<<<static_cast<unsigned>(sms), 1024, 0, st>>>(pb, w);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 4. grad_feat and d

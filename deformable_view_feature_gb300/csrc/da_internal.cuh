@@ -69,24 +69,33 @@ struct BwdArgs {
 
 // Device scratch of the binned backward, carved out of one caller-provided
 // buffer. Every region starts on a 256-byte boundary.
-//   row_off  [ntiles*kScanTile + 4] int32: per feature row (over all B*rows
-//            rows): the corner count, then its exclusive prefix sum, then
-//            (after the fill) the end of the row's record range
+//   row_off  [ntiles*kScanTile + kRowOffTail] int32: per feature row (over
+//            all B*rows rows): the corner count, then its exclusive prefix
+//            sum, then (after the fill) the end of the row's record range.
+//            The tail holds the scan's total and the sort's list counters.
 //   tile_sum [ntiles + 4] int32: per-tile totals of the scan
 //   rec      [ncap] int2: {sample id * 4 + corner, corner weight bits},
-//            grouped by feature row
+//            grouped by feature row; in deterministic mode sorted by the
+//            first field within each row
 //   pos4     [nsid * 4] int32: record index of each (sample, corner), or -1;
 //            samples in view-major order ((b*K + k)*A*P + a*P + p)*S + s
 //   dpix     [ncap * G] fp32: d = grad_out . feat of each (record, group)
+//   lists    [cap_m + cap_s + cap_g] int32: rows the deterministic sort
+//            hands to a warp (9..128 records), a CTA with shared memory
+//            (129..2048) or a CTA working in global memory (more)
 // A sample id here is ((b*A + a)*P + p)*K + k)*S + s: a sample of all groups.
 constexpr int kScanTile = 4096;
+constexpr int kRowOffTail = 8;  // [0] scan total, [4..6] sort list counters
 
 struct BinLayout {
     int64_t rows_total;  // B * rows
     int64_t nsid;        // B*A*P*K*S
     int64_t ncap;        // 4 * nsid
     int64_t ntiles;
-    size_t off_row_off, off_tile_sum, off_rec, off_pos4, off_dpix, bytes;
+    size_t off_row_off, off_tile_sum, off_rec, off_pos4, off_dpix, off_lists, bytes;
+    // Capacities of the three row lists of the deterministic sort (rows
+    // with more than 8, 128 and 2048 records).
+    int64_t cap_m, cap_s, cap_g;
 };
 BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, int64_t S, int64_t G);
 
@@ -105,6 +114,11 @@ struct BinArgs {
     int32_t *pos4;
     float *dpix;
     int64_t rows_total, nsid, ncap, ntiles;
+    // Deterministic mode: the row lists of the per-row sort, and their three
+    // counters (zeroed with row_off; NULL sort_lists = no sort).
+    int32_t *sort_lists;
+    int32_t *sort_counts;
+    int64_t cap_m, cap_s, cap_g;
 };
 
 // `chunks` = D * sizeof(feature) / 16, one of 1, 2, 4, 8.

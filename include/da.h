@@ -123,8 +123,9 @@ da_status da_forward(const da_dims *dims,
 /*
  * Size in bytes of the device workspace that the binned path of da_backward
  * needs for `dims` (stored in *bytes). It depends on the sizes only:
- * about 4*B*A*P*K*S*(12 + 4*G) bytes plus 4 bytes per feature row. This is
- * about 300 MB for B=6, A=900, P=13, K=6, S=4, G=8.
+ * about 4*B*A*P*K*S*(12.5 + 4*G) bytes plus 4 bytes per feature row. This
+ * is about 300 MB for B=6, A=900, P=13, K=6, S=4, G=8. The same workspace
+ * serves both modes of da_backward_ex.
  * Returns DA_ERR_UNSUPPORTED when 4*B*A*P*K*S or B*num_feat_rows does not
  * fit in int32. It also returns DA_ERR_UNSUPPORTED unless C is a power of
  * two in [8, 256] and D is a multiple of 8. The scatter path (no workspace)
@@ -141,7 +142,8 @@ da_status da_backward_workspace_size(const da_dims *dims, size_t *bytes);
  *   grad_feat   device [B, num_feat_rows, C] fp32 for both feature types,
  *               16-byte aligned; overwritten. Rows outside every map get 0.
  *               Contributions are summed in an unspecified order, so the
- *               bits may differ from run to run.
+ *               bits may differ from run to run (see da_backward_ex for a
+ *               deterministic mode).
  *   grad_loc    device [B, A, P, K, 2] fp32, 4-byte aligned; overwritten.
  *               [...,0] is dL/dx (scaled by W), [...,1] is dL/dy (scaled by H).
  *   grad_weight device [B, A, P, K, S, G] fp32, 4-byte aligned; overwritten.
@@ -171,6 +173,36 @@ da_status da_backward(const da_dims *dims,
                       void *workspace,
                       size_t workspace_bytes,
                       da_stream_t stream);
+
+/*
+ * da_backward_ex: da_backward with option flags.
+ *
+ *   DA_BACKWARD_DETERMINISTIC  grad_feat, grad_loc and grad_weight are the
+ *       same bit for bit on every run with the same inputs and sizes. Needs
+ *       the binned path (a workspace); without one the call returns
+ *       DA_ERR_WORKSPACE. The corner contributions of every feature row are
+ *       put in a fixed order (by sample and corner) before they are summed.
+ *       This costs four more kernels and a few percent of the backward's
+ *       time, more when many samples crowd a few pixels.
+ *
+ * Other arguments are those of da_backward. Unknown flags give
+ * DA_ERR_SHAPE. da_backward(...) is da_backward_ex(..., 0, stream).
+ */
+#define DA_BACKWARD_DETERMINISTIC 1u
+da_status da_backward_ex(const da_dims *dims,
+                         const void *mc_ms_feat,
+                         const int32_t *spatial_shape,
+                         const int32_t *level_start_index,
+                         const float *sampling_location,
+                         const float *weights,
+                         const float *grad_out,
+                         float *grad_feat,
+                         float *grad_loc,
+                         float *grad_weight,
+                         void *workspace,
+                         size_t workspace_bytes,
+                         uint32_t flags,
+                         da_stream_t stream);
 
 /*
  * da_backward_noalloc: the binned backward, with its scratch in a fixed

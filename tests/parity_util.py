@@ -21,12 +21,19 @@ longest accumulation chain:
     a row's chunks, the four-corner combination);
   * grad_loc: kappa = D + S*G + 8 (the same, plus the sum over the S*G
     samples that share one location).
+grad_feat sums one product per record of its feature row, one fp32 rounding
+each, so its kappa is the row's record count plus 2. Rows of the standard
+workloads hold few records and need no such term. Tests that crowd
+thousands of samples onto a few pixels ask for it ("grad_feat" in
+kind_names) with the bound that holds for every row: a location puts at most
+one corner in a row, so a row holds at most A*P records, and kappa = A*P + 2.
 The oracle supplies M:
   * grad_weight: M is the oracle's grad_weight with |feat| and |grad_out|.
     Every product in it is then non-negative.
   * grad_loc: M comes from oracle.grad_loc_magnitude.
-A dropped corner, a wrong sign or a swapped axis moves an element by about M,
-far beyond kappa*u*M.
+A dropped corner, a wrong sign or a swapped axis moves an element by about M
+(by about M/n for a grad_feat row of n records), far beyond kappa*u*M.
+For grad_feat, M is the oracle's grad_feat with |weights| and |grad_out|.
 """
 from __future__ import annotations
 
@@ -68,7 +75,8 @@ U32 = 2.0 ** -24
 
 
 def conditioning_atol(inp, kind_names=("grad_loc", "grad_weight")):
-    """Per-element kappa*u*M for grad_loc and grad_weight (see the module doc)."""
+    """Per-element kappa*u*M for grad_loc, grad_weight and, when asked,
+    grad_feat (see the module doc)."""
     import oracle
     wl = inp.wl
     K, S = inp.spatial_shape.shape[0], inp.spatial_shape.shape[1]
@@ -83,6 +91,10 @@ def conditioning_atol(inp, kind_names=("grad_loc", "grad_weight")):
     if "grad_weight" in kind_names:
         _, _, m_gw = oracle.backward(afeat, *args, np.abs(go))
         res["grad_weight"] = (D + 8) * U32 * m_gw.astype(np.float64)
+    if "grad_feat" in kind_names:
+        A, P = inp.loc.shape[1], inp.loc.shape[2]
+        m_gf, _, _ = oracle.backward(feat, *args[:3], np.abs(inp.weights.numpy()), np.abs(go))
+        res["grad_feat"] = (A * P + 2) * U32 * m_gf.astype(np.float64)
     if "grad_loc" in kind_names:
         m_gl = oracle.grad_loc_magnitude(feat, *args, go)
         res["grad_loc"] = (D + S * G + 8) * U32 * m_gl.astype(np.float64)

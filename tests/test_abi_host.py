@@ -148,9 +148,12 @@ def test_workspace_size_and_errors(lib):
               num_pts=13, num_feat_rows=6 * 14960)
     assert lib.da_backward_workspace_size(ctypes.byref(d), ctypes.byref(n)) == DA_OK
     nsid = 6 * 900 * 13 * 6 * 4
-    # records (cid + weight), pos4, dpix for 8 groups: 4*nsid*(4+4) + 16*nsid + 4*nsid*8*4
-    assert n.value >= nsid * (32 + 16 + 128)
-    assert n.value < nsid * (32 + 16 + 128) + 8 * 1024 * 1024
+    # records (cid + weight), pos4, dpix for 8 groups: 4*nsid*(4+4) + 16*nsid + 4*nsid*8*4,
+    # plus the deterministic sort's row lists (rows of > 8, > 128, > 2048 records)
+    ncap = 4 * nsid
+    lists = 4 * (ncap // 9 + ncap // 129 + ncap // 2049 + 3)
+    assert n.value >= nsid * (32 + 16 + 128) + lists
+    assert n.value < nsid * (32 + 16 + 128) + lists + 4 * 1024 * 1024
     assert lib.da_backward_workspace_size(None, ctypes.byref(n)) == DA_ERR_NULL
     big = _dims(batch=1 << 20, num_anchors=1 << 10, num_pts=4)
     assert lib.da_backward_workspace_size(ctypes.byref(big), ctypes.byref(n)) == DA_ERR_UNSUPPORTED
@@ -158,6 +161,21 @@ def test_workspace_size_and_errors(lib):
     assert _bwd(lib, _dims(), ws=FAKE, ws_bytes=16) == 6
     assert _bwd(lib, _dims(), ws=FAKE + 16, ws_bytes=1 << 30) == 6
     assert lib.da_status_string(6) == b"DA_ERR_WORKSPACE"
+
+
+def test_backward_ex_flags(lib):
+    vp = ctypes.c_void_p
+    lib.da_backward_ex.argtypes = [ctypes.POINTER(da.DaDims)] + [vp] * 10 + [ctypes.c_size_t, ctypes.c_uint32, vp]
+    ss, ls = _tables()
+
+    def call(flags, ws=None, ws_bytes=0):
+        return lib.da_backward_ex(ctypes.byref(_dims()), FAKE, ss, ls, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws,
+                                  ws_bytes, flags, None)
+    assert call(2) == DA_ERR_SHAPE  # unknown flag
+    assert b"flags" in lib.da_last_error()
+    assert call(1) == 6  # deterministic without a workspace
+    assert b"DETERMINISTIC" in lib.da_last_error()
+    assert call(1, FAKE, 16) == 6  # workspace too small
 
 
 def test_empty_problem_needs_no_pointers(lib):
