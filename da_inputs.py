@@ -46,7 +46,7 @@ class Workload:
     num_groups: int
     num_anchors: int
     num_pts: int
-    feat_dtype: str  # "f32" or "bf16"
+    feat_dtype: str  # "f32", "bf16" or "f16"
     loc_kind: str  # "uniform" or "dcnv4_grid"
     loc_lo: float
     loc_hi: float
@@ -118,7 +118,7 @@ class Inputs:
         raw uint16 bit patterns of bf16 values."""
         if self.feat.dtype == torch.bfloat16:
             return self.feat.view(torch.int16).numpy().view(np.uint16)
-        return self.feat.numpy()
+        return self.feat.numpy()  # float32 or float16
 
 
 def map_tables(num_cams: int, shapes) -> Tuple[torch.Tensor, torch.Tensor]:
@@ -193,11 +193,53 @@ def make_inputs(wl: Workload | str, seed: Optional[int] = None) -> Inputs:
     feat = torch.randn(B, wl.num_feat_rows, C, generator=g, dtype=torch.float32)
     if wl.feat_dtype == "bf16":
         feat = feat.to(torch.bfloat16)  # round to nearest even
+    elif wl.feat_dtype == "f16":
+        feat = feat.to(torch.float16)  # round to nearest even
     ss, ls = map_tables(wl.num_cams, wl.shapes)
     loc = _draw_loc(wl, g)
     w = _draw_weights(wl, g)
     grad_out = torch.randn(B, wl.num_anchors, C, generator=g, dtype=torch.float32)
     return Inputs(wl, feat, ss, ls, loc, w, grad_out)
+
+
+@dataclasses.dataclass
+class FusedInputs:
+    """Inputs of the DCNv4 form: every group has its own points, and the
+    points and weights share one tensor (the DCNv4 page, "Solving the
+    problem: 1": one linear layer yields offsets and weights together)."""
+    wl: Workload
+    feat: torch.Tensor  # [B, rows, C]
+    spatial_shape: torch.Tensor  # [K, S, 2] int32
+    level_start_index: torch.Tensor  # [K, S] int32
+    loc_weight: torch.Tensor  # [B, A, G, P, K, 2 + S] float32: (x, y, w_0 .. w_{S-1})
+    grad_out: torch.Tensor  # [B, A, C] float32
+
+    def feat_numpy(self) -> np.ndarray:
+        return Inputs.feat_numpy(self)  # same rule: bf16 travels as its bits
+
+
+def make_fused_inputs(wl: Workload | str, seed: Optional[int] = None) -> FusedInputs:
+    """The workload's draws with per-group points: the location recipe runs
+    once per group (in group order), the weight recipe once for all groups,
+    and both are packed into loc_weight."""
+    if isinstance(wl, str):
+        wl = WORKLOADS[wl]
+    g = torch.Generator().manual_seed((wl.seed if seed is None else seed) + 1000)
+    B, C, G, S = wl.batch, wl.num_embeds, wl.num_groups, wl.num_scales
+    feat = torch.randn(B, wl.num_feat_rows, C, generator=g, dtype=torch.float32)
+    if wl.feat_dtype == "bf16":
+        feat = feat.to(torch.bfloat16)
+    elif wl.feat_dtype == "f16":
+        feat = feat.to(torch.float16)
+    ss, ls = map_tables(wl.num_cams, wl.shapes)
+    locs = [_draw_loc(wl, g) for _ in range(G)]  # G x [B, A, P, K, 2]
+    w = _draw_weights(wl, g)  # [B, A, P, K, S, G]
+    lw = torch.empty(B, wl.num_anchors, G, wl.num_pts, wl.num_cams, 2 + S, dtype=torch.float32)
+    for gi in range(G):
+        lw[:, :, gi, :, :, :2] = locs[gi]
+        lw[:, :, gi, :, :, 2:] = w[..., gi]
+    grad_out = torch.randn(B, wl.num_anchors, C, generator=g, dtype=torch.float32)
+    return FusedInputs(wl, feat, ss, ls, lw.contiguous(), grad_out)
 
 
 def small_variant(name: str, batch: int = 1, num_anchors: int = 24) -> Workload:

@@ -26,10 +26,10 @@ import torch
 
 from . import build as _build
 
-__all__ = ["da_forward", "da_backward", "backward_workspace_size", "DeformableAggregationFunction",
-           "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
+__all__ = ["da_forward", "da_backward", "da_forward_fused", "da_backward_fused", "backward_workspace_size",
+           "DeformableAggregationFunction", "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
 
-DA_F32, DA_BF16 = 0, 1
+DA_F32, DA_BF16, DA_F16 = 0, 1, 2
 _STATUS = {0: "DA_OK", 1: "DA_ERR_NULL", 2: "DA_ERR_SHAPE", 3: "DA_ERR_ALIGN",
            4: "DA_ERR_UNSUPPORTED", 5: "DA_ERR_CUDA", 6: "DA_ERR_WORKSPACE"}
 
@@ -76,6 +76,10 @@ def load_library():
     lib.da_backward_ex.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                    ctypes.c_size_t, ctypes.c_uint32, vp]
     lib.da_backward_ex.restype = ctypes.c_int
+    lib.da_forward_fused.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp]
+    lib.da_forward_fused.restype = ctypes.c_int
+    lib.da_backward_fused.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+    lib.da_backward_fused.restype = ctypes.c_int
     lib.da_backward_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
     lib.da_backward_workspace_size.restype = ctypes.c_int
     lib.da_status_string.argtypes = [ctypes.c_int]
@@ -147,8 +151,10 @@ def _dims(feat: torch.Tensor, ss: torch.Tensor, loc: torch.Tensor, weights: torc
         dt = DA_F32
     elif feat.dtype == torch.bfloat16:
         dt = DA_BF16
+    elif feat.dtype == torch.float16:
+        dt = DA_F16
     else:
-        raise TypeError("mc_ms_feat must be float32 or bfloat16")
+        raise TypeError("mc_ms_feat must be float32, bfloat16 or float16")
     if loc.dtype != torch.float32 or weights.dtype != torch.float32:
         raise TypeError("sampling_location and weights must be float32")
     return DaDims(B, K, S, C, G, A, P, dt, rows)
@@ -285,7 +291,7 @@ class HostPipeline:
 
     def shapes(self):
         d = self.dims
-        fdt = torch.bfloat16 if d.feat_dtype == DA_BF16 else torch.float32
+        fdt = {DA_BF16: torch.bfloat16, DA_F16: torch.float16}.get(d.feat_dtype, torch.float32)
         S, G = d.num_scales, d.num_groups
         B, A, P, K, C = d.batch, d.num_anchors, d.num_pts, d.num_cams, d.num_embeds
         return {"mc_ms_feat": ((B, d.num_feat_rows, C), fdt),
@@ -340,6 +346,62 @@ class HostPipeline:
             self.close()
         except Exception:
             pass
+
+
+def _dims_fused(feat: torch.Tensor, ss: torch.Tensor, loc_weight: torch.Tensor) -> DaDims:
+    if loc_weight.dim() != 6:
+        raise ValueError("loc_weight must be [B, A, G, P, K, 2 + S]")
+    B, A, G, P, K, E = loc_weight.shape
+    if ss.dim() != 3 or ss.shape[0] != K or ss.shape[2] != 2 or E != 2 + ss.shape[1]:
+        raise ValueError("spatial_shape must be [K, S, 2] with loc_weight's last dim 2 + S")
+    if loc_weight.dtype != torch.float32:
+        raise TypeError("loc_weight must be float32")
+    # The standard dims, read off stand-in shapes.
+    d = _dims(feat, ss, torch.empty(B, A, P, K, 2, device="meta"),
+              torch.empty(B, A, P, K, ss.shape[1], G, device="meta"))
+    return d
+
+
+def da_forward_fused(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index, loc_weight: torch.Tensor,
+                     out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """The DCNv4 form (da_forward_fused): per-group points fused with their
+    weights, loc_weight [B, A, G, P, K, 2 + S] = (x, y, w_0 .. w_{S-1})."""
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims_fused(mc_ms_feat, ss, loc_weight)
+    if out is None:
+        out = torch.empty(d.batch, d.num_anchors, d.num_embeds, device=mc_ms_feat.device, dtype=torch.float32)
+    elif out.shape != (d.batch, d.num_anchors, d.num_embeds) or out.dtype != torch.float32:
+        raise ValueError("out must be float32 [B, A, C]")
+    _check(lib.da_forward_fused(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
+                                ls.data_ptr() if ls.numel() else None, _dptr(loc_weight), _dptr(out),
+                                _stream_handle(stream)))
+    return out
+
+
+def da_backward_fused(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index, loc_weight: torch.Tensor,
+                      grad_out: torch.Tensor, grad_feat: Optional[torch.Tensor] = None,
+                      grad_loc_weight: Optional[torch.Tensor] = None,
+                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
+    """Backward of the DCNv4 form; returns (grad_feat fp32, grad_loc_weight)."""
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims_fused(mc_ms_feat, ss, loc_weight)
+    dev = mc_ms_feat.device
+    if tuple(grad_out.shape) != (d.batch, d.num_anchors, d.num_embeds) or grad_out.dtype != torch.float32:
+        raise ValueError("grad_out must be float32 [B, A, C]")
+    if grad_feat is None:
+        grad_feat = torch.empty(mc_ms_feat.shape, device=dev, dtype=torch.float32)
+    if grad_loc_weight is None:
+        grad_loc_weight = torch.empty(loc_weight.shape, device=dev, dtype=torch.float32)
+    if grad_feat.shape != mc_ms_feat.shape or grad_feat.dtype != torch.float32:
+        raise ValueError("grad_feat must be float32 with mc_ms_feat's shape")
+    if grad_loc_weight.shape != loc_weight.shape or grad_loc_weight.dtype != torch.float32:
+        raise ValueError("grad_loc_weight must be float32 with loc_weight's shape")
+    _check(lib.da_backward_fused(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
+                                 ls.data_ptr() if ls.numel() else None, _dptr(loc_weight), _dptr(grad_out),
+                                 _dptr(grad_feat), _dptr(grad_loc_weight), None, 0, _stream_handle(stream)))
+    return grad_feat, grad_loc_weight
 
 
 class DeformableAggregationFunction(torch.autograd.Function):

@@ -54,7 +54,7 @@ da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const
     if (d.num_embeds < 1 || d.num_groups < 1 || d.num_embeds % d.num_groups != 0)
         return fail(DA_ERR_SHAPE, "num_embeds (%d) must be a positive multiple of num_groups (%d)",
                     d.num_embeds, d.num_groups);
-    if (d.feat_dtype != DA_F32 && d.feat_dtype != DA_BF16)
+    if (d.feat_dtype != DA_F32 && d.feat_dtype != DA_BF16 && d.feat_dtype != DA_F16)
         return fail(DA_ERR_SHAPE, "unknown feat_dtype %d", d.feat_dtype);
     if (d.num_feat_rows < 0 || d.num_feat_rows > DA_MAX_ROWS)
         return fail(DA_ERR_SHAPE, "num_feat_rows %lld outside [0, %d]",
@@ -64,7 +64,7 @@ da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const
         return fail(DA_ERR_UNSUPPORTED, "num_cams*num_scales = %lld exceeds %d",
                     static_cast<long long>(nmaps), DA_MAX_MAPS);
     const int D = d.num_embeds / d.num_groups;
-    const int elem = d.feat_dtype == DA_BF16 ? 2 : 4;
+    const int elem = d.feat_dtype == DA_F32 ? 4 : 2;
     const int row_bytes = D * elem;
     if (row_bytes != 16 && row_bytes != 32 && row_bytes != 64 && row_bytes != 128)
         return fail(DA_ERR_UNSUPPORTED, "group width D*elem = %d bytes; supported: 16, 32, 64, 128",
@@ -162,6 +162,102 @@ da_status binned_layout(const da_dims &d, da::BinLayout &L)
     return DA_OK;
 }
 
+// The part of both forward entry points after the layout-specific checks.
+da_status forward_impl(const da_dims &d, da::FwdArgs &a, int chunks, float *out, da_stream_t stream)
+{
+    const int64_t n_out = static_cast<int64_t>(a.pb.num_ba) * a.pb.C;
+    if (n_out > 0 && !out) return fail(DA_ERR_NULL, "out is NULL");
+    if (!aligned(out, 16)) return fail(DA_ERR_ALIGN, "out must be 16-byte aligned");
+    a.out = out;
+    if (n_out == 0) return DA_OK;
+    const cudaError_t e = da::launch_forward(a, d.feat_dtype, chunks, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
+    return DA_OK;
+}
+
+// The part of every backward entry point after the layout-specific checks
+// (a.grad_loc and a.grad_weight are set and checked).
+da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const float *grad_out, float *grad_feat,
+                        void *workspace, size_t workspace_bytes, uint32_t flags, da_stream_t stream)
+{
+    if (flags & ~static_cast<uint32_t>(DA_BACKWARD_DETERMINISTIC))
+        return fail(DA_ERR_SHAPE, "unknown flags 0x%x", flags);
+    const bool deterministic = (flags & DA_BACKWARD_DETERMINISTIC) != 0;
+    if (deterministic && !workspace && !workspace_bytes)
+        return fail(DA_ERR_WORKSPACE, "DA_BACKWARD_DETERMINISTIC needs the binned path's workspace");
+    const da::Problem &pb = a.pb;
+    const int64_t n_out = static_cast<int64_t>(pb.num_ba) * pb.C;
+    const int64_t n_gf = static_cast<int64_t>(pb.B) * pb.rows * pb.C;
+    if (n_out > 0 && !grad_out) return fail(DA_ERR_NULL, "grad_out is NULL");
+    if (n_gf > 0 && !grad_feat) return fail(DA_ERR_NULL, "grad_feat is NULL");
+    if (!aligned(grad_out, 16)) return fail(DA_ERR_ALIGN, "grad_out must be 16-byte aligned");
+    if (!aligned(grad_feat, 16)) return fail(DA_ERR_ALIGN, "grad_feat must be 16-byte aligned");
+    // The per-CTA grad_loc staging area of the scatter path must fit in
+    // shared memory.
+    const size_t smem = da::scatter_smem_bytes(pb);
+    if (smem > 200 * 1024)
+        return fail(DA_ERR_UNSUPPORTED, "num_pts = %d too large for the grad_loc staging area", pb.P);
+    a.grad_out = grad_out;
+    a.grad_feat = grad_feat;
+    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (workspace || workspace_bytes) {
+        da::BinLayout L;
+        da_status st = binned_layout(d, L);
+        if (st != DA_OK) return st;
+        if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.bytes)
+            return fail(DA_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)",
+                        L.bytes, workspace_bytes);
+        char *ws = static_cast<char *>(workspace);
+        da::BinArgs w{};
+        w.row_off = reinterpret_cast<int32_t *>(ws + L.off_row_off);
+        w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
+        w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
+        w.pos4 = reinterpret_cast<int32_t *>(ws + L.off_pos4);
+        w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
+        w.rows_total = L.rows_total;
+        w.nsid = L.nsid;
+        w.ncap = L.ncap;
+        w.ntiles = L.ntiles;
+        if (deterministic) {
+            w.sort_lists = reinterpret_cast<int32_t *>(ws + L.off_lists);
+            w.sort_counts = w.row_off + L.ntiles * da::kScanTile + 4;
+            w.cap_m = L.cap_m;
+            w.cap_s = L.cap_s;
+            w.cap_g = L.cap_g;
+        }
+        const cudaError_t e = da::launch_backward_binned(a, w, d.feat_dtype, s);
+        if (e != cudaSuccess) return cuda_fail(e, "binned backward launch");
+        return DA_OK;
+    }
+    cudaError_t e = da::launch_zero_fill(grad_feat, n_gf, s);
+    if (e != cudaSuccess) return cuda_fail(e, "grad_feat zero-fill");
+    if (n_out == 0) return DA_OK;
+    e = da::launch_backward(a, d.feat_dtype, chunks, s);
+    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+    return DA_OK;
+}
+
+// Checks of the fused per-group layout: loc_weight [B,A,G,P,K,2+S] fp32.
+da_status prepare_fused(const da_dims *dims, const void *feat, const int32_t *spatial_shape,
+                        const int32_t *level_start_index, const float *loc_weight, da::Problem &pb, int &chunks)
+{
+    da_status st = da::prepare_shape(dims, spatial_shape, level_start_index, pb, chunks);
+    if (st != DA_OK) return st;
+    const int64_t n_feat = static_cast<int64_t>(dims->batch) * dims->num_feat_rows * dims->num_embeds;
+    const int64_t n_lw = static_cast<int64_t>(pb.num_ba) * pb.G * pb.pk * (2 + pb.S);
+    if (static_cast<int64_t>(pb.num_ba) * pb.G * pb.pk > INT32_MAX)
+        return fail(DA_ERR_UNSUPPORTED, "batch*anchors*groups*pts*cams exceeds int32");
+    if (n_feat > 0 && !feat) return fail(DA_ERR_NULL, "mc_ms_feat is NULL");
+    if (n_lw > 0 && pb.pks > 0 && !loc_weight) return fail(DA_ERR_NULL, "loc_weight is NULL");
+    if (!aligned(feat, 16)) return fail(DA_ERR_ALIGN, "mc_ms_feat must be 16-byte aligned");
+    if (!aligned(loc_weight, 4)) return fail(DA_ERR_ALIGN, "loc_weight must be 4-byte aligned");
+    pb.feat = feat;
+    pb.loc = loc_weight;
+    pb.weights = nullptr;
+    pb.fused = 1;
+    return DA_OK;
+}
+
 // Device address of g_noalloc_scratch on the current device.
 constexpr int kMaxDevices = 256;
 std::mutex g_noalloc_mu;
@@ -197,14 +293,7 @@ da_status da_forward(const da_dims *dims, const void *mc_ms_feat, const int32_t 
     da_status st = prepare(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location,
                            weights, a.pb, chunks);
     if (st != DA_OK) return st;
-    const int64_t n_out = static_cast<int64_t>(a.pb.num_ba) * a.pb.C;
-    if (n_out > 0 && !out) return fail(DA_ERR_NULL, "out is NULL");
-    if (!aligned(out, 16)) return fail(DA_ERR_ALIGN, "out must be 16-byte aligned");
-    a.out = out;
-    if (n_out == 0) return DA_OK;
-    const cudaError_t e = da::launch_forward(a, dims->feat_dtype, chunks, reinterpret_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "forward launch");
-    return DA_OK;
+    return forward_impl(*dims, a, chunks, out, stream);
 }
 
 da_status da_backward_workspace_size(const da_dims *dims, size_t *bytes)
@@ -237,74 +326,52 @@ da_status da_backward_ex(const da_dims *dims, const void *mc_ms_feat, const int3
                          float *grad_weight, void *workspace, size_t workspace_bytes, uint32_t flags,
                          da_stream_t stream)
 {
-    if (flags & ~static_cast<uint32_t>(DA_BACKWARD_DETERMINISTIC))
-        return fail(DA_ERR_SHAPE, "unknown flags 0x%x", flags);
-    const bool deterministic = (flags & DA_BACKWARD_DETERMINISTIC) != 0;
-    if (deterministic && !workspace && !workspace_bytes)
-        return fail(DA_ERR_WORKSPACE, "DA_BACKWARD_DETERMINISTIC needs the binned path's workspace");
     da::BwdArgs a{};
     int chunks = 0;
     da_status st = prepare(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location,
                            weights, a.pb, chunks);
     if (st != DA_OK) return st;
     const da::Problem &pb = a.pb;
-    const int64_t n_out = static_cast<int64_t>(pb.num_ba) * pb.C;
-    const int64_t n_gf = static_cast<int64_t>(pb.B) * pb.rows * pb.C;
     const int64_t n_gl = static_cast<int64_t>(pb.num_ba) * pb.pk * 2;
     const int64_t n_gw = static_cast<int64_t>(pb.num_ba) * pb.pks * pb.G;
-    if (n_out > 0 && !grad_out) return fail(DA_ERR_NULL, "grad_out is NULL");
-    if (n_gf > 0 && !grad_feat) return fail(DA_ERR_NULL, "grad_feat is NULL");
     if (n_gl > 0 && !grad_loc) return fail(DA_ERR_NULL, "grad_loc is NULL");
     if (n_gw > 0 && !grad_weight) return fail(DA_ERR_NULL, "grad_weight is NULL");
-    if (!aligned(grad_out, 16)) return fail(DA_ERR_ALIGN, "grad_out must be 16-byte aligned");
-    if (!aligned(grad_feat, 16)) return fail(DA_ERR_ALIGN, "grad_feat must be 16-byte aligned");
     if (!aligned(grad_loc, 4)) return fail(DA_ERR_ALIGN, "grad_loc must be 4-byte aligned");
     if (!aligned(grad_weight, 4)) return fail(DA_ERR_ALIGN, "grad_weight must be 4-byte aligned");
-    // The per-CTA grad_loc staging area of the scatter path must fit in
-    // shared memory.
-    const int64_t smem = static_cast<int64_t>(pb.anchors_per_cta) * pb.P * 2 * 4;
-    if (smem > 200 * 1024)
-        return fail(DA_ERR_UNSUPPORTED, "num_pts = %d too large for the grad_loc staging area", pb.P);
-    a.grad_out = grad_out;
-    a.grad_feat = grad_feat;
     a.grad_loc = grad_loc;
     a.grad_weight = grad_weight;
-    const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (workspace || workspace_bytes) {
-        da::BinLayout L;
-        st = binned_layout(*dims, L);
-        if (st != DA_OK) return st;
-        if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.bytes)
-            return fail(DA_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)",
-                        L.bytes, workspace_bytes);
-        char *ws = static_cast<char *>(workspace);
-        da::BinArgs w{};
-        w.row_off = reinterpret_cast<int32_t *>(ws + L.off_row_off);
-        w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
-        w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
-        w.pos4 = reinterpret_cast<int32_t *>(ws + L.off_pos4);
-        w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
-        w.rows_total = L.rows_total;
-        w.nsid = L.nsid;
-        w.ncap = L.ncap;
-        w.ntiles = L.ntiles;
-        if (deterministic) {
-            w.sort_lists = reinterpret_cast<int32_t *>(ws + L.off_lists);
-            w.sort_counts = w.row_off + L.ntiles * da::kScanTile + 4;
-            w.cap_m = L.cap_m;
-            w.cap_s = L.cap_s;
-            w.cap_g = L.cap_g;
-        }
-        const cudaError_t e = da::launch_backward_binned(a, w, dims->feat_dtype, s);
-        if (e != cudaSuccess) return cuda_fail(e, "binned backward launch");
-        return DA_OK;
-    }
-    cudaError_t e = da::launch_zero_fill(grad_feat, n_gf, s);
-    if (e != cudaSuccess) return cuda_fail(e, "grad_feat zero-fill");
-    if (n_out == 0) return DA_OK;
-    e = da::launch_backward(a, dims->feat_dtype, chunks, s);
-    if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    return DA_OK;
+    return backward_impl(*dims, a, chunks, grad_out, grad_feat, workspace, workspace_bytes, flags, stream);
+}
+
+da_status da_forward_fused(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                           const int32_t *level_start_index, const float *loc_weight, float *out,
+                           da_stream_t stream)
+{
+    da::FwdArgs a{};
+    int chunks = 0;
+    const da_status st = prepare_fused(dims, mc_ms_feat, spatial_shape, level_start_index, loc_weight, a.pb, chunks);
+    if (st != DA_OK) return st;
+    return forward_impl(*dims, a, chunks, out, stream);
+}
+
+da_status da_backward_fused(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                            const int32_t *level_start_index, const float *loc_weight, const float *grad_out,
+                            float *grad_feat, float *grad_loc_weight, void *workspace, size_t workspace_bytes,
+                            da_stream_t stream)
+{
+    da::BwdArgs a{};
+    int chunks = 0;
+    const da_status st = prepare_fused(dims, mc_ms_feat, spatial_shape, level_start_index, loc_weight, a.pb, chunks);
+    if (st != DA_OK) return st;
+    const da::Problem &pb = a.pb;
+    const int64_t n_glw = static_cast<int64_t>(pb.num_ba) * pb.G * pb.pk * (2 + pb.S);
+    if (n_glw > 0 && !grad_loc_weight) return fail(DA_ERR_NULL, "grad_loc_weight is NULL");
+    if (!aligned(grad_loc_weight, 4)) return fail(DA_ERR_ALIGN, "grad_loc_weight must be 4-byte aligned");
+    if (workspace || workspace_bytes)
+        return fail(DA_ERR_UNSUPPORTED, "the fused layout has the scatter backward only (pass no workspace)");
+    a.grad_loc = grad_loc_weight;
+    a.grad_weight = nullptr;
+    return backward_impl(*dims, a, chunks, grad_out, grad_feat, nullptr, 0, 0u, stream);
 }
 
 da_status da_backward_noalloc(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,

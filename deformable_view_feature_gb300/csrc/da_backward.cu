@@ -24,6 +24,9 @@
 //   * grad_loc[b,a,p,k] sums over s and g, all inside the CTA that owns view
 //     (b, k, a). It is accumulated with shared-memory atomics and stored
 //     once.
+// With FUSED (per-group locations, one loc_weight tensor [B,A,G,P,K,2+S]),
+// grad_loc is kept per group (summed over s only), and both gradients land
+// in one grad_loc_weight tensor of the same layout.
 #include "da_internal.cuh"
 
 namespace da {
@@ -81,7 +84,7 @@ __device__ __forceinline__ void row_sum_store(const float (&d)[4], int chunk, fl
 // are already there. Every output element still has one owner:
 //   * grad_weight and grad_loc are per camera;
 //   * grad_feat rows belong to one camera's maps.
-template <typename T, int CH>
+template <typename T, int CH, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
 {
     using Ck = Chunk<T>;
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
     // grad_x = sum ax_i d_i, grad_y = sum ay_i d_i.
     __shared__ __align__(16) float4 etab[kWarps][32][3];
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
-    extern __shared__ float gl_s[];                             // [views_per_cta][P][2]
+    extern __shared__ float gl_s[];  // [views_per_cta][P][2], or [views_per_cta][G][P][2] if FUSED
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -113,7 +116,8 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
     const uint32_t grow_bytes = static_cast<uint32_t>(pb.C) * 4;  // grad_feat row pitch
 
     stage_maps(pb, maps_s);
-    const int nloc = nv * pb.P * 2;
+    const int gl_groups = FUSED ? pb.G : 1;
+    const int nloc = nv * gl_groups * pb.P * 2;
     for (int i = threadIdx.x; i < nloc; i += kThreads) gl_s[i] = 0.f;
     __syncthreads();
 
@@ -156,9 +160,9 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
                     const int j = j0 + lane;
                     const int p = static_cast<int>(pb.div_S.div(j));
                     const int s = j - p * pb.S;
-                    const int64_t bapk = (ba * pb.P + p) * pb.K + k;
-                    const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + bapk * 2);
-                    const float w = pb.weights[(bapk * pb.S + s) * pb.G + g];
+                    float2 xy;
+                    float w;
+                    sample_xyw<FUSED>(pb, ba, g, p * pb.K + k, s, xy, w);
                     const MapInfo m = maps_s[k * pb.S + s];
                     Footprint f;
                     footprint(xy.x, xy.y, m, f);
@@ -217,44 +221,61 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
                 const float4 ax = etab[warp][lane][1];
                 const float4 ay = etab[warp][lane][2];
                 const float gweight = cw.x * dd.x + cw.y * dd.y + cw.z * dd.z + cw.w * dd.w;
-                args.grad_weight[(((ba * pb.P + p) * pb.K + k) * pb.S + s) * pb.G + g] = gweight;
+                if constexpr (FUSED)
+                    args.grad_loc[((ba * pb.G + g) * pb.pk + p * pb.K + k) * (2 + pb.S) + 2 + s] = gweight;
+                else
+                    args.grad_weight[(((ba * pb.P + p) * pb.K + k) * pb.S + s) * pb.G + g] = gweight;
                 const float gx = ax.x * dd.x + ax.y * dd.y + ax.z * dd.z + ax.w * dd.w;
                 const float gy = ay.x * dd.x + ay.y * dd.y + ay.z * dd.z + ay.w * dd.w;
-                atomicAdd(&gl_s[(vloc * pb.P + p) * 2 + 0], gx);
-                atomicAdd(&gl_s[(vloc * pb.P + p) * 2 + 1], gy);
+                const int gslot = ((vloc * gl_groups + (FUSED ? g : 0)) * pb.P + p) * 2;
+                atomicAdd(&gl_s[gslot + 0], gx);
+                atomicAdd(&gl_s[gslot + 1], gy);
             }
             __syncwarp();
         }
     }
     __syncthreads();
     // grad_loc[b,a,p,k,:] for the CTA's views: a stride of K pairs between p.
+    // (FUSED: grad_loc_weight[b,a,g,p,k,0..1].)
     for (int i = threadIdx.x; i < nloc; i += kThreads) {
-        const int vloc = i / (pb.P * 2);
-        const int r = i - vloc * pb.P * 2;
+        const int vg = i / (pb.P * 2);  // vloc * gl_groups + g
+        const int r = i - vg * pb.P * 2;
         const int p = r >> 1;
+        const int vloc = vg / gl_groups;
+        const int g = vg - vloc * gl_groups;
         const int view = v0 + vloc;
         const int bk = static_cast<int>(pb.div_A.div(view));
         const int a = view - bk * pb.A;
         const int b = static_cast<int>(pb.div_K.div(bk));
         const int k = bk - b * pb.K;
-        args.grad_loc[(((static_cast<int64_t>(b) * pb.A + a) * pb.P + p) * pb.K + k) * 2 + (r & 1)] = gl_s[i];
+        const int64_t ba = static_cast<int64_t>(b) * pb.A + a;
+        if constexpr (FUSED)
+            args.grad_loc[((ba * pb.G + g) * pb.pk + p * pb.K + k) * (2 + pb.S) + (r & 1)] = gl_s[i];
+        else
+            args.grad_loc[((ba * pb.P + p) * pb.K + k) * 2 + (r & 1)] = gl_s[i];
     }
+}
+
+template <typename T, int CH, bool FUSED>
+cudaError_t launch_layout(const BwdArgs &a, cudaStream_t st)
+{
+    const int64_t views = static_cast<int64_t>(a.pb.num_ba) * a.pb.K;
+    const int64_t grid = (views + a.pb.anchors_per_cta - 1) / a.pb.anchors_per_cta;
+    if (grid == 0) return cudaSuccess;
+    const size_t smem = scatter_smem_bytes(a.pb);
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(bwd_kernel<T, CH, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    bwd_kernel<T, CH, FUSED><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 template <typename T, int CH>
 cudaError_t launch(const BwdArgs &a, cudaStream_t st)
 {
-    const int64_t views = static_cast<int64_t>(a.pb.num_ba) * a.pb.K;
-    const int64_t grid = (views + a.pb.anchors_per_cta - 1) / a.pb.anchors_per_cta;
-    if (grid == 0) return cudaSuccess;
-    const size_t smem = static_cast<size_t>(a.pb.anchors_per_cta) * a.pb.P * 2 * sizeof(float);
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(bwd_kernel<T, CH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
-    bwd_kernel<T, CH><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return a.pb.fused ? launch_layout<T, CH, true>(a, st) : launch_layout<T, CH, false>(a, st);
 }
 
 template <typename T>
@@ -287,8 +308,11 @@ cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st)
 
 cudaError_t launch_backward(const BwdArgs &a, int feat_dtype, int chunks, cudaStream_t st)
 {
-    return feat_dtype == DA_BF16 ? dispatch_ch<Bf16Tag>(a, chunks, st)
-                                 : dispatch_ch<float>(a, chunks, st);
+    switch (feat_dtype) {
+        case DA_BF16: return dispatch_ch<Bf16Tag>(a, chunks, st);
+        case DA_F16: return dispatch_ch<F16Tag>(a, chunks, st);
+        default: return dispatch_ch<float>(a, chunks, st);
+    }
 }
 
 }  // namespace da

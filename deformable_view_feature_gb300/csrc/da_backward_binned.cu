@@ -564,6 +564,12 @@ __device__ __forceinline__ void load_feat8<Bf16Tag>(const void *p, float (&v)[8]
     Chunk<Bf16Tag>::unpack(__ldg(reinterpret_cast<const uint4 *>(p)), v);
 }
 
+template <>
+__device__ __forceinline__ void load_feat8<F16Tag>(const void *p, float (&v)[8])
+{
+    Chunk<F16Tag>::unpack(__ldg(reinterpret_cast<const uint4 *>(p)), v);
+}
+
 struct PullArgs {
     Problem pb;
     const float *grad_out;
@@ -825,7 +831,9 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     // 4. grad_feat and d
     if (w.rows_total > 0) {
         const PullArgs pa{pb, a.grad_out, a.grad_feat, w, 0, w.rows_total};
-        e = feat_dtype == DA_BF16 ? dispatch_pull<Bf16Tag>(pa, st) : dispatch_pull<float>(pa, st);
+        e = feat_dtype == DA_BF16  ? dispatch_pull<Bf16Tag>(pa, st)
+            : feat_dtype == DA_F16 ? dispatch_pull<F16Tag>(pa, st)
+                                   : dispatch_pull<float>(pa, st);
         if (e != cudaSuccess) return e;
     }
     // 5. grad_weight and grad_loc

@@ -2,7 +2,10 @@
 //
 // out[b,a,c] = sum_{p,k,s} weights[b,a,p,k,s,g] * bilinear(map (b,k,s), loc[b,a,p,k], c)
 // (page "Inside Sparse4D's CUDA core", §3.2 for the sample and §5.1 for the
-// dimensions summed over).
+// dimensions summed over). With FUSED, every group has its own location and
+// both come from one tensor: the DCNv4 form y_g = sum_k m_gk x_g(p_gk) of
+// the DCNv4 page ("Defining the problem"), whose offsets and weights one
+// linear layer produces together ("Solving the problem: 1").
 //
 // Work decomposition (the page's kernel uses one thread per sample; here a
 // warp owns one (b*A+a, g) task and its P*K*S samples):
@@ -32,7 +35,7 @@
 namespace da {
 namespace {
 
-template <typename T, int CH>
+template <typename T, int CH, bool FUSED>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 {
     using Ck = Chunk<T>;
@@ -81,9 +84,9 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                     const int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k
                     const int s = j - jk * pb.S;
                     const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
-                    const int64_t locid = static_cast<int64_t>(ba) * pb.pk + jk;  // (b,a,p,k)
-                    const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + locid * 2);
-                    const float w = pb.weights[(locid * pb.S + s) * pb.G + g];
+                    float2 xy;
+                    float w;
+                    sample_xyw<FUSED>(pb, ba, g, jk, s, xy, w);
                     Footprint f;
                     footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
 #pragma unroll
@@ -145,7 +148,10 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
 {
     const int64_t grid = sampling_grid(a.pb);
     if (grid == 0) return cudaSuccess;
-    fwd_kernel<T, CH><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
+    if (a.pb.fused)
+        fwd_kernel<T, CH, true><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
+    else
+        fwd_kernel<T, CH, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -165,8 +171,11 @@ cudaError_t dispatch_ch(const FwdArgs &a, int chunks, cudaStream_t st)
 
 cudaError_t launch_forward(const FwdArgs &a, int feat_dtype, int chunks, cudaStream_t st)
 {
-    return feat_dtype == DA_BF16 ? dispatch_ch<Bf16Tag>(a, chunks, st)
-                                 : dispatch_ch<float>(a, chunks, st);
+    switch (feat_dtype) {
+        case DA_BF16: return dispatch_ch<Bf16Tag>(a, chunks, st);
+        case DA_F16: return dispatch_ch<F16Tag>(a, chunks, st);
+        default: return dispatch_ch<float>(a, chunks, st);
+    }
 }
 
 }  // namespace da

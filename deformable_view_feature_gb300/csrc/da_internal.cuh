@@ -2,6 +2,7 @@
 // The public C ABI is include/da.h. Nothing here is exported.
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -41,6 +42,9 @@ struct FastDiv {
 // as a kernel parameter; the kernels copy the map table to shared memory.
 struct Problem {
     const void *feat;
+    // Standard layout: loc [B,A,P,K,2] and weights [B,A,P,K,S,G].
+    // Fused per-group layout (the DCNv4 form): loc points to
+    // loc_weight [B,A,G,P,K,2+S] = (x, y, w_0 .. w_{S-1}) and weights is NULL.
     const float *loc;
     const float *weights;
     int64_t rows;             // feature rows per batch item
@@ -50,6 +54,7 @@ struct Problem {
     int32_t num_ba;           // B*A
     int32_t anchors_per_cta;  // anchors (or views) owned by one CTA, all groups
     int32_t nmaps;            // K*S
+    int32_t fused;            // 1: the fused per-group layout
     FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS, div_rows;
     MapInfo maps[DA_MAX_MAPS];
 };
@@ -138,6 +143,13 @@ bool aligned(const void *p, uintptr_t a);
 da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const int32_t *level_start_index,
                         Problem &pb, int &chunks);
 
+// Dynamic shared memory of the scatter backward: the grad_loc staging area
+// of one CTA's views (per group in the fused layout).
+inline size_t scatter_smem_bytes(const Problem &pb)
+{
+    return static_cast<size_t>(pb.anchors_per_cta) * (pb.fused ? pb.G : 1) * pb.P * 2 * sizeof(float);
+}
+
 // Grid size that covers num_ba anchors, anchors_per_cta at a time.
 inline int64_t sampling_grid(const Problem &pb)
 {
@@ -145,6 +157,25 @@ inline int64_t sampling_grid(const Problem &pb)
 }
 
 // ------------------------------------------------------------------ device helpers
+
+// Location (x, y) and weight of the sample (b*A + a = ba, group g,
+// jk = p*K + k, scale s) in either layout (see Problem). In the fused layout
+// the entry of (ba, g, jk) holds 2 + S floats, so (x, y) need not be 8-byte
+// aligned and is read as two floats.
+template <bool FUSED>
+__device__ __forceinline__ void sample_xyw(const Problem &pb, int64_t ba, int g, int jk, int s, float2 &xy,
+                                           float &w)
+{
+    if constexpr (FUSED) {
+        const float *e = pb.loc + ((ba * pb.G + g) * pb.pk + jk) * (2 + pb.S);
+        xy = make_float2(e[0], e[1]);
+        w = e[2 + s];
+    } else {
+        const int64_t locid = ba * pb.pk + jk;
+        xy = *reinterpret_cast<const float2 *>(pb.loc + locid * 2);
+        w = pb.weights[(locid * pb.S + s) * pb.G + g];
+    }
+}
 
 // Bilinear footprint of one sample. The steps are those of the page "Inside
 // Sparse4D's CUDA core", §3.2:
@@ -221,7 +252,8 @@ __device__ __forceinline__ const char *row_addr(const char *base, int32_t row, u
     return base + static_cast<uint64_t>(static_cast<uint32_t>(row)) * row_bytes;
 }
 
-// The 16 bytes as floats: 4 fp32 values, or 8 bf16 values widened exactly.
+// The 16 bytes as floats: 4 fp32 values, or 8 bf16 or fp16 values widened
+// exactly.
 template <typename T>
 struct Chunk;
 
@@ -252,6 +284,24 @@ struct Chunk<Bf16Tag> {
         v[5] = __uint_as_float(r.z & 0xffff0000u);
         v[6] = __uint_as_float(r.w << 16);
         v[7] = __uint_as_float(r.w & 0xffff0000u);
+    }
+};
+
+struct F16Tag {};
+
+// 8 fp16 values widened exactly (every binary16 value is a binary32 value).
+template <>
+struct Chunk<F16Tag> {
+    static constexpr int kVec = 8;
+    __device__ __forceinline__ static void unpack(const uint4 &r, float (&v)[8])
+    {
+        const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&w[i]));
+            v[2 * i] = f.x;
+            v[2 * i + 1] = f.y;
+        }
     }
 };
 

@@ -180,7 +180,7 @@ da_status da_pipeline_create(const da_dims *dims, const int32_t *spatial_shape, 
     da_status st = da::prepare_shape(dims, spatial_shape, level_start_index, pb, chunks);
     if (st != DA_OK) return st;
     const da_dims d = *dims;
-    const size_t elem = d.feat_dtype == DA_BF16 ? 2 : 4;
+    const size_t elem = d.feat_dtype == DA_F32 ? 4 : 2;
     const size_t n_rows = static_cast<size_t>(d.batch) * static_cast<size_t>(d.num_feat_rows);
     const size_t n_samp = static_cast<size_t>(pb.num_ba) * static_cast<size_t>(pb.pk);  // (b,a,p,k)
 

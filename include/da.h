@@ -70,7 +70,9 @@ typedef enum da_status {
 
 typedef enum da_dtype {
     DA_F32 = 0,  /* IEEE binary32 features */
-    DA_BF16 = 1  /* bfloat16 features; all arithmetic and every other tensor stay fp32 */
+    DA_BF16 = 1, /* bfloat16 features; all arithmetic and every other tensor stay fp32 */
+    DA_F16 = 2   /* IEEE binary16 features (the half precision of the DCNv4 page,
+                    "Solving the problem: 2"); arithmetic and other tensors fp32 */
 } da_dtype;
 
 typedef struct da_dims {
@@ -203,6 +205,57 @@ da_status da_backward_ex(const da_dims *dims,
                          size_t workspace_bytes,
                          uint32_t flags,
                          da_stream_t stream);
+
+/*
+ * The DCNv4 form: per-group locations, fused with the weights in one tensor.
+ *
+ * The DCNv4 page ("Defining the problem") writes the operator as
+ * y_g(p0) = sum_k m_gk x_g(p0 + p_k + dp_gk): every group g of channels has
+ * its own sampling points and weights. Its step "Solving the problem: 1"
+ * produces offsets and weights with one linear layer, so they arrive in one
+ * tensor. Here, in the dimensions above:
+ *
+ *   loc_weight  device [B, A, G, P, K, 2 + S] fp32, 4-byte aligned. The entry
+ *               of (b, a, g, p, k) is (x, y, w_0, ..., w_{S-1}): the
+ *               normalised location of point p in camera k for group g (the
+ *               same at every scale), and its weight at each scale.
+ *   out[b,a,c]  = sum_{p,k,s} w_s(b,a,g,p,k) *
+ *                 bilinear(map (b,k,s), (x, y)(b,a,g,p,k), channel c),
+ *               with g = c / D; the bilinear step is da_forward's.
+ *
+ * Turning DCNv4's pixel offsets p0 + p_k + dp_gk into normalised locations
+ * is the caller's step: (x, y) = ((j + 0.5) / W, (i + 0.5) / H) for pixel
+ * (i, j), so a location on a pixel centre reads that pixel exactly.
+ *
+ * da_forward_fused: arguments and rules of da_forward, with loc_weight in
+ * place of sampling_location and weights.
+ *
+ * da_backward_fused: arguments and rules of da_backward's scatter path, with
+ * grad_loc_weight [B, A, G, P, K, 2 + S] fp32 (4-byte aligned, overwritten)
+ * in place of grad_loc and grad_weight: entries 0, 1 hold dL/dx, dL/dy
+ * (scaled by W and H, summed over the scales and the group's channels) and
+ * entry 2 + s holds dL/dw_s. The binned path does not serve this layout:
+ * workspace must be NULL and workspace_bytes 0 (else DA_ERR_UNSUPPORTED).
+ */
+da_status da_forward_fused(const da_dims *dims,
+                           const void *mc_ms_feat,
+                           const int32_t *spatial_shape,
+                           const int32_t *level_start_index,
+                           const float *loc_weight,
+                           float *out,
+                           da_stream_t stream);
+
+da_status da_backward_fused(const da_dims *dims,
+                            const void *mc_ms_feat,
+                            const int32_t *spatial_shape,
+                            const int32_t *level_start_index,
+                            const float *loc_weight,
+                            const float *grad_out,
+                            float *grad_feat,
+                            float *grad_loc_weight,
+                            void *workspace,
+                            size_t workspace_bytes,
+                            da_stream_t stream);
 
 /*
  * da_backward_noalloc: the binned backward, with its scratch in a fixed

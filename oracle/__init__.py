@@ -55,6 +55,10 @@ def _load():
         lib.dao_grad_loc_magnitude.argtypes = ([i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp,
                                                             i64, i64, vp])
         lib.dao_grad_loc_magnitude.restype = i32
+        lib.dao_forward_fused.argtypes = [i32] * 7 + [i64, vp, vp, vp, i32, vp, vp]
+        lib.dao_forward_fused.restype = i32
+        lib.dao_backward_fused.argtypes = [i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp, vp]
+        lib.dao_backward_fused.restype = i32
         lib.dao_bilinear.argtypes = [vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float]
         lib.dao_bilinear.restype = ctypes.c_double
         _lib = lib
@@ -67,12 +71,15 @@ def _ptr(a: np.ndarray) -> int:
 
 def _prep(feat, spatial_shape, level_start_index, loc, weights):
     feat = np.ascontiguousarray(feat)
+    # feat kind passed to the C oracle: 0 fp32, 1 bf16 bits, 2 fp16 bits
     if feat.dtype == np.uint16:
         bf16 = 1
+    elif feat.dtype == np.float16:
+        feat, bf16 = feat.view(np.uint16), 2
     elif feat.dtype == np.float32:
         bf16 = 0
     else:
-        raise TypeError("feat must be float32, or uint16 holding bf16 bits")
+        raise TypeError("feat must be float32, float16, or uint16 holding bf16 bits")
     ss = np.ascontiguousarray(spatial_shape, dtype=np.int32)
     ls = np.ascontiguousarray(level_start_index, dtype=np.int32)
     loc = np.ascontiguousarray(loc, dtype=np.float32)
@@ -143,6 +150,45 @@ def grad_loc_magnitude(feat, spatial_shape, level_start_index, loc, weights, gra
     if rc != 0:
         raise ValueError(f"oracle magnitude rejected its arguments (code {rc})")
     return mag
+
+
+def _prep_fused(feat, spatial_shape, level_start_index, loc_weight):
+    ss = np.ascontiguousarray(spatial_shape, dtype=np.int32)
+    S = ss.shape[1]
+    lw = np.ascontiguousarray(loc_weight, dtype=np.float32)
+    B, A, G, P, K, E = lw.shape
+    assert E == 2 + S, (E, S)
+    # The standard-layout checks with stand-in loc/weights of the right shapes.
+    feat, kind, ss, ls, _, _, dims = _prep(feat, ss, level_start_index, np.zeros((B, A, P, K, 2), np.float32),
+                                           np.zeros((B, A, P, K, S, G), np.float32))
+    return feat, kind, ss, ls, lw, dims
+
+
+def forward_fused(feat, spatial_shape, level_start_index, loc_weight) -> np.ndarray:
+    """The DCNv4 form (per-group locations fused with the weights):
+    loc_weight [B, A, G, P, K, 2 + S] -> out [B, A, C] float32."""
+    feat, kind, ss, ls, lw, dims = _prep_fused(feat, spatial_shape, level_start_index, loc_weight)
+    B, K, S, C, G, A, P, rows = dims
+    out = np.empty((B, A, C), dtype=np.float32)
+    rc = _load().dao_forward_fused(B, K, S, C, G, A, P, rows, _ptr(ss), _ptr(ls), _ptr(feat), kind, _ptr(lw),
+                                   _ptr(out))
+    if rc != 0:
+        raise ValueError(f"oracle fused forward rejected its arguments (code {rc})")
+    return out
+
+
+def backward_fused(feat, spatial_shape, level_start_index, loc_weight, grad_out):
+    """(grad_feat [B, rows, C], grad_loc_weight [B, A, G, P, K, 2 + S]) of the DCNv4 form."""
+    feat, kind, ss, ls, lw, dims = _prep_fused(feat, spatial_shape, level_start_index, loc_weight)
+    B, K, S, C, G, A, P, rows = dims
+    grad_out = np.ascontiguousarray(grad_out, dtype=np.float32)
+    gf = np.empty((B, rows, C), dtype=np.float32)
+    glw = np.empty(lw.shape, dtype=np.float32)
+    rc = _load().dao_backward_fused(B, K, S, C, G, A, P, rows, _ptr(ss), _ptr(ls), _ptr(feat), kind, _ptr(lw),
+                                    _ptr(grad_out), _ptr(gf), _ptr(glw))
+    if rc != 0:
+        raise ValueError(f"oracle fused backward rejected its arguments (code {rc})")
+    return gf, glw
 
 
 def bilinear(fmap: np.ndarray, c: int, x: float, y: float) -> float:

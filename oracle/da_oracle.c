@@ -94,15 +94,35 @@ static void corner_weights(const footprint *f, double cw[4])
     cw[3] = (double)f->lh * (double)f->lw;
 }
 
-static double feat_value(const void *feat, int feat_bf16, int64_t index)
+/* IEEE binary16 bits to double, from the format's definition: 1 sign bit,
+ * 5 exponent bits (bias 15), 10 fraction bits; exponent 0 holds zero and the
+ * subnormals (fraction * 2^-24), exponent 31 infinity and NaN. */
+static double f16_bits_to_double(uint16_t h)
 {
-    if (feat_bf16) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1f;
+    int m = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return sign ? -v : v;
+}
+
+/* feat_kind: 0 = fp32, 1 = bf16 bits, 2 = fp16 bits. */
+static double feat_value(const void *feat, int feat_kind, int64_t index)
+{
+    if (feat_kind == 1) {
         /* bf16 is the top half of an fp32 bit pattern: widening is exact. */
         uint32_t bits = (uint32_t)((const uint16_t *)feat)[index] << 16;
         float v;
         memcpy(&v, &bits, sizeof v);
         return (double)v;
     }
+    if (feat_kind == 2) return f16_bits_to_double(((const uint16_t *)feat)[index]);
     return (double)((const float *)feat)[index];
 }
 
@@ -131,7 +151,7 @@ static int check_dims(int B, int K, int S, int C, int G, int A, int P, int64_t r
  */
 int dao_forward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
                 const int32_t *shape, const int32_t *start,
-                const void *feat, int feat_bf16,
+                const void *feat, int feat_kind,
                 const float *loc, const float *weights,
                 int64_t ba_begin, int64_t ba_end, float *out)
 {
@@ -164,7 +184,7 @@ int dao_forward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
                             if (f.row[i] < 0) continue;
                             const int64_t base = (b * rows + f.row[i]) * C + (int64_t)g * D;
                             for (c = 0; c < D; ++c)
-                                val[c] += cw[i] * feat_value(feat, feat_bf16, base + c);
+                                val[c] += cw[i] * feat_value(feat, feat_kind, base + c);
                         }
                         for (c = 0; c < D; ++c) acc[g * D + c] += w * val[c];
                     }
@@ -186,7 +206,7 @@ int dao_forward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
  */
 int dao_backward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
                  const int32_t *shape, const int32_t *start,
-                 const void *feat, int feat_bf16,
+                 const void *feat, int feat_kind,
                  const float *loc, const float *weights, const float *grad_out,
                  int64_t ba_begin, int64_t ba_end,
                  float *grad_feat, float *grad_loc, float *grad_weight)
@@ -227,7 +247,7 @@ int dao_backward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
                             for (i = 0; i < 4; ++i) {
                                 if (f.row[i] < 0) continue;
                                 const int64_t idx = (b * rows + f.row[i]) * C + (int64_t)g * D + c;
-                                v[i] = feat_value(feat, feat_bf16, idx);
+                                v[i] = feat_value(feat, feat_kind, idx);
                                 gf[idx] += cw[i] * top_grad;
                             }
                             const double grad_w = lh * (v[3] - v[2]) + hh * (v[1] - v[0]);
@@ -249,6 +269,121 @@ int dao_backward(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
     for (e = 0; e < nfeat; ++e) grad_feat[e] = (float)gf[e];
     free(gf);
     free(gl);
+    return DAO_OK;
+}
+
+/*
+ * The DCNv4 form (page "DCNv4", "Defining the problem" and "Solving the
+ * problem: 1"): every group g has its own sampling points and weights,
+ *   y_g(p0) = sum_k m_gk x_g(p0 + p_k + dp_gk),
+ * here with the points given as normalised locations, one per camera, valid
+ * at every scale, and one weight per scale. The locations and weights share
+ * one tensor lw [B, A, G, P, K, 2 + S] = (x, y, w_0 .. w_{S-1}).
+ *   out[b,a,c] = sum over p,k,s of lw[b,a,g,p,k,2+s] *
+ *                bilinear(map (b,k,s), lw[b,a,g,p,k,0..1], c),  g = c / (C/G).
+ * The bilinear step and its precision are those of dao_forward.
+ */
+int dao_forward_fused(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
+                      const int32_t *shape, const int32_t *start,
+                      const void *feat, int feat_kind, const float *lw, float *out)
+{
+    if (!check_dims(B, K, S, C, G, A, P, rows, shape, start)) return DAO_ERR_ARGS;
+    const int D = C / G;
+    const int E = 2 + S;
+    int64_t ba;
+    for (ba = 0; ba < (int64_t)B * A; ++ba) {
+        const int64_t b = ba / A;
+        int g, p, k, s, c, i;
+        for (g = 0; g < G; ++g) {
+            double *acc = (double *)calloc((size_t)D, sizeof(double));
+            if (!acc) return DAO_ERR_NOMEM;
+            for (p = 0; p < P; ++p)
+                for (k = 0; k < K; ++k) {
+                    const float *e = lw + (((ba * G + g) * P + p) * K + k) * E;
+                    for (s = 0; s < S; ++s) {
+                        footprint f;
+                        double cw[4];
+                        make_footprint(e[0], e[1], shape[(k * S + s) * 2], shape[(k * S + s) * 2 + 1],
+                                       start[k * S + s], &f);
+                        corner_weights(&f, cw);
+                        const double m = e[2 + s];
+                        for (c = 0; c < D; ++c) {
+                            double val = 0.0;
+                            for (i = 0; i < 4; ++i)
+                                if (f.row[i] >= 0)
+                                    val += cw[i] * feat_value(feat, feat_kind,
+                                                              (b * rows + f.row[i]) * C + (int64_t)g * D + c);
+                            acc[c] += m * val;
+                        }
+                    }
+                }
+            for (c = 0; c < D; ++c) out[ba * C + (int64_t)g * D + c] = (float)acc[c];
+            free(acc);
+        }
+    }
+    return DAO_OK;
+}
+
+/*
+ * Backward of the DCNv4 form: the gradients of §4.1 of the Sparse4D page,
+ * kept per group. grad_lw has lw's layout: entries 0 and 1 hold dL/dx and
+ * dL/dy (scaled by W and H, summed over the scales and the group's
+ * channels), entry 2 + s holds dL/dw_s. grad_feat [B, rows, C] is written
+ * in full.
+ */
+int dao_backward_fused(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
+                       const int32_t *shape, const int32_t *start,
+                       const void *feat, int feat_kind, const float *lw, const float *grad_out,
+                       float *grad_feat, float *grad_lw)
+{
+    if (!check_dims(B, K, S, C, G, A, P, rows, shape, start)) return DAO_ERR_ARGS;
+    const int D = C / G;
+    const int E = 2 + S;
+    const int64_t nfeat = (int64_t)B * rows * C;
+    double *gf = (double *)calloc((size_t)(nfeat > 0 ? nfeat : 1), sizeof(double));
+    if (!gf) return DAO_ERR_NOMEM;
+    int64_t ba;
+    for (ba = 0; ba < (int64_t)B * A; ++ba) {
+        const int64_t b = ba / A;
+        int g, p, k, s, c, i;
+        for (g = 0; g < G; ++g)
+            for (p = 0; p < P; ++p)
+                for (k = 0; k < K; ++k) {
+                    const int64_t eoff = (((ba * G + g) * P + p) * K + k) * E;
+                    const float *e = lw + eoff;
+                    double gx = 0.0, gy = 0.0;
+                    for (s = 0; s < S; ++s) {
+                        const int32_t H = shape[(k * S + s) * 2];
+                        const int32_t W = shape[(k * S + s) * 2 + 1];
+                        footprint f;
+                        double cw[4];
+                        make_footprint(e[0], e[1], H, W, start[k * S + s], &f);
+                        corner_weights(&f, cw);
+                        const double m = e[2 + s];
+                        double gm = 0.0;
+                        for (c = 0; c < D; ++c) {
+                            const double go = grad_out[ba * C + (int64_t)g * D + c];
+                            const double top_grad = go * m;
+                            double v[4] = {0.0, 0.0, 0.0, 0.0};
+                            for (i = 0; i < 4; ++i) {
+                                if (f.row[i] < 0) continue;
+                                const int64_t idx = (b * rows + f.row[i]) * C + (int64_t)g * D + c;
+                                v[i] = feat_value(feat, feat_kind, idx);
+                                gf[idx] += cw[i] * top_grad;
+                            }
+                            gx += (double)W * (f.lh * (v[3] - v[2]) + f.hh * (v[1] - v[0])) * top_grad;
+                            gy += (double)H * (f.lw * (v[3] - v[1]) + f.hw * (v[2] - v[0])) * top_grad;
+                            gm += go * (cw[0] * v[0] + cw[1] * v[1] + cw[2] * v[2] + cw[3] * v[3]);
+                        }
+                        grad_lw[eoff + 2 + s] = (float)gm;
+                    }
+                    grad_lw[eoff + 0] = (float)gx;
+                    grad_lw[eoff + 1] = (float)gy;
+                }
+    }
+    int64_t j;
+    for (j = 0; j < nfeat; ++j) grad_feat[j] = (float)gf[j];
+    free(gf);
     return DAO_OK;
 }
 
@@ -280,7 +415,7 @@ double dao_bilinear(const float *map, int32_t H, int32_t W, int32_t C, int32_t c
  */
 int dao_grad_loc_magnitude(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
                            const int32_t *shape, const int32_t *start,
-                           const void *feat, int feat_bf16,
+                           const void *feat, int feat_kind,
                            const float *loc, const float *weights, const float *grad_out,
                            int64_t ba_begin, int64_t ba_end, float *mag)
 {
@@ -307,7 +442,7 @@ int dao_grad_loc_magnitude(int B, int K, int S, int C, int G, int A, int P, int6
                             double v[4] = {0.0, 0.0, 0.0, 0.0};
                             for (i = 0; i < 4; ++i)
                                 if (f.row[i] >= 0)
-                                    v[i] = fabs(feat_value(feat, feat_bf16,
+                                    v[i] = fabs(feat_value(feat, feat_kind,
                                                            (b * rows + f.row[i]) * C + (int64_t)g * D + c));
                             mx += (double)W * tg * (f.lh * (v[3] + v[2]) + f.hh * (v[1] + v[0]));
                             my += (double)H * tg * (f.lw * (v[3] + v[1]) + f.hw * (v[2] + v[0]));

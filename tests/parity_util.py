@@ -45,6 +45,10 @@ EPS32 = float(np.finfo(np.float32).eps)
 TOL = {
     "f32": {"out": (1e-5, 1e-6), "grad_feat": (1e-4, 1e-6), "grad_loc": (1e-4, 1e-6),
             "grad_weight": (1e-4, 1e-6)},
+    # fp16 features: the oracle reads the same fp16 values exactly widened and
+    # the kernels compute in fp32, so the fp32 bounds apply.
+    "f16": {"out": (1e-5, 1e-6), "grad_feat": (1e-4, 1e-6), "grad_loc": (1e-4, 1e-6),
+            "grad_weight": (1e-4, 1e-6)},
     "bf16": {"out": (2e-2, 1e-6), "grad_feat": (2e-2, 1e-6), "grad_loc": (2e-2, 1e-6),
              "grad_weight": (2e-2, 1e-6)},
 }

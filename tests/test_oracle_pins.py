@@ -392,6 +392,37 @@ def test_bf16_features_are_widened_exactly():
                                   oracle.forward(as_f32, *args))
 
 
+def test_f16_decoder_reads_every_bit_pattern_like_numpy():
+    # One 1x1 map whose single pixel holds all 65536 binary16 bit patterns as
+    # channels; a sample at the pixel centre with weight 1 returns them. numpy's
+    # float16 -> float64 conversion is the independent reference.
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    feat = bits.view(np.float16).reshape(1, 1, 65536)
+    ss = np.array([[[1, 1]]], np.int32)
+    ls = np.array([[0]], np.int32)
+    loc = np.full((1, 1, 1, 1, 2), 0.5, np.float32)
+    w = np.ones((1, 1, 1, 1, 1, 1), np.float32)
+    out = oracle.forward(feat, ss, ls, loc, w).reshape(-1)
+    want = feat.reshape(-1).astype(np.float64).astype(np.float32)
+    nan = np.isnan(want)
+    assert np.array_equal(np.isnan(out), nan)
+    np.testing.assert_array_equal(out[~nan], want[~nan])
+    assert nan.sum() == 2 * 1023  # every exponent-31 pattern with a non-zero fraction
+
+
+def test_f16_features_are_widened_exactly():
+    wl = da_inputs.small_variant("dcnv4", batch=1).replace(feat_dtype="f16")
+    inp = da_inputs.make_inputs(wl)
+    assert inp.feat.dtype == torch.float16
+    as_f32 = inp.feat.to(torch.float32).numpy()
+    args = (inp.spatial_shape.numpy(), inp.level_start_index.numpy(), inp.loc.numpy(),
+            inp.weights.numpy())
+    np.testing.assert_array_equal(oracle.forward(inp.feat_numpy(), *args), oracle.forward(as_f32, *args))
+    go = inp.grad_out.numpy()
+    for a, b in zip(oracle.backward(inp.feat_numpy(), *args, go), oracle.backward(as_f32, *args, go)):
+        np.testing.assert_array_equal(a, b)
+
+
 def test_anchor_range_matches_full_run():
     inp = da_inputs.make_inputs(da_inputs.small_variant("sp4d_train", batch=2, num_anchors=5))
     full = oracle.run_inputs(inp)

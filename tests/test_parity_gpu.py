@@ -3,7 +3,7 @@
 All five workloads run at full size, and every output element is compared
 with the oracle on the same seeded inputs. The launch configuration is the
 one the bench times. Smaller cases cover:
-  * every supported group width (D*elem = 16/32/64/128 bytes, fp32 and bf16);
+  * every supported group width (D*elem = 16/32/64/128 bytes, fp32, bf16 and fp16);
   * ragged sample counts and anchor counts that are not a multiple of a CTA's
     share;
   * 1x1 maps, wide location ranges, empty inputs and non-finite locations;
@@ -100,6 +100,8 @@ def _custom(seed, shapes_ks, B, C, G, A, P, dtype="f32", lo=-0.3, hi=1.3, wscale
     feat = torch.randn(B, row, C, generator=g)
     if dtype == "bf16":
         feat = feat.to(torch.bfloat16)
+    elif dtype == "f16":
+        feat = feat.to(torch.float16)
     loc = lo + (hi - lo) * torch.rand(B, A, P, K, 2, generator=g)
     w = torch.randn(B, A, P, K, S, G, generator=g) * wscale
     go = torch.randn(B, A, C, generator=g)
@@ -119,6 +121,11 @@ CASES = [
     (8, [[(7, 9)], [(3, 5)]], 1, 32, 2, 9, 5, "bf16"),                     # D=16 bf16
     (9, [[(7, 9)], [(3, 5)]], 1, 32, 4, 10, 6, "bf16"),                    # D=8 bf16
     (10, [[(31, 47), (16, 24), (8, 12)]] * 3, 1, 64, 2, 37, 11, "f32"),    # many chunks per warp
+    (11, [[(7, 9), (3, 5)], [(6, 11), (2, 2)]], 2, 128, 2, 6, 3, "f16"),  # D=64 fp16
+    (12, [[(7, 9), (3, 5)], [(6, 11), (2, 2)]], 2, 64, 2, 6, 3, "f16"),   # D=32 fp16
+    (13, [[(7, 9)], [(3, 5)]], 1, 64, 4, 9, 5, "f16"),                     # D=16 fp16
+    (14, [[(7, 9)], [(3, 5)]], 1, 32, 4, 10, 6, "f16"),                    # D=8 fp16
+    (15, [[(56, 56)]], 2, 64, 4, 40, 9, "f16"),                            # DCNv4-like, fp16
 ]
 
 
