@@ -256,9 +256,160 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
     }
 }
 
+// Few samples per (anchor, group) (the DCNv4 form): one thread per 16-byte
+// chunk of an anchor's C channels, as in the forward's small-task kernel.
+// An anchor's cpa threads (a power of two, at most 32) are adjacent lanes;
+// the CH lanes of a group sum the corner dot products d_i with xor
+// shuffles, and (standard layout) the groups' grad_loc terms are summed over
+// the anchor's lanes the same way. kSmallUnroll samples' loads are in
+// flight together.
+constexpr int kSmallUnroll = 3;
+
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(kThreads) bwd_small_kernel(const BwdArgs args, int cpa_log2, int ch)
+{
+    using Ck = Chunk<T>;
+    constexpr int VEC = Ck::kVec;
+    constexpr int ESZ = 16 / VEC;
+    const Problem &pb = args.pb;
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    stage_maps(pb, maps_s);
+    __syncthreads();
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int cpa = 1 << cpa_log2;
+    const int64_t ba_raw = t >> cpa_log2;
+    // Lanes past the last anchor run along on anchor num_ba - 1 (whole
+    // anchors, so the shuffles stay within live lanes) and store nothing.
+    const bool live = ba_raw < pb.num_ba;
+    const int64_t ba = live ? ba_raw : pb.num_ba - 1;
+    const int chunk = static_cast<int>(t & (cpa - 1));
+    const int c0 = chunk * VEC;
+    const int g = c0 / pb.D;
+    const int gsub = chunk & (ch - 1);
+    const int b = static_cast<int>(pb.div_A.div(static_cast<uint32_t>(ba)));
+    const char *base = static_cast<const char *>(pb.feat) + (static_cast<int64_t>(b) * pb.rows * pb.C + c0) * ESZ;
+    float *gbase = args.grad_feat + static_cast<int64_t>(b) * pb.rows * pb.C + c0;
+    const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
+    float go[VEC];
+    {
+        const float4 *src = reinterpret_cast<const float4 *>(args.grad_out + ba * pb.C + c0);
+#pragma unroll
+        for (int q = 0; q < VEC / 4; ++q) {
+            const float4 v = src[q];
+            go[4 * q] = v.x;
+            go[4 * q + 1] = v.y;
+            go[4 * q + 2] = v.z;
+            go[4 * q + 3] = v.w;
+        }
+    }
+    float gx = 0.f, gy = 0.f;  // the current (p, k): sums over s
+    for (int j0 = 0; j0 < pb.pks; j0 += kSmallUnroll) {
+        uint4 raw[kSmallUnroll][4];
+        Footprint f[kSmallUnroll];
+        float w[kSmallUnroll];
+        int mw[kSmallUnroll], mh[kSmallUnroll];
+#pragma unroll
+        for (int u = 0; u < kSmallUnroll; ++u) {
+            const int j = j0 + u;
+            w[u] = 0.f;
+            mw[u] = mh[u] = 0;
+            if (j < pb.pks) {
+                const int jk = static_cast<int>(pb.div_S.div(j));
+                const int s = j - jk * pb.S;
+                const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
+                float2 xy;
+                sample_xyw<FUSED>(pb, ba, g, jk, s, xy, w[u]);
+                const MapInfo m = maps_s[k * pb.S + s];
+                mw[u] = m.W;
+                mh[u] = m.H;
+                footprint(xy.x, xy.y, m, f[u]);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    f[u].row[c] = -1;
+                    f[u].cw[c] = 0.f;
+                }
+                f[u].lh = f[u].lw = f[u].hh = f[u].hw = 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) raw[u][c] = ldg16_if(f[u].row[c] >= 0, row_addr(base, f[u].row[c], row_bytes));
+        }
+#pragma unroll
+        for (int u = 0; u < kSmallUnroll; ++u) {
+            const int j = j0 + u;
+            if (j >= pb.pks) break;  // uniform: every lane walks the same j
+            float d[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[VEC];
+                Ck::unpack(raw[u][c], v);
+                float acc = 0.f;
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) acc = fmaf(go[q], v[q], acc);
+                d[c] = acc;
+                const float tw = w[u] * f[u].cw[c];
+                float *dst = gbase + static_cast<int64_t>(f[u].row[c]) * pb.C;
+#pragma unroll
+                for (int q = 0; q < VEC / 4; ++q)
+                    red_add_v4_if(live && f[u].row[c] >= 0, dst + 4 * q, tw * go[4 * q], tw * go[4 * q + 1],
+                                  tw * go[4 * q + 2], tw * go[4 * q + 3]);
+            }
+            for (int m = 1; m < ch; m <<= 1)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) d[c] += __shfl_xor_sync(0xffffffffu, d[c], m);
+            const int jk = static_cast<int>(pb.div_S.div(j));
+            const int s = j - jk * pb.S;
+            const float gweight = f[u].cw[0] * d[0] + f[u].cw[1] * d[1] + f[u].cw[2] * d[2] + f[u].cw[3] * d[3];
+            const float wx = static_cast<float>(mw[u]) * w[u];
+            const float wy = static_cast<float>(mh[u]) * w[u];
+            gx += wx * (f[u].lh * (d[3] - d[2]) + f[u].hh * (d[1] - d[0]));
+            gy += wy * (f[u].lw * (d[3] - d[1]) + f[u].hw * (d[2] - d[0]));
+            if constexpr (FUSED) {
+                float *e = args.grad_loc + ((ba * pb.G + g) * pb.pk + jk) * (2 + pb.S);
+                if (live && gsub == 0) e[2 + s] = gweight;
+                if (s == pb.S - 1) {
+                    if (live && gsub == 0) {
+                        e[0] = gx;
+                        e[1] = gy;
+                    }
+                    gx = gy = 0.f;
+                }
+            } else {
+                if (live && gsub == 0) args.grad_weight[((ba * pb.pk + jk) * pb.S + s) * pb.G + g] = gweight;
+                if (s == pb.S - 1) {
+                    // Sum over the groups: one value per group, held by
+                    // all of its lanes.
+                    for (int m = ch; m < cpa; m <<= 1) {
+                        gx += __shfl_xor_sync(0xffffffffu, gx, m);
+                        gy += __shfl_xor_sync(0xffffffffu, gy, m);
+                    }
+                    if (live && chunk == 0) {
+                        args.grad_loc[(ba * pb.pk + jk) * 2] = gx;
+                        args.grad_loc[(ba * pb.pk + jk) * 2 + 1] = gy;
+                    }
+                    gx = gy = 0.f;
+                }
+            }
+        }
+    }
+}
+
 template <typename T, int CH, bool FUSED>
 cudaError_t launch_layout(const BwdArgs &a, cudaStream_t st)
 {
+    constexpr int ESZ = 16 / Chunk<T>::kVec;
+    if (use_small_task_kernels(a.pb, ESZ)) {
+        const int cpa = a.pb.C * ESZ / 16;
+        if ((cpa & (cpa - 1)) == 0) {
+            int cpa_log2 = 0;
+            while ((1 << cpa_log2) < cpa) ++cpa_log2;
+            const int64_t threads = static_cast<int64_t>(a.pb.num_ba) << cpa_log2;
+            const int64_t grid = (threads + kThreads - 1) / kThreads;
+            if (grid == 0) return cudaSuccess;
+            bwd_small_kernel<T, FUSED><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa_log2, CH);
+            return cudaGetLastError();
+        }
+    }
     const int64_t views = static_cast<int64_t>(a.pb.num_ba) * a.pb.K;
     const int64_t grid = (views + a.pb.anchors_per_cta - 1) / a.pb.anchors_per_cta;
     if (grid == 0) return cudaSuccess;

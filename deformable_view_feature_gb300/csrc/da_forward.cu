@@ -143,9 +143,96 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     }
 }
 
+// Few samples per (anchor, group), as in the DCNv4 form (9 points, one map):
+// the warp-per-task mapping above would leave most lanes idle. Here one
+// thread owns one 16-byte chunk of one anchor's C channels (the DCNv4 page's
+// "one thread, several channels of a group", "Solving the problem: 2"), and
+// walks all the samples of its group itself. A anchor's C*elem/16 threads
+// (at most 32, a power of two) sit side by side in a warp, so each corner
+// row is read as one contiguous segment per group. Footprints are computed
+// by every thread of a group (the same arithmetic as above, so the same
+// result); the loads of UNR samples (4 corners each) are in flight together.
+constexpr int kSmallUnroll = 3;
+
+template <typename T, bool FUSED>
+__global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args, int chunks_per_anchor)
+{
+    using Ck = Chunk<T>;
+    constexpr int VEC = Ck::kVec;
+    constexpr int ESZ = 16 / VEC;
+    const Problem &pb = args.pb;
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    stage_maps(pb, maps_s);
+    __syncthreads();
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
+    const int64_t ba = t / chunks_per_anchor;
+    if (ba >= pb.num_ba) return;
+    const int chunk = static_cast<int>(t - ba * chunks_per_anchor);  // 16-byte chunk of the C channels
+    const int c0 = chunk * VEC;                                       // first channel
+    const int g = c0 / pb.D;
+    const int b = static_cast<int>(pb.div_A.div(static_cast<uint32_t>(ba)));
+    const char *base = static_cast<const char *>(pb.feat) + (static_cast<int64_t>(b) * pb.rows * pb.C + c0) * ESZ;
+    const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
+    float acc[VEC];
+#pragma unroll
+    for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+    for (int j0 = 0; j0 < pb.pks; j0 += kSmallUnroll) {
+        uint4 raw[kSmallUnroll][4];
+        float tw[kSmallUnroll][4];
+#pragma unroll
+        for (int u = 0; u < kSmallUnroll; ++u) {
+            const int j = j0 + u;
+            Footprint f;
+            float w = 0.f;
+            if (j < pb.pks) {
+                const int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k
+                const int s = j - jk * pb.S;
+                const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
+                float2 xy;
+                sample_xyw<FUSED>(pb, ba, g, jk, s, xy, w);
+                footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
+            } else {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    f.row[c] = -1;
+                    f.cw[c] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                tw[u][c] = w * f.cw[c];
+                raw[u][c] = ldg16_if(f.row[c] >= 0, row_addr(base, f.row[c], row_bytes));
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kSmallUnroll; ++u)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                float v[VEC];
+                Ck::unpack(raw[u][c], v);
+#pragma unroll
+                for (int q = 0; q < VEC; ++q) acc[q] = fmaf(tw[u][c], v[q], acc[q]);
+            }
+    }
+    float4 *o = reinterpret_cast<float4 *>(args.out + ba * pb.C + c0);
+#pragma unroll
+    for (int q = 0; q < VEC / 4; ++q) o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+}
+
 template <typename T, int CH>
 cudaError_t launch(const FwdArgs &a, cudaStream_t st)
 {
+    if (use_small_task_kernels(a.pb, sizeof(T) == 4 ? 4 : 2)) {
+        const int cpa = a.pb.C * (sizeof(T) == 4 ? 4 : 2) / 16;
+        const int64_t threads = static_cast<int64_t>(a.pb.num_ba) * cpa;
+        const int64_t grid = (threads + kThreads - 1) / kThreads;
+        if (grid == 0) return cudaSuccess;
+        if (a.pb.fused)
+            fwd_small_kernel<T, true><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa);
+        else
+            fwd_small_kernel<T, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa);
+        return cudaGetLastError();
+    }
     const int64_t grid = sampling_grid(a.pb);
     if (grid == 0) return cudaSuccess;
     if (a.pb.fused)

@@ -150,6 +150,15 @@ inline size_t scatter_smem_bytes(const Problem &pb)
     return static_cast<size_t>(pb.anchors_per_cta) * (pb.fused ? pb.G : 1) * pb.P * 2 * sizeof(float);
 }
 
+// Whether the forward and the scatter backward take the thread-per-chunk
+// kernels: few samples per (anchor, group) (the DCNv4 form has 9), and an
+// anchor's C channels in at most 32 chunks of 16 bytes.
+inline bool use_small_task_kernels(const Problem &pb, int elem_bytes)
+{
+    const int cpa = pb.C * elem_bytes / 16;
+    return pb.pks <= 16 && cpa <= 32 && (pb.C * elem_bytes) % 16 == 0;
+}
+
 // Grid size that covers num_ba anchors, anchors_per_cta at a time.
 inline int64_t sampling_grid(const Problem &pb)
 {
