@@ -96,6 +96,11 @@ WORKLOADS: Dict[str, Workload] = {
                            "uniform", 0.0, 1.0, "softmax", 0.0, True, 3),
     "dcnv4": Workload("dcnv4", 8, 1, ((56, 56),), 64, 4, 56 * 56, 9, "f32",
                       "dcnv4_grid", 0.0, 0.0, "normal", 0.5, True, 4, offset_sigma_px=1.5),
+    # The DCNv4 page's kernel benchmark (its Table 10 excerpt, "Solving the
+    # problem: 2"): input 56x56x128, batch 64, 4 groups of 32 channels,
+    # 3x3 points. Measured in the DCNv4 form (per-group points).
+    "dcnv4_table10": Workload("dcnv4_table10", 64, 1, ((56, 56),), 128, 4, 56 * 56, 9, "f32",
+                              "dcnv4_grid", 0.0, 0.0, "normal", 0.5, True, 5, offset_sigma_px=1.5),
 }
 
 # The order in which the workloads are listed by the project's configuration.

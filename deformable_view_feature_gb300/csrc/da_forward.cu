@@ -145,75 +145,108 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 
 // Few samples per (anchor, group), as in the DCNv4 form (9 points, one map):
 // the warp-per-task mapping above would leave most lanes idle. Here one
-// thread owns one 16-byte chunk of one anchor's C channels (the DCNv4 page's
-// "one thread, several channels of a group", "Solving the problem: 2"), and
-// walks all the samples of its group itself. A anchor's C*elem/16 threads
-// (at most 32, a power of two) sit side by side in a warp, so each corner
-// row is read as one contiguous segment per group. Footprints are computed
-// by every thread of a group (the same arithmetic as above, so the same
-// result); the loads of UNR samples (4 corners each) are in flight together.
-constexpr int kSmallUnroll = 3;
+// lane owns one 16-byte chunk of one anchor's C channels (the DCNv4 page's
+// "one thread, several channels of a group", "Solving the problem: 2"). A
+// warp holds APW = 32 / cpa anchors, cpa = C*elem/16 lanes each (a power of
+// two). Per round of J samples, the warp first builds the footprints of its
+// APW*G*J <= 32 (anchor, group, sample) items, one per lane, into a shared
+// table: {row, weight * corner weight} for the four corners. Then every lane
+// walks the J entries of its own (anchor, group), four at a time, with the
+// 16 corner loads of a step in flight together. (A 64-entry table, two
+// items per lane, measured slower: its item decode needs runtime divisions
+// in the loop.)
+constexpr int kSmallItems = 32;  // table entries per warp and round
 
 template <typename T, bool FUSED>
-__global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args, int chunks_per_anchor)
+__global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args, int cpa_log2, int jstep)
 {
     using Ck = Chunk<T>;
     constexpr int VEC = Ck::kVec;
     constexpr int ESZ = 16 / VEC;
     const Problem &pb = args.pb;
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    __shared__ __align__(16) int4 tab[kWarps][kSmallItems][2];
     stage_maps(pb, maps_s);
     __syncthreads();
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x;
-    const int64_t ba = t / chunks_per_anchor;
-    if (ba >= pb.num_ba) return;
-    const int chunk = static_cast<int>(t - ba * chunks_per_anchor);  // 16-byte chunk of the C channels
-    const int c0 = chunk * VEC;                                       // first channel
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int apw = 32 >> cpa_log2;
+    const int aw = lane >> cpa_log2;                 // anchor slot in the warp
+    const int chunk = lane & ((1 << cpa_log2) - 1);  // 16-byte chunk of the C channels
+    const int c0 = chunk * VEC;
     const int g = c0 / pb.D;
-    const int b = static_cast<int>(pb.div_A.div(static_cast<uint32_t>(ba)));
+    const int64_t ba0 = (static_cast<int64_t>(blockIdx.x) * kWarps + warp) * apw;
+    const int64_t ba = ba0 + aw;
+    const bool live = ba < pb.num_ba;
+    const int b = live ? static_cast<int>(pb.div_A.div(static_cast<uint32_t>(ba))) : 0;
     const char *base = static_cast<const char *>(pb.feat) + (static_cast<int64_t>(b) * pb.rows * pb.C + c0) * ESZ;
     const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
+    // This lane's table item in a round: (anchor slot, group, sample).
+    const int it_aw = lane / (pb.G * jstep);
+    const int it_g = (lane / jstep) % pb.G;
+    const int it_j = lane % jstep;
+    const int64_t it_ba = ba0 + it_aw;
+    const bool it_live = lane < apw * pb.G * jstep && it_ba < pb.num_ba;
+    const int my_item0 = (aw * pb.G + g) * jstep;
+
     float acc[VEC];
 #pragma unroll
     for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
-    for (int j0 = 0; j0 < pb.pks; j0 += kSmallUnroll) {
-        uint4 raw[kSmallUnroll][4];
-        float tw[kSmallUnroll][4];
-#pragma unroll
-        for (int u = 0; u < kSmallUnroll; ++u) {
-            const int j = j0 + u;
-            Footprint f;
-            float w = 0.f;
-            if (j < pb.pks) {
+    for (int j0 = 0; j0 < pb.pks; j0 += jstep) {
+        {
+            int row[4] = {-1, -1, -1, -1};
+            float tw[4] = {0.f, 0.f, 0.f, 0.f};
+            const int j = j0 + it_j;
+            if (it_live && j < pb.pks) {
                 const int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k
                 const int s = j - jk * pb.S;
                 const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
                 float2 xy;
-                sample_xyw<FUSED>(pb, ba, g, jk, s, xy, w);
+                float w;
+                sample_xyw<FUSED>(pb, it_ba, it_g, jk, s, xy, w);
+                Footprint f;
                 footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
-            } else {
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    f.row[c] = -1;
-                    f.cw[c] = 0.f;
+                    row[c] = f.row[c];
+                    tw[c] = w * f.cw[c];
                 }
             }
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                tw[u][c] = w * f.cw[c];
-                raw[u][c] = ldg16_if(f.row[c] >= 0, row_addr(base, f.row[c], row_bytes));
-            }
+            tab[warp][lane][0] = make_int4(row[0], __float_as_int(tw[0]), row[1], __float_as_int(tw[1]));
+            tab[warp][lane][1] = make_int4(row[2], __float_as_int(tw[2]), row[3], __float_as_int(tw[3]));
         }
+        __syncwarp();
+        const int n = min(jstep, pb.pks - j0);
+        for (int jj = 0; jj < n; jj += 4) {
+            uint4 raw[4][4];
+            float tw[4][4];
 #pragma unroll
-        for (int u = 0; u < kSmallUnroll; ++u)
+            for (int u = 0; u < 4; ++u) {
+                int4 e0 = make_int4(-1, 0, -1, 0), e1 = e0;
+                if (jj + u < n) {
+                    e0 = tab[warp][my_item0 + jj + u][0];
+                    e1 = tab[warp][my_item0 + jj + u][1];
+                }
+                const int r[4] = {e0.x, e0.z, e1.x, e1.z};
+                tw[u][0] = __int_as_float(e0.y);
+                tw[u][1] = __int_as_float(e0.w);
+                tw[u][2] = __int_as_float(e1.y);
+                tw[u][3] = __int_as_float(e1.w);
 #pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float v[VEC];
-                Ck::unpack(raw[u][c], v);
-#pragma unroll
-                for (int q = 0; q < VEC; ++q) acc[q] = fmaf(tw[u][c], v[q], acc[q]);
+                for (int c = 0; c < 4; ++c) raw[u][c] = ldg16_if(live && r[c] >= 0, row_addr(base, r[c], row_bytes));
             }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    float v[VEC];
+                    Ck::unpack(raw[u][c], v);
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) acc[q] = fmaf(tw[u][c], v[q], acc[q]);
+                }
+        }
+        __syncwarp();
     }
+    if (!live) return;
     float4 *o = reinterpret_cast<float4 *>(args.out + ba * pb.C + c0);
 #pragma unroll
     for (int q = 0; q < VEC / 4; ++q) o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
@@ -222,16 +255,25 @@ __global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args,
 template <typename T, int CH>
 cudaError_t launch(const FwdArgs &a, cudaStream_t st)
 {
-    if (use_small_task_kernels(a.pb, sizeof(T) == 4 ? 4 : 2)) {
-        const int cpa = a.pb.C * (sizeof(T) == 4 ? 4 : 2) / 16;
-        const int64_t threads = static_cast<int64_t>(a.pb.num_ba) * cpa;
-        const int64_t grid = (threads + kThreads - 1) / kThreads;
-        if (grid == 0) return cudaSuccess;
-        if (a.pb.fused)
-            fwd_small_kernel<T, true><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa);
-        else
-            fwd_small_kernel<T, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa);
-        return cudaGetLastError();
+    constexpr int ESZ = 16 / Chunk<T>::kVec;
+    const int cpa = a.pb.C * ESZ / 16;
+    if (use_small_task_kernels(a.pb, ESZ) && (cpa & (cpa - 1)) == 0) {
+        int cpa_log2 = 0;
+        while ((1 << cpa_log2) < cpa) ++cpa_log2;
+        const int apw = 32 >> cpa_log2;
+        // Samples per round: the warp's apw*G*jstep items fit one per lane.
+        const int per_j = apw * a.pb.G;
+        if (per_j <= kSmallItems) {
+            const int jstep = kSmallItems / per_j;
+            const int64_t warps = (static_cast<int64_t>(a.pb.num_ba) + apw - 1) / apw;
+            const int64_t grid = (warps + kWarps - 1) / kWarps;
+            if (grid == 0) return cudaSuccess;
+            if (a.pb.fused)
+                fwd_small_kernel<T, true><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa_log2, jstep);
+            else
+                fwd_small_kernel<T, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa_log2, jstep);
+            return cudaGetLastError();
+        }
     }
     const int64_t grid = sampling_grid(a.pb);
     if (grid == 0) return cudaSuccess;
