@@ -422,6 +422,84 @@ def run_ours(a, wl):
     print(json.dumps(line), flush=True)
 
 
+def run_fused(a, wl):
+    """The DCNv4 form (da_forward_fused + da_backward_fused, per-group points
+    fused with their weights) on one GPU. Default workload: the DCNv4 page's
+    kernel benchmark (its Table 10 excerpt: 56x56x128, batch 64, 4 groups,
+    3x3 points), whose A100 kernel times the line quotes as context."""
+    import deformable_view_feature_gb300 as da
+    da.load_library()
+    dev = torch.device("cuda", 0)
+    inp = da_inputs.make_fused_inputs(wl)
+    feat, lw, go = inp.feat.to(dev), inp.loc_weight.to(dev), inp.grad_out.to(dev)
+    ss, ls = inp.spatial_shape, inp.level_start_index
+    out = torch.empty(go.shape, device=dev)
+    gf = torch.empty(feat.shape, device=dev)
+    glw = torch.empty_like(lw)
+    stream = torch.cuda.Stream(device=dev)
+    fwd_bytes = tensor_bytes(feat, lw) + out.numel() * 4
+    bwd_bytes = tensor_bytes(feat, lw, go) + 2 * gf.numel() * 4 + glw.numel() * 4
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        da.da_forward_fused(feat, ss, ls, lw, out=out, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        if wl.backward:
+            da.da_backward_fused(feat, ss, ls, lw, go, grad_feat=gf, grad_loc_weight=glw, stream=stream)
+            if ev is not None:
+                ev[2].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            step()
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(0)
+    clocks.start()
+    time.sleep(0.3)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(a.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record(stream)
+    for i in range(a.steps):
+        step(evs[i])
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.time()
+    time.sleep(0.1)
+    clocks.stop()
+    ms = start.elapsed_time(end) / a.steps
+    fwd_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(a.steps))
+    bwd_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(a.steps)) if wl.backward else None
+    peak, peak_kind = peaks()
+    dom_ms, dom_bytes, dom = (bwd_ms, bwd_bytes, "da_backward_fused") if wl.backward else \
+        (fwd_ms, fwd_bytes, "da_forward_fused")
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    line = {
+        "metric": "fwd+bwd bilinear samples/sec, DCNv4 form (per-group points fused with weights)",
+        "value": wl.num_samples / (ms / 1e3), "unit": "samples/s", "n_gpus": 1, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32" if wl.feat_dtype == "f32" else f"{wl.feat_dtype}-features/f32",
+        "data": "synthetic (seeded da_inputs draw, per-group 3x3 grid points plus N(0, 1.5 px) offsets)",
+        "config": {"workload": f"{wl.name}: B{wl.batch} {wl.shapes[0][0]}x{wl.shapes[0][1]} C{wl.num_embeds} "
+                               f"G{wl.num_groups} P{wl.num_pts}, {wl.feat_dtype} features",
+                   "samples_per_step": wl.num_samples,
+                   "l2": "inputs and outputs larger than L2" if fwd_bytes > 129e6 else "fits in L2, no flush"},
+        "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+                     "algorithmic_bytes": dom_bytes, "traffic": None},
+        "page_context": {"what": "DCNv4 page, Table 10 excerpt: DCNv4 CUDA kernel on A100 for this workload "
+                                 "(another machine; context, not a target)",
+                         "a100_kernel_ms": {"f32": 0.606, "f16": 0.404}.get(wl.feat_dtype),
+                         "ours_fwd_ms": fwd_ms} if wl.name.startswith("dcnv4_table10") else None,
+        "gpu_launches": a.steps * (1 + (2 if wl.backward else 0)),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -435,12 +513,25 @@ def main():
     ap.add_argument("--ref-anchors", type=int, default=300,
                     help="anchors per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["da", "fused"], default="da",
+                    help="da: the Sparse4D operator (the headline); fused: the DCNv4 form "
+                         "(default workload dcnv4_table10)")
+    ap.add_argument("--feat-dtype", choices=["f32", "bf16", "f16"], default=None,
+                    help="override the workload's feature type (--op fused)")
     ap.add_argument("--bwd-path", choices=["binned", "binned-det", "scatter"], default="binned",
                     help="backward algorithm (binned needs a device workspace; binned-det is its "
                          "deterministic mode)")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if a.op == "fused":
+        wl = da_inputs.WORKLOADS["dcnv4_table10" if a.workload == "sp4d_train" else a.workload]
+        if a.feat_dtype:
+            wl = wl.replace(feat_dtype=a.feat_dtype)
+        if a.impl == "reference" or a.gpus != 1:
+            ap.error("--op fused runs our implementation on one GPU")
+        run_fused(a, wl)
+        return
     wl = da_inputs.WORKLOADS[a.workload]
     if a.impl == "reference":
         run_reference(a, wl)
