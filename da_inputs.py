@@ -47,10 +47,10 @@ class Workload:
     num_anchors: int
     num_pts: int
     feat_dtype: str  # "f32", "bf16" or "f16"
-    loc_kind: str  # "uniform" or "dcnv4_grid"
+    loc_kind: str  # "uniform", "dcnv4_grid" or "projected" (make_projected_inputs only)
     loc_lo: float
     loc_hi: float
-    weight_kind: str  # "uniform01", "softmax" or "normal"
+    weight_kind: str  # "uniform01", "softmax", "normal" or "logits" (make_projected_inputs only)
     weight_sigma: float
     backward: bool
     seed: int
@@ -96,6 +96,10 @@ WORKLOADS: Dict[str, Workload] = {
                            "uniform", 0.0, 1.0, "softmax", 0.0, True, 3),
     "dcnv4": Workload("dcnv4", 8, 1, ((56, 56),), 64, 4, 56 * 56, 9, "f32",
                       "dcnv4_grid", 0.0, 0.0, "normal", 0.5, True, 4, offset_sigma_px=1.5),
+    # The training shape fed from one step upstream: key points, a camera
+    # ring and weight logits (make_projected_inputs).
+    "sp4d_proj": Workload("sp4d_proj", 6, 6, SP4D_SHAPES, 256, 8, 900, 13, "f32",
+                          "projected", 0.0, 0.0, "logits", 0.0, True, 6),
     # The DCNv4 page's kernel benchmark (its Table 10 excerpt, "Solving the
     # problem: 2"): input 56x56x128, batch 64, 4 groups of 32 channels,
     # 3x3 points. Measured in the DCNv4 form (per-group points).
@@ -245,6 +249,78 @@ def make_fused_inputs(wl: Workload | str, seed: Optional[int] = None) -> FusedIn
         lw[:, :, gi, :, :, 2:] = w[..., gi]
     grad_out = torch.randn(B, wl.num_anchors, C, generator=g, dtype=torch.float32)
     return FusedInputs(wl, feat, ss, ls, lw.contiguous(), grad_out)
+
+
+@dataclasses.dataclass
+class ProjectedInputs:
+    """Inputs one step upstream of the operator, as the Sparse4D head holds
+    them (the Sparse4D page, §1 and §6: 3D anchors' key points are projected
+    into the camera views): key points in the ego frame, one 4x4 projection
+    matrix per camera, and weight logits that a softmax turns into weights."""
+    wl: Workload
+    feat: torch.Tensor  # [B, rows, C]
+    spatial_shape: torch.Tensor  # [K, S, 2] int32
+    level_start_index: torch.Tensor  # [K, S] int32
+    keypoints: torch.Tensor  # [B, A, P, 3] float32, metres, ego frame (x forward, y left, z up)
+    projection: torch.Tensor  # [B, K, 4, 4] float32, ego point -> (u*d, v*d, d, 1) in pixels
+    image_w: float
+    image_h: float
+    logits: torch.Tensor  # [B, A, P, K, S, G] float32
+    grad_out: torch.Tensor  # [B, A, C] float32
+
+    def feat_numpy(self) -> np.ndarray:
+        return Inputs.feat_numpy(self)
+
+
+def camera_rig(num_cams: int, image_w: float, image_h: float, focal_px: float = 300.0,
+               height_m: float = 1.6) -> np.ndarray:
+    """A ring of num_cams pinhole cameras at the ego origin, height_m above the
+    ground, looking out at evenly spaced yaws (the first one straight ahead).
+    Returns [K, 4, 4] float64 matrices: ego (X, Y, Z, 1) -> (u*d, v*d, d, 1),
+    with the principal point at the image centre. Input construction only."""
+    cx, cy = image_w / 2.0, image_h / 2.0
+    mats = np.zeros((num_cams, 4, 4))
+    t = np.array([0.0, 0.0, height_m])
+    for k in range(num_cams):
+        yaw = 2.0 * np.pi * k / num_cams
+        fwd = np.array([np.cos(yaw), np.sin(yaw), 0.0])
+        right = np.array([np.sin(yaw), -np.cos(yaw), 0.0])
+        down = np.array([0.0, 0.0, -1.0])
+        rows = [focal_px * right + cx * fwd, focal_px * down + cy * fwd, fwd]
+        for r, vec in enumerate(rows):
+            mats[k, r, :3] = vec
+            mats[k, r, 3] = -vec @ t
+        mats[k, 3, 3] = 1.0
+    return mats
+
+
+def make_projected_inputs(wl: Workload | str, seed: Optional[int] = None) -> ProjectedInputs:
+    """Anchors uniform in a 100 m x 100 m square around the ego car (centres
+    0.5 m below to 2 m above the ground); each anchor's P key points spread
+    up to +-2 m (x, y) and +-1 m (z) around its centre; a six-camera ring;
+    logits N(0, 1). The image is four times the finest map (stride 4)."""
+    if isinstance(wl, str):
+        wl = WORKLOADS[wl]
+    g = torch.Generator().manual_seed((wl.seed if seed is None else seed) + 2000)
+    B, C, A, P, K = wl.batch, wl.num_embeds, wl.num_anchors, wl.num_pts, wl.num_cams
+    feat = torch.randn(B, wl.num_feat_rows, C, generator=g, dtype=torch.float32)
+    if wl.feat_dtype == "bf16":
+        feat = feat.to(torch.bfloat16)
+    elif wl.feat_dtype == "f16":
+        feat = feat.to(torch.float16)
+    ss, ls = map_tables(K, wl.shapes)
+    image_h, image_w = 4.0 * wl.shapes[0][0], 4.0 * wl.shapes[0][1]
+    lo = torch.tensor([-50.0, -50.0, -0.5], dtype=torch.float64)
+    hi = torch.tensor([50.0, 50.0, 2.0], dtype=torch.float64)
+    centre = lo + (hi - lo) * torch.rand(B, A, 1, 3, generator=g, dtype=torch.float64)
+    spread = torch.tensor([2.0, 2.0, 1.0], dtype=torch.float64)
+    kp = centre + spread * (2.0 * torch.rand(B, A, P, 3, generator=g, dtype=torch.float64) - 1.0)
+    rig = torch.from_numpy(camera_rig(K, image_w, image_h)).to(torch.float32)
+    projection = rig.unsqueeze(0).expand(B, K, 4, 4).contiguous()
+    logits = torch.randn(B, A, P, K, wl.num_scales, wl.num_groups, generator=g, dtype=torch.float32)
+    grad_out = torch.randn(B, A, C, generator=g, dtype=torch.float32)
+    return ProjectedInputs(wl, feat, ss, ls, kp.to(torch.float32).contiguous(), projection, image_w, image_h,
+                           logits, grad_out)
 
 
 def small_variant(name: str, batch: int = 1, num_anchors: int = 24) -> Workload:

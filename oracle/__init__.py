@@ -59,6 +59,13 @@ def _load():
         lib.dao_forward_fused.restype = i32
         lib.dao_backward_fused.argtypes = [i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp, vp]
         lib.dao_backward_fused.restype = i32
+        f32 = ctypes.c_float
+        lib.dao_project.argtypes = [i32, i32, i32, i32, vp, vp, f32, f32, vp]
+        lib.dao_project.restype = i32
+        lib.dao_softmax_weights.argtypes = [i32] * 6 + [vp, vp]
+        lib.dao_softmax_weights.restype = i32
+        lib.dao_projected_chain.argtypes = [i32] * 6 + [vp, vp, f32, f32, vp, vp, vp, vp, vp]
+        lib.dao_projected_chain.restype = i32
         lib.dao_bilinear.argtypes = [vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float]
         lib.dao_bilinear.restype = ctypes.c_double
         _lib = lib
@@ -189,6 +196,66 @@ def backward_fused(feat, spatial_shape, level_start_index, loc_weight, grad_out)
     if rc != 0:
         raise ValueError(f"oracle fused backward rejected its arguments (code {rc})")
     return gf, glw
+
+
+def project(keypoints, projection, image_w: float, image_h: float) -> np.ndarray:
+    """Key points [B, A, P, 3] seen through the cameras [B, K, 4, 4]: the
+    normalised locations [B, A, P, K, 2] (NaN behind a camera); see
+    dao_project in da_oracle.c for the exact fp32 steps."""
+    kp = np.ascontiguousarray(keypoints, dtype=np.float32)
+    pr = np.ascontiguousarray(projection, dtype=np.float32)
+    B, A, P, _ = kp.shape
+    K = pr.shape[1]
+    assert pr.shape == (B, K, 4, 4), pr.shape
+    loc = np.empty((B, A, P, K, 2), dtype=np.float32)
+    if _load().dao_project(B, K, A, P, _ptr(kp), _ptr(pr), float(image_w), float(image_h), _ptr(loc)) != 0:
+        raise ValueError("oracle projection rejected its arguments")
+    return loc
+
+
+def softmax_weights(logits) -> np.ndarray:
+    """Softmax of logits [B, A, P, K, S, G] over (P, K, S) for every (b, a, g)."""
+    z = np.ascontiguousarray(logits, dtype=np.float32)
+    B, A, P, K, S, G = z.shape
+    w = np.empty_like(z)
+    if _load().dao_softmax_weights(B, A, P, K, S, G, _ptr(z), _ptr(w)) != 0:
+        raise ValueError("oracle softmax rejected its arguments")
+    return w
+
+
+def projected_chain(keypoints, projection, image_w, image_h, weights, grad_loc, grad_weight):
+    """(grad_keypoints [B, A, P, 3], grad_logits [B, A, P, K, S, G]) from the
+    operator's grad_loc and grad_weight."""
+    kp = np.ascontiguousarray(keypoints, dtype=np.float32)
+    pr = np.ascontiguousarray(projection, dtype=np.float32)
+    w = np.ascontiguousarray(weights, dtype=np.float32)
+    gl = np.ascontiguousarray(grad_loc, dtype=np.float32)
+    gw = np.ascontiguousarray(grad_weight, dtype=np.float32)
+    B, A, P, K, S, G = w.shape
+    gkp = np.empty(kp.shape, dtype=np.float32)
+    glg = np.empty(w.shape, dtype=np.float32)
+    rc = _load().dao_projected_chain(B, K, S, G, A, P, _ptr(kp), _ptr(pr), float(image_w), float(image_h), _ptr(w),
+                                     _ptr(gl), _ptr(gw), _ptr(gkp), _ptr(glg))
+    if rc != 0:
+        raise ValueError("oracle chain rule rejected its arguments")
+    return gkp, glg
+
+
+def forward_projected(feat, spatial_shape, level_start_index, keypoints, projection, image_w, image_h, logits):
+    """The operator fed by the projection and the softmax: (out, loc, weights)."""
+    loc = project(keypoints, projection, image_w, image_h)
+    w = softmax_weights(logits)
+    return forward(feat, spatial_shape, level_start_index, loc, w), loc, w
+
+
+def backward_projected(feat, spatial_shape, level_start_index, keypoints, projection, image_w, image_h, logits,
+                       grad_out):
+    """(grad_feat, grad_loc, grad_weight, grad_keypoints, grad_logits)."""
+    loc = project(keypoints, projection, image_w, image_h)
+    w = softmax_weights(logits)
+    gf, gl, gw = backward(feat, spatial_shape, level_start_index, loc, w, grad_out)
+    gkp, glg = projected_chain(keypoints, projection, image_w, image_h, w, gl, gw)
+    return gf, gl, gw, gkp, glg
 
 
 def bilinear(fmap: np.ndarray, c: int, x: float, y: float) -> float:

@@ -387,6 +387,128 @@ int dao_backward_fused(int B, int K, int S, int C, int G, int A, int P, int64_t 
     return DAO_OK;
 }
 
+/*
+ * The step before the operator in Sparse4D (the Sparse4D page, §1 and §6:
+ * each 3D anchor's key points are projected into every camera view). The
+ * page prints no formula; the reading here is the pinhole projection by a
+ * 4x4 matrix whose first three rows map a homogeneous point (X, Y, Z, 1) to
+ * (u*d, v*d, d) in pixels, then a division by the image size:
+ *   ud = ((m00*X + m01*Y) + m02*Z) + m03   (fp32: every product and sum
+ *   vd, d likewise with rows 1 and 2        rounded, in this order)
+ *   x = (ud / d) / image_w,  y = (vd / d) / image_h   (fp32 divisions)
+ * A point with d <= 1e-5 (behind or on the camera plane) gets the location
+ * (NaN, NaN), which reads nothing. The location decides which pixels are
+ * read, so the kernel computes it with the same fp32 operations.
+ * kp [B, A, P, 3], proj [B, K, 4, 4] row-major, loc [B, A, P, K, 2].
+ */
+static void project_point(const float *kp, const float *m, float image_w, float image_h, float *xy)
+{
+    float ud = ((m[0] * kp[0] + m[1] * kp[1]) + m[2] * kp[2]) + m[3];
+    float vd = ((m[4] * kp[0] + m[5] * kp[1]) + m[6] * kp[2]) + m[7];
+    float d = ((m[8] * kp[0] + m[9] * kp[1]) + m[10] * kp[2]) + m[11];
+    if (!(d > 1e-5f)) {
+        xy[0] = NAN;
+        xy[1] = NAN;
+        return;
+    }
+    float u = ud / d, v = vd / d;
+    xy[0] = u / image_w;
+    xy[1] = v / image_h;
+}
+
+int dao_project(int B, int K, int A, int P, const float *kp, const float *proj, float image_w, float image_h,
+                float *loc)
+{
+    if (B < 0 || K < 0 || A < 0 || P < 0) return DAO_ERR_ARGS;
+    int64_t b, a, p, k;
+    for (b = 0; b < B; ++b)
+        for (a = 0; a < A; ++a)
+            for (p = 0; p < P; ++p)
+                for (k = 0; k < K; ++k)
+                    project_point(kp + ((b * A + a) * P + p) * 3, proj + (b * K + k) * 16, image_w, image_h,
+                                  loc + (((b * A + a) * P + p) * K + k) * 2);
+    return DAO_OK;
+}
+
+/*
+ * Weights from logits: a softmax over the P*K*S samples of every (b, a, g),
+ * the normalisation the Sparse4D head applies before the operator. In double,
+ * rounded to fp32 at the end. logits and w are [B, A, P, K, S, G].
+ */
+int dao_softmax_weights(int B, int A, int P, int K, int S, int G, const float *logits, float *w)
+{
+    if (B < 0 || A < 0 || P < 0 || K < 0 || S < 0 || G <= 0) return DAO_ERR_ARGS;
+    const int64_t n = (int64_t)P * K * S;
+    int64_t ba, j;
+    int g;
+    for (ba = 0; ba < (int64_t)B * A; ++ba)
+        for (g = 0; g < G; ++g) {
+            double mx = -INFINITY, sum = 0.0;
+            for (j = 0; j < n; ++j) {
+                const double z = logits[(ba * n + j) * G + g];
+                if (z > mx) mx = z;
+            }
+            for (j = 0; j < n; ++j) sum += exp((double)logits[(ba * n + j) * G + g] - mx);
+            for (j = 0; j < n; ++j)
+                w[(ba * n + j) * G + g] = (float)(exp((double)logits[(ba * n + j) * G + g] - mx) / sum);
+        }
+    return DAO_OK;
+}
+
+/*
+ * Chain rule from the operator's gradients back to the key points and the
+ * logits (double):
+ *   grad_logits[b,a,p,k,s,g] = w * (grad_weight - sum over (p,k,s) of w * grad_weight),
+ *     per (b, a, g), the derivative of the softmax;
+ *   grad_kp[b,a,p,:] = sum over k of J_k^T grad_loc[b,a,p,k,:], with J_k the
+ *     derivative of (x, y) above with respect to (X, Y, Z):
+ *     dx/dX_i = (m0i * d - ud * m2i) / (d^2 * image_w),
+ *     dy/dX_i = (m1i * d - vd * m2i) / (d^2 * image_h),
+ *     and 0 for a point with d <= 1e-5.
+ */
+int dao_projected_chain(int B, int K, int S, int G, int A, int P, const float *kp, const float *proj,
+                        float image_w, float image_h, const float *w, const float *grad_loc,
+                        const float *grad_weight, float *grad_kp, float *grad_logits)
+{
+    if (B < 0 || K < 0 || S < 0 || G <= 0 || A < 0 || P < 0) return DAO_ERR_ARGS;
+    const int64_t n = (int64_t)P * K * S;
+    int64_t ba, j;
+    int g, p, k, i;
+    for (ba = 0; ba < (int64_t)B * A; ++ba) {
+        for (g = 0; g < G; ++g) {
+            double dot = 0.0;
+            for (j = 0; j < n; ++j) dot += (double)w[(ba * n + j) * G + g] * grad_weight[(ba * n + j) * G + g];
+            for (j = 0; j < n; ++j) {
+                const int64_t e = (ba * n + j) * G + g;
+                grad_logits[e] = (float)((double)w[e] * ((double)grad_weight[e] - dot));
+            }
+        }
+        const int64_t b = ba / A;
+        for (p = 0; p < P; ++p) {
+            const float *x = kp + (ba * P + p) * 3;
+            double acc[3] = {0.0, 0.0, 0.0};
+            for (k = 0; k < K; ++k) {
+                const float *m = proj + (b * K + k) * 16;
+                const double ud = (double)m[0] * x[0] + (double)m[1] * x[1] + (double)m[2] * x[2] + m[3];
+                const double vd = (double)m[4] * x[0] + (double)m[5] * x[1] + (double)m[6] * x[2] + m[7];
+                const double d = (double)m[8] * x[0] + (double)m[9] * x[1] + (double)m[10] * x[2] + m[11];
+                /* the validity test is the forward's fp32 one */
+                const float d32 = (((m[8] * x[0] + m[9] * x[1]) + m[10] * x[2]) + m[11]);
+                if (!(d32 > 1e-5f)) continue;
+                const double gx = grad_loc[((ba * P + p) * K + k) * 2];
+                const double gy = grad_loc[((ba * P + p) * K + k) * 2 + 1];
+                for (i = 0; i < 3; ++i) {
+                    const double dxd = (m[i] * d - ud * m[8 + i]) / (d * d * image_w);
+                    const double dyd = (m[4 + i] * d - vd * m[8 + i]) / (d * d * image_h);
+                    acc[i] += gx * dxd + gy * dyd;
+                }
+            }
+            for (i = 0; i < 3; ++i) grad_kp[(ba * P + p) * 3 + i] = (float)acc[i];
+        }
+    }
+    return DAO_OK;
+}
+
 /* Bilinear value of one channel at one location, for pin tests. */
 double dao_bilinear(const float *map, int32_t H, int32_t W, int32_t C, int32_t c,
                     float x, float y)
