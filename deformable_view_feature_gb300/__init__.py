@@ -26,7 +26,8 @@ import torch
 
 from . import build as _build
 
-__all__ = ["da_forward", "da_backward", "da_forward_fused", "da_backward_fused", "backward_workspace_size",
+__all__ = ["da_forward", "da_backward", "da_forward_fused", "da_backward_fused", "da_forward_projected",
+           "da_backward_projected", "backward_workspace_size",
            "DeformableAggregationFunction", "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
 
 DA_F32, DA_BF16, DA_F16 = 0, 1, 2
@@ -80,6 +81,12 @@ def load_library():
     lib.da_forward_fused.restype = ctypes.c_int
     lib.da_backward_fused.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
     lib.da_backward_fused.restype = ctypes.c_int
+    f32 = ctypes.c_float
+    lib.da_forward_projected.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, f32, f32, vp, vp, vp, vp, vp]
+    lib.da_forward_projected.restype = ctypes.c_int
+    lib.da_backward_projected.argtypes = ([ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, f32, f32]
+                                          + [vp] * 9 + [ctypes.c_size_t, ctypes.c_uint32, vp])
+    lib.da_backward_projected.restype = ctypes.c_int
     lib.da_backward_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
     lib.da_backward_workspace_size.restype = ctypes.c_int
     lib.da_status_string.argtypes = [ctypes.c_int]
@@ -402,6 +409,77 @@ def da_backward_fused(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index
                                  ls.data_ptr() if ls.numel() else None, _dptr(loc_weight), _dptr(grad_out),
                                  _dptr(grad_feat), _dptr(grad_loc_weight), None, 0, _stream_handle(stream)))
     return grad_feat, grad_loc_weight
+
+
+def _dims_projected(feat, ss, keypoints, logits) -> DaDims:
+    if keypoints.dim() != 4 or keypoints.shape[-1] != 3:
+        raise ValueError("keypoints must be [B, A, P, 3]")
+    if logits.dim() != 6:
+        raise ValueError("weight_logits must be [B, A, P, K, S, G]")
+    B, A, P, K, S, G = logits.shape
+    if tuple(keypoints.shape[:3]) != (B, A, P):
+        raise ValueError("keypoints and weight_logits disagree on B, A, P")
+    if keypoints.dtype != torch.float32 or logits.dtype != torch.float32:
+        raise TypeError("keypoints and weight_logits must be float32")
+    return _dims(feat, ss, torch.empty(B, A, P, K, 2, device="meta"), torch.empty(B, A, P, K, S, G, device="meta"))
+
+
+def da_forward_projected(mc_ms_feat, spatial_shape, level_start_index, keypoints, projection, image_w: float,
+                         image_h: float, weight_logits, keep_samples: bool = True, stream=None):
+    """Key points projected into the cameras and softmax weights, fused into
+    the forward (da_forward_projected). Returns (out, sampling_location,
+    weights); the last two are None unless keep_samples (the backward needs
+    them)."""
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims_projected(mc_ms_feat, ss, keypoints, weight_logits)
+    dev = mc_ms_feat.device
+    if tuple(projection.shape) != (d.batch, d.num_cams, 4, 4) or projection.dtype != torch.float32:
+        raise ValueError("projection must be float32 [B, K, 4, 4]")
+    out = torch.empty(d.batch, d.num_anchors, d.num_embeds, device=dev, dtype=torch.float32)
+    loc = w = None
+    if keep_samples:
+        loc = torch.empty(d.batch, d.num_anchors, d.num_pts, d.num_cams, 2, device=dev, dtype=torch.float32)
+        w = torch.empty(weight_logits.shape, device=dev, dtype=torch.float32)
+    _check(lib.da_forward_projected(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
+                                    ls.data_ptr() if ls.numel() else None, _dptr(keypoints), _dptr(projection),
+                                    float(image_w), float(image_h), _dptr(weight_logits), _dptr(out),
+                                    _dptr(loc), _dptr(w), _stream_handle(stream)))
+    return out, loc, w
+
+
+def da_backward_projected(mc_ms_feat, spatial_shape, level_start_index, keypoints, projection, image_w: float,
+                          image_h: float, sampling_location, weights, grad_out, path: str = "binned",
+                          deterministic: bool = False, stream=None):
+    """Backward of da_forward_projected: returns (grad_feat, grad_loc,
+    grad_weight, grad_keypoints, grad_logits)."""
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims(mc_ms_feat, ss, sampling_location, weights)
+    dev = mc_ms_feat.device
+    if tuple(keypoints.shape) != (d.batch, d.num_anchors, d.num_pts, 3) or keypoints.dtype != torch.float32:
+        raise ValueError("keypoints must be float32 [B, A, P, 3]")
+    if tuple(projection.shape) != (d.batch, d.num_cams, 4, 4) or projection.dtype != torch.float32:
+        raise ValueError("projection must be float32 [B, K, 4, 4]")
+    gf = torch.empty(mc_ms_feat.shape, device=dev, dtype=torch.float32)
+    gl = torch.empty(sampling_location.shape, device=dev, dtype=torch.float32)
+    gw = torch.empty(weights.shape, device=dev, dtype=torch.float32)
+    gkp = torch.empty(keypoints.shape, device=dev, dtype=torch.float32)
+    glg = torch.empty(weights.shape, device=dev, dtype=torch.float32)
+    sh = _stream_handle(stream)
+    ws_ptr, ws_bytes = None, 0
+    if path == "binned":
+        need = backward_workspace_size(d)
+        ws = _workspace(dev, sh, need)
+        ws_ptr, ws_bytes = _dptr(ws), ws.numel()
+    elif path != "scatter" or deterministic:
+        raise ValueError("path must be 'binned' or 'scatter' (deterministic needs 'binned')")
+    _check(lib.da_backward_projected(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
+                                     ls.data_ptr() if ls.numel() else None, _dptr(keypoints), _dptr(projection),
+                                     float(image_w), float(image_h), _dptr(sampling_location), _dptr(weights),
+                                     _dptr(grad_out), _dptr(gf), _dptr(gl), _dptr(gw), _dptr(gkp), _dptr(glg),
+                                     ws_ptr, ws_bytes, 1 if deterministic else 0, sh))
+    return gf, gl, gw, gkp, glg
 
 
 class DeformableAggregationFunction(torch.autograd.Function):

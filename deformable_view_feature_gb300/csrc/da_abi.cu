@@ -7,6 +7,7 @@
 // Here the start index is called level_start_index, the two small map tables
 // are host arrays (so the host can check every map against the feature rows
 // without a device round trip), and the sizes travel in da_dims.
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -254,7 +255,34 @@ da_status prepare_fused(const da_dims *dims, const void *feat, const int32_t *sp
     pb.feat = feat;
     pb.loc = loc_weight;
     pb.weights = nullptr;
-    pb.fused = 1;
+    pb.layout = da::kLayoutFused;
+    return DA_OK;
+}
+
+// Checks of the projected layout's inputs; fills pb's projection fields.
+da_status prepare_projected(const da_dims *dims, const void *feat, const int32_t *spatial_shape,
+                            const int32_t *level_start_index, const float *keypoints, const float *projection,
+                            float image_w, float image_h, da::Problem &pb, int &chunks)
+{
+    da_status st = da::prepare_shape(dims, spatial_shape, level_start_index, pb, chunks);
+    if (st != DA_OK) return st;
+    const int64_t n_feat = static_cast<int64_t>(dims->batch) * dims->num_feat_rows * dims->num_embeds;
+    const int64_t n_kp = static_cast<int64_t>(pb.num_ba) * pb.P;
+    const int64_t n_cam = static_cast<int64_t>(pb.B) * pb.K;
+    if (n_kp > INT32_MAX) return fail(DA_ERR_UNSUPPORTED, "batch*anchors*pts exceeds int32");
+    if (n_feat > 0 && !feat) return fail(DA_ERR_NULL, "mc_ms_feat is NULL");
+    if (n_kp > 0 && !keypoints) return fail(DA_ERR_NULL, "keypoints is NULL");
+    if (n_cam > 0 && !projection) return fail(DA_ERR_NULL, "projection is NULL");
+    if (!aligned(feat, 16)) return fail(DA_ERR_ALIGN, "mc_ms_feat must be 16-byte aligned");
+    if (!aligned(keypoints, 4) || !aligned(projection, 4))
+        return fail(DA_ERR_ALIGN, "keypoints and projection must be 4-byte aligned");
+    if (!(image_w > 0.f) || !(image_h > 0.f) || !std::isfinite(image_w) || !std::isfinite(image_h))
+        return fail(DA_ERR_SHAPE, "image size %g x %g must be positive and finite", image_w, image_h);
+    pb.feat = feat;
+    pb.keypoints = keypoints;
+    pb.projection = projection;
+    pb.image_w = image_w;
+    pb.image_h = image_h;
     return DA_OK;
 }
 
@@ -372,6 +400,58 @@ da_status da_backward_fused(const da_dims *dims, const void *mc_ms_feat, const i
     a.grad_loc = grad_loc_weight;
     a.grad_weight = nullptr;
     return backward_impl(*dims, a, chunks, grad_out, grad_feat, nullptr, 0, 0u, stream);
+}
+
+da_status da_forward_projected(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                               const int32_t *level_start_index, const float *keypoints, const float *projection,
+                               float image_w, float image_h, const float *weight_logits, float *out,
+                               float *sampling_location, float *weights, da_stream_t stream)
+{
+    da::FwdArgs a{};
+    int chunks = 0;
+    const da_status st = prepare_projected(dims, mc_ms_feat, spatial_shape, level_start_index, keypoints, projection,
+                                           image_w, image_h, a.pb, chunks);
+    if (st != DA_OK) return st;
+    const int64_t n_w = static_cast<int64_t>(a.pb.num_ba) * a.pb.pks * a.pb.G;
+    if (n_w > 0 && !weight_logits) return fail(DA_ERR_NULL, "weight_logits is NULL");
+    if (!aligned(weight_logits, 4) || !aligned(sampling_location, 4) || !aligned(weights, 4))
+        return fail(DA_ERR_ALIGN, "weight_logits, sampling_location and weights must be 4-byte aligned");
+    a.pb.logits = weight_logits;
+    a.pb.layout = da::kLayoutProj;
+    if (da::projected_smem_bytes(a.pb) > da::kProjectedSmemMax)
+        return fail(DA_ERR_UNSUPPORTED, "projected layout: pts*cams*scales = %d too large for the shared staging",
+                    a.pb.pks);
+    a.loc_out = sampling_location;
+    a.weights_out = weights;
+    return forward_impl(*dims, a, chunks, out, stream);
+}
+
+da_status da_backward_projected(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
+                                const int32_t *level_start_index, const float *keypoints, const float *projection,
+                                float image_w, float image_h, const float *sampling_location, const float *weights,
+                                const float *grad_out, float *grad_feat, float *grad_loc, float *grad_weight,
+                                float *grad_keypoints, float *grad_logits, void *workspace, size_t workspace_bytes,
+                                uint32_t flags, da_stream_t stream)
+{
+    da::Problem pp{};
+    int chunks = 0;
+    da_status st = prepare_projected(dims, mc_ms_feat, spatial_shape, level_start_index, keypoints, projection,
+                                     image_w, image_h, pp, chunks);
+    if (st != DA_OK) return st;
+    const int64_t n_kp = static_cast<int64_t>(pp.num_ba) * pp.P;
+    const int64_t n_w = static_cast<int64_t>(pp.num_ba) * pp.pks * pp.G;
+    if (n_kp > 0 && !grad_keypoints) return fail(DA_ERR_NULL, "grad_keypoints is NULL");
+    if (n_w > 0 && !grad_logits) return fail(DA_ERR_NULL, "grad_logits is NULL");
+    if (!aligned(grad_keypoints, 4) || !aligned(grad_logits, 4))
+        return fail(DA_ERR_ALIGN, "grad_keypoints and grad_logits must be 4-byte aligned");
+    // The operator's backward on the forward's locations and weights.
+    st = da_backward_ex(dims, mc_ms_feat, spatial_shape, level_start_index, sampling_location, weights, grad_out,
+                        grad_feat, grad_loc, grad_weight, workspace, workspace_bytes, flags, stream);
+    if (st != DA_OK) return st;
+    const cudaError_t e = da::launch_projected_chain(pp, weights, grad_loc, grad_weight, grad_keypoints, grad_logits,
+                                                     reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "projected chain-rule launch");
+    return DA_OK;
 }
 
 da_status da_backward_noalloc(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,

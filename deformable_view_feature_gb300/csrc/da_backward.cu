@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
                     const int s = j - p * pb.S;
                     float2 xy;
                     float w;
-                    sample_xyw<FUSED>(pb, ba, g, p * pb.K + k, s, xy, w);
+                    sample_xyw<FUSED ? kLayoutFused : kLayoutStd>(pb, ba, g, p * pb.K + k, s, xy, w);
                     const MapInfo m = maps_s[k * pb.S + s];
                     Footprint f;
                     footprint(xy.x, xy.y, m, f);
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(kThreads) bwd_small_kernel(const BwdArgs args,
                 const int s = j - jk * pb.S;
                 const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
                 float2 xy;
-                sample_xyw<FUSED>(pb, ba, g, jk, s, xy, w[u]);
+                sample_xyw<FUSED ? kLayoutFused : kLayoutStd>(pb, ba, g, jk, s, xy, w[u]);
                 const MapInfo m = maps_s[k * pb.S + s];
                 mw[u] = m.W;
                 mh[u] = m.H;
@@ -426,7 +426,7 @@ cudaError_t launch_layout(const BwdArgs &a, cudaStream_t st)
 template <typename T, int CH>
 cudaError_t launch(const BwdArgs &a, cudaStream_t st)
 {
-    return a.pb.fused ? launch_layout<T, CH, true>(a, st) : launch_layout<T, CH, false>(a, st);
+    return a.pb.layout == kLayoutFused ? launch_layout<T, CH, true>(a, st) : launch_layout<T, CH, false>(a, st);
 }
 
 template <typename T>

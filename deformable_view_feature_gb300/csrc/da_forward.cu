@@ -2,10 +2,14 @@
 //
 // out[b,a,c] = sum_{p,k,s} weights[b,a,p,k,s,g] * bilinear(map (b,k,s), loc[b,a,p,k], c)
 // (page "Inside Sparse4D's CUDA core", §3.2 for the sample and §5.1 for the
-// dimensions summed over). With FUSED, every group has its own location and
-// both come from one tensor: the DCNv4 form y_g = sum_k m_gk x_g(p_gk) of
-// the DCNv4 page ("Defining the problem"), whose offsets and weights one
-// linear layer produces together ("Solving the problem: 1").
+// dimensions summed over). In the fused layout every group has its own
+// location and both come from one tensor: the DCNv4 form
+// y_g = sum_k m_gk x_g(p_gk) of the DCNv4 page ("Defining the problem"),
+// whose offsets and weights one linear layer produces together ("Solving the
+// problem: 1"). In the projected layout the kernel itself projects the
+// anchors' key points into the cameras (the Sparse4D page, §1 and §6) and
+// takes the softmax of the weight logits over each task's P*K*S samples, so
+// no location or weight tensor is read.
 //
 // Work decomposition (the page's kernel uses one thread per sample; here a
 // warp owns one (b*A+a, g) task and its P*K*S samples):
@@ -35,7 +39,10 @@
 namespace da {
 namespace {
 
-template <typename T, int CH, bool FUSED>
+// Anchor of a task within its CTA.
+__device__ __forceinline__ int tq_of(int task, const Problem &pb) { return static_cast<int>(pb.div_G.div(task)); }
+
+template <typename T, int CH, int LAYOUT>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 {
     using Ck = Chunk<T>;
@@ -48,8 +55,11 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 
     __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    // Projected layout only (dynamic): the CTA's projected locations
+    // [anchors_per_cta][P*K], then per warp the softmax numerators of its
+    // task's P*K*S samples.
+    extern __shared__ float2 proj_s[];
     stage_maps(pb, maps_s);
-    __syncthreads();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -61,6 +71,29 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     const int na = min(pb.anchors_per_cta, pb.num_ba - ba0);
     const int ntask = na * pb.G;
     const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
+    float *ebuf = nullptr;
+    if constexpr (LAYOUT == kLayoutProj) {
+        // Each (anchor, point, camera) is projected once for all G groups.
+        for (int i = threadIdx.x; i < na * pb.pk; i += kThreads) {
+            const int tq = i / pb.pk;
+            const int jk = i - tq * pb.pk;
+            const int ba = ba0 + tq;
+            const int p = static_cast<int>(pb.div_K.div(jk));
+            const int k = jk - p * pb.K;
+            const int b = static_cast<int>(pb.div_A.div(ba));
+            const float2 xy = project_point(pb.keypoints + (static_cast<int64_t>(ba) * pb.P + p) * 3,
+                                            pb.projection + (static_cast<int64_t>(b) * pb.K + k) * 16, pb.image_w,
+                                            pb.image_h);
+            proj_s[i] = xy;
+            if (args.loc_out) {
+                float *o = args.loc_out + (static_cast<int64_t>(ba) * pb.pk + jk) * 2;
+                o[0] = xy.x;
+                o[1] = xy.y;
+            }
+        }
+        ebuf = reinterpret_cast<float *>(proj_s + pb.anchors_per_cta * pb.pk) + warp * pb.pks;
+    }
+    __syncthreads();
 
     for (int task = warp; task < ntask; task += kWarps) {
         const int tq = static_cast<int>(pb.div_G.div(task));
@@ -74,6 +107,27 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 #pragma unroll
         for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
 
+        // Projected layout: the softmax over the task's samples. The
+        // numerators exp(z - max) go to the warp's buffer; 1/sum scales them.
+        float inv_sum = 1.f;
+        if constexpr (LAYOUT == kLayoutProj) {
+            const float *z = pb.logits + static_cast<int64_t>(ba) * pb.pks * pb.G + g;
+            float m = -INFINITY;
+            for (int j = lane; j < pb.pks; j += 32) m = fmaxf(m, z[static_cast<int64_t>(j) * pb.G]);
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+            float sum = 0.f;
+            for (int j = lane; j < pb.pks; j += 32) {
+                const float e = expf(z[static_cast<int64_t>(j) * pb.G] - m);
+                ebuf[j] = e;
+                sum += e;
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+            inv_sum = 1.f / sum;
+            __syncwarp();
+        }
+
         for (int j0 = 0; j0 < pb.pks; j0 += 32) {
             const int n = min(32, pb.pks - j0);
             {
@@ -86,7 +140,14 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                     const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
                     float2 xy;
                     float w;
-                    sample_xyw<FUSED>(pb, ba, g, jk, s, xy, w);
+                    if constexpr (LAYOUT == kLayoutProj) {
+                        xy = proj_s[tq_of(task, pb) * pb.pk + jk];
+                        w = ebuf[j] * inv_sum;
+                        if (args.weights_out)
+                            args.weights_out[((static_cast<int64_t>(ba) * pb.pk + jk) * pb.S + s) * pb.G + g] = w;
+                    } else {
+                        sample_xyw<LAYOUT>(pb, ba, g, jk, s, xy, w);
+                    }
                     Footprint f;
                     footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
 #pragma unroll
@@ -202,7 +263,7 @@ __global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args,
                 const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
                 float2 xy;
                 float w;
-                sample_xyw<FUSED>(pb, it_ba, it_g, jk, s, xy, w);
+                sample_xyw<FUSED ? kLayoutFused : kLayoutStd>(pb, it_ba, it_g, jk, s, xy, w);
                 Footprint f;
                 footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
 #pragma unroll
@@ -257,7 +318,7 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
 {
     constexpr int ESZ = 16 / Chunk<T>::kVec;
     const int cpa = a.pb.C * ESZ / 16;
-    if (use_small_task_kernels(a.pb, ESZ) && (cpa & (cpa - 1)) == 0) {
+    if (a.pb.layout != kLayoutProj && use_small_task_kernels(a.pb, ESZ) && (cpa & (cpa - 1)) == 0) {
         int cpa_log2 = 0;
         while ((1 << cpa_log2) < cpa) ++cpa_log2;
         const int apw = 32 >> cpa_log2;
@@ -268,7 +329,7 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
             const int64_t warps = (static_cast<int64_t>(a.pb.num_ba) + apw - 1) / apw;
             const int64_t grid = (warps + kWarps - 1) / kWarps;
             if (grid == 0) return cudaSuccess;
-            if (a.pb.fused)
+            if (a.pb.layout == kLayoutFused)
                 fwd_small_kernel<T, true><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa_log2, jstep);
             else
                 fwd_small_kernel<T, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa_log2, jstep);
@@ -277,10 +338,21 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
     }
     const int64_t grid = sampling_grid(a.pb);
     if (grid == 0) return cudaSuccess;
-    if (a.pb.fused)
-        fwd_kernel<T, CH, true><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
-    else
-        fwd_kernel<T, CH, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a);
+    switch (a.pb.layout) {
+        case kLayoutFused: fwd_kernel<T, CH, kLayoutFused><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
+        case kLayoutProj: {
+            const size_t smem = projected_smem_bytes(a.pb);
+            if (smem > 48 * 1024) {
+                const cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, CH, kLayoutProj>,
+                                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                           static_cast<int>(smem));
+                if (e != cudaSuccess) return e;
+            }
+            fwd_kernel<T, CH, kLayoutProj><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+            break;
+        }
+        default: fwd_kernel<T, CH, kLayoutStd><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
+    }
     return cudaGetLastError();
 }
 

@@ -40,13 +40,24 @@ struct FastDiv {
 
 // Everything a sampling kernel needs about the problem. It is passed by value
 // as a kernel parameter; the kernels copy the map table to shared memory.
+constexpr int kLayoutStd = 0;    // loc + weights
+constexpr int kLayoutFused = 1;  // per-group loc_weight (the DCNv4 form)
+constexpr int kLayoutProj = 2;   // key points + cameras + logits
+
 struct Problem {
     const void *feat;
     // Standard layout: loc [B,A,P,K,2] and weights [B,A,P,K,S,G].
     // Fused per-group layout (the DCNv4 form): loc points to
     // loc_weight [B,A,G,P,K,2+S] = (x, y, w_0 .. w_{S-1}) and weights is NULL.
+    // Projected layout (forward only): loc and weights are NULL; the
+    // locations come from keypoints [B,A,P,3] through projection [B,K,4,4]
+    // and the weights are a softmax of logits [B,A,P,K,S,G].
     const float *loc;
     const float *weights;
+    const float *keypoints;
+    const float *projection;
+    const float *logits;
+    float image_w, image_h;
     int64_t rows;             // feature rows per batch item
     int32_t B, A, P, K, S, C, G, D;
     int32_t pks;              // P*K*S samples per (b, a, g)
@@ -54,7 +65,7 @@ struct Problem {
     int32_t num_ba;           // B*A
     int32_t anchors_per_cta;  // anchors (or views) owned by one CTA, all groups
     int32_t nmaps;            // K*S
-    int32_t fused;            // 1: the fused per-group layout
+    int32_t layout;           // kLayoutStd, kLayoutFused or kLayoutProj
     FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS, div_rows;
     MapInfo maps[DA_MAX_MAPS];
 };
@@ -62,6 +73,10 @@ struct Problem {
 struct FwdArgs {
     Problem pb;
     float *out;
+    // Projected layout only: where to write the computed locations
+    // [B,A,P,K,2] and weights [B,A,P,K,S,G]; NULL = do not write.
+    float *loc_out;
+    float *weights_out;
 };
 
 struct BwdArgs {
@@ -131,6 +146,12 @@ cudaError_t launch_forward(const FwdArgs &a, int feat_dtype, int chunks, cudaStr
 cudaError_t launch_backward(const BwdArgs &a, int feat_dtype, int chunks, cudaStream_t st);
 cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st);
 cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st);
+// Chain rule of the projected layout: grad_logits and grad_keypoints from the
+// operator's grad_loc and grad_weight (pb holds keypoints, projection, image
+// size).
+cudaError_t launch_projected_chain(const Problem &pb, const float *weights, const float *grad_loc,
+                                   const float *grad_weight, float *grad_keypoints, float *grad_logits,
+                                   cudaStream_t st);
 
 // Host-side helpers of the entry points (da_abi.cu).
 // fail: records a one-line reason for da_last_error() and returns st.
@@ -147,7 +168,8 @@ da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const
 // of one CTA's views (per group in the fused layout).
 inline size_t scatter_smem_bytes(const Problem &pb)
 {
-    return static_cast<size_t>(pb.anchors_per_cta) * (pb.fused ? pb.G : 1) * pb.P * 2 * sizeof(float);
+    return static_cast<size_t>(pb.anchors_per_cta) * (pb.layout == kLayoutFused ? pb.G : 1) * pb.P * 2 *
+           sizeof(float);
 }
 
 // Whether the forward and the scatter backward take the thread-per-chunk
@@ -159,6 +181,14 @@ inline bool use_small_task_kernels(const Problem &pb, int elem_bytes)
     return pb.pks <= 16 && cpa <= 32 && (pb.C * elem_bytes) % 16 == 0;
 }
 
+// Dynamic shared memory of the projected forward: the CTA's projected
+// locations and one buffer of softmax numerators per warp.
+inline size_t projected_smem_bytes(const Problem &pb)
+{
+    return static_cast<size_t>(pb.anchors_per_cta) * pb.pk * 8 + static_cast<size_t>(kWarps) * pb.pks * 4;
+}
+constexpr size_t kProjectedSmemMax = 160 * 1024;
+
 // Grid size that covers num_ba anchors, anchors_per_cta at a time.
 inline int64_t sampling_grid(const Problem &pb)
 {
@@ -167,15 +197,33 @@ inline int64_t sampling_grid(const Problem &pb)
 
 // ------------------------------------------------------------------ device helpers
 
+// Normalised location of key point kp seen through camera matrix m: the
+// pinhole reading of the Sparse4D page's projection step (§1, §6), in fp32
+// with every product, sum and quotient rounded in this order (the location
+// decides which pixels are read):
+//   ud = ((m00*X + m01*Y) + m02*Z) + m03, vd and d likewise with rows 1, 2;
+//   x = (ud / d) / image_w, y = (vd / d) / image_h;
+// (NaN, NaN) when d <= 1e-5 (behind the camera), which reads nothing.
+__device__ __forceinline__ float2 project_point(const float *kp, const float *m, float image_w, float image_h)
+{
+    const float X = kp[0], Y = kp[1], Z = kp[2];
+    const float ud = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(m[0], X), __fmul_rn(m[1], Y)), __fmul_rn(m[2], Z)), m[3]);
+    const float vd = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(m[4], X), __fmul_rn(m[5], Y)), __fmul_rn(m[6], Z)), m[7]);
+    const float d = __fadd_rn(__fadd_rn(__fadd_rn(__fmul_rn(m[8], X), __fmul_rn(m[9], Y)), __fmul_rn(m[10], Z)), m[11]);
+    if (!(d > 1e-5f)) return make_float2(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+    return make_float2(__fdiv_rn(__fdiv_rn(ud, d), image_w), __fdiv_rn(__fdiv_rn(vd, d), image_h));
+}
+
 // Location (x, y) and weight of the sample (b*A + a = ba, group g,
-// jk = p*K + k, scale s) in either layout (see Problem). In the fused layout
+// jk = p*K + k, scale s) in the standard or the fused layout (see Problem). In the fused layout
 // the entry of (ba, g, jk) holds 2 + S floats, so (x, y) need not be 8-byte
-// aligned and is read as two floats.
-template <bool FUSED>
+// aligned and is read as two floats. (The projected layout computes both in
+// the forward kernel itself.)
+template <int LAYOUT>
 __device__ __forceinline__ void sample_xyw(const Problem &pb, int64_t ba, int g, int jk, int s, float2 &xy,
                                            float &w)
 {
-    if constexpr (FUSED) {
+    if constexpr (LAYOUT == kLayoutFused) {
         const float *e = pb.loc + ((ba * pb.G + g) * pb.pk + jk) * (2 + pb.S);
         xy = make_float2(e[0], e[1]);
         w = e[2 + s];

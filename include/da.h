@@ -258,6 +258,77 @@ da_status da_backward_fused(const da_dims *dims,
                             da_stream_t stream);
 
 /*
+ * The step before the operator, fused into it (the projected layout).
+ *
+ * The Sparse4D page (§1, §6) projects each 3D anchor's key points into every
+ * camera view before the aggregation, and the Sparse4D head normalises the
+ * weights with a softmax. Here the forward kernel does both while it builds
+ * the samples, so no location or weight tensor has to be written and read
+ * back in between:
+ *   keypoints     device [B, A, P, 3] fp32 (X, Y, Z), 4-byte aligned.
+ *   projection    device [B, K, 4, 4] fp32 row-major: rows 0..2 map
+ *                 (X, Y, Z, 1) to (u*d, v*d, d) in pixels; row 3 is unused.
+ *   image_w, image_h  the image size in pixels (> 0).
+ *   weight_logits device [B, A, P, K, S, G] fp32, 4-byte aligned.
+ * The page gives no formula; the reading is the pinhole projection:
+ *   ud = ((m00*X + m01*Y) + m02*Z) + m03, vd and d likewise (rows 1, 2),
+ *   x = (ud / d) / image_w, y = (vd / d) / image_h,
+ * every step an fp32 operation rounded in this order (no fused
+ * multiply-add), because the location decides which pixels are read. A key
+ * point with d <= 1e-5 (behind the camera) gets the location (NaN, NaN) and
+ * reads nothing. weights = softmax of the logits over the P*K*S samples of
+ * each (b, a, g). Then out is da_forward's.
+ *
+ * da_forward_projected also writes the locations [B, A, P, K, 2] and the
+ * weights [B, A, P, K, S, G] it used when sampling_location / weights are
+ * not NULL (the backward needs them).
+ *
+ * da_backward_projected takes those two tensors, runs da_backward_ex on
+ * them (grad_feat, grad_loc, grad_weight, workspace and flags as there), and
+ * then the chain rule:
+ *   grad_logits    [B, A, P, K, S, G]: w * (grad_weight - sum over
+ *                  (p, k, s) of w * grad_weight), per (b, a, g);
+ *   grad_keypoints [B, A, P, 3]: sum over k of J_k^T grad_loc[b,a,p,k,:],
+ *                  J_k the derivative of (x, y) above; 0 for cameras the
+ *                  point is behind.
+ * grad_loc and grad_weight are outputs too (the chain rule reads them).
+ */
+da_status da_forward_projected(const da_dims *dims,
+                               const void *mc_ms_feat,
+                               const int32_t *spatial_shape,
+                               const int32_t *level_start_index,
+                               const float *keypoints,
+                               const float *projection,
+                               float image_w,
+                               float image_h,
+                               const float *weight_logits,
+                               float *out,
+                               float *sampling_location,
+                               float *weights,
+                               da_stream_t stream);
+
+da_status da_backward_projected(const da_dims *dims,
+                                const void *mc_ms_feat,
+                                const int32_t *spatial_shape,
+                                const int32_t *level_start_index,
+                                const float *keypoints,
+                                const float *projection,
+                                float image_w,
+                                float image_h,
+                                const float *sampling_location,
+                                const float *weights,
+                                const float *grad_out,
+                                float *grad_feat,
+                                float *grad_loc,
+                                float *grad_weight,
+                                float *grad_keypoints,
+                                float *grad_logits,
+                                void *workspace,
+                                size_t workspace_bytes,
+                                uint32_t flags,
+                                da_stream_t stream);
+
+/*
  * da_backward_noalloc: the binned backward, with its scratch in a fixed
  * array of DA_NOALLOC_SCRATCH_BYTES that the library carries in device
  * memory. No call allocates anything.

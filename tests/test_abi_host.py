@@ -229,3 +229,23 @@ def test_pipeline_create_without_gpu_fails_cleanly(lib):
     assert lib.da_pipeline_create(ctypes.byref(_dims()), ss, ls, 1, 2, ctypes.byref(h)) == 5  # DA_ERR_CUDA
     assert not h.value
     assert b"pipeline set-up" in lib.da_last_error()
+
+
+def test_binding_signatures_reach_validation(lib):
+    """Every entry point called through the argtypes the Python binding
+    declares: arguments that fail validation come back as the documented
+    status before any CUDA call, which also checks the declared argument
+    counts."""
+    bl = da.load_library()
+    ss, ls = _tables()
+    d = ctypes.byref(_dims())
+    F = FAKE
+    # Fused layout: a misaligned loc_weight.
+    assert bl.da_forward_fused(d, F, ss, ls, F + 2, F, None) == DA_ERR_ALIGN
+    assert bl.da_backward_fused(d, F, ss, ls, F + 2, F, F, F, None, 0, None) == DA_ERR_ALIGN
+    # Projected layout: a zero image width.
+    assert bl.da_forward_projected(d, F, ss, ls, F, F, 0.0, 4.0, F, F, None, None, None) == DA_ERR_SHAPE
+    assert bl.da_backward_projected(d, F, ss, ls, F, F, 0.0, 4.0, F, F, F, F, F, F, F, F, None, 0, 0,
+                                    None) == DA_ERR_SHAPE
+    assert bl.da_backward_ex(d, F, ss, ls, F, F, F, F, F, F, None, 0, 2, None) == DA_ERR_SHAPE
+    assert b"flags" in bl.da_last_error()
