@@ -323,6 +323,62 @@ def make_projected_inputs(wl: Workload | str, seed: Optional[int] = None) -> Pro
                            logits, grad_out)
 
 
+@dataclasses.dataclass
+class WarpAffineInputs:
+    """Inputs of the warpaffine preprocessing (the warpaffine page, §3-§4):
+    8-bit BGR frames in HWC layout, one destination->source affine matrix per
+    frame, the fill value and the per-channel normalisation."""
+    src: torch.Tensor  # [B, H, W, 3] uint8
+    d2i: torch.Tensor  # [B, 6] float32: src_x = m0*dx + m1*dy + m2, src_y = m3*dx + m4*dy + m5
+    dst_hw: Tuple[int, int]
+    fill: int
+    mean: torch.Tensor  # [3] float32, source channel order (B, G, R)
+    std: torch.Tensor  # [3] float32
+
+
+# The page's benchmark: 1920x1080 frames resized to 640x640 (its §4.3).
+WARPAFFINE_SRC_HW = (1080, 1920)
+WARPAFFINE_DST_HW = (640, 640)
+
+
+def letterbox_d2i(src_hw, dst_hw) -> np.ndarray:
+    """The destination->source matrix of a letterbox resize: scale by
+    s = min(Wd/W, Hd/H) and centre (input construction, float64; the inverse
+    of i2d = [s, 0, (Wd - s*W)/2; 0, s, (Hd - s*H)/2])."""
+    (H, W), (Hd, Wd) = src_hw, dst_hw
+    s = min(Wd / W, Hd / H)
+    tx, ty = (Wd - s * W) / 2.0, (Hd - s * H) / 2.0
+    return np.array([1.0 / s, 0.0, -tx / s, 0.0, 1.0 / s, -ty / s])
+
+
+def make_warpaffine_inputs(batch: int = 64, src_hw=WARPAFFINE_SRC_HW, dst_hw=WARPAFFINE_DST_HW, seed: int = 7,
+                           jitter: bool = True) -> WarpAffineInputs:
+    """Uniform random bytes for the frames. Every frame gets the letterbox
+    matrix, and with jitter also a small random rotation (up to 5 degrees)
+    and zoom (up to 10 %) about the destination centre, as an augmenting
+    pipeline would."""
+    g = torch.Generator().manual_seed(seed)
+    H, W = src_hw
+    src = torch.randint(0, 256, (batch, H, W, 3), generator=g, dtype=torch.int32).to(torch.uint8)
+    base = letterbox_d2i(src_hw, dst_hw)
+    mats = np.empty((batch, 6))
+    r = torch.rand(batch, 2, generator=g, dtype=torch.float64).numpy()
+    for b in range(batch):
+        m = base.copy()
+        if jitter:
+            ang = np.deg2rad(10.0 * r[b, 0] - 5.0)
+            zoom = 0.9 + 0.2 * r[b, 1]
+            cx, cy = dst_hw[1] / 2.0, dst_hw[0] / 2.0
+            # destination pixel -> rotated/zoomed destination pixel -> source
+            c, s_ = np.cos(ang) / zoom, np.sin(ang) / zoom
+            rot = np.array([[c, -s_, cx - c * cx + s_ * cy], [s_, c, cy - s_ * cx - c * cy], [0, 0, 1.0]])
+            full = np.vstack([m.reshape(2, 3), [0, 0, 1.0]]) @ rot
+            m = full[:2].reshape(6)
+        mats[b] = m
+    return WarpAffineInputs(src, torch.from_numpy(mats).to(torch.float32), tuple(dst_hw), 114,
+                            torch.tensor([0.406, 0.456, 0.485]), torch.tensor([0.225, 0.224, 0.229]))
+
+
 def small_variant(name: str, batch: int = 1, num_anchors: int = 24) -> Workload:
     """A cut-down copy of a named workload with the same maps, channels and
     distributions but few anchors, for fast CPU/GPU parity runs."""

@@ -1,7 +1,8 @@
 """CPU oracle for the deformable-aggregation operator (test infrastructure).
 
 This package wraps ``da_oracle.c``, a plain single-threaded C implementation
-of what the operator computes, through ctypes. Only these may import it:
+of what the operator computes, and ``wa_oracle.c``, the same for the
+warpaffine preprocessing kernels, through ctypes. Only these may import it:
 
 * the tests;
 * ``__graft_entry__.smoke()``;
@@ -22,6 +23,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "da_oracle.c")
+_SRCS = [_SRC, os.path.join(_HERE, "wa_oracle.c")]
 _LIB = os.path.join(_HERE, "_build", "libda_oracle.so")
 
 # -ffp-contract=off: the coordinate step must round twice (see da_oracle.c).
@@ -33,11 +35,11 @@ _lib = None
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc into ``oracle/_build``; return the .so path."""
     if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+            and all(os.path.getmtime(_LIB) >= os.path.getmtime(src) for src in _SRCS)):
         return _LIB
     os.makedirs(os.path.dirname(_LIB), exist_ok=True)
     tmp = _LIB + f".tmp{os.getpid()}"
-    subprocess.run(["gcc", *CFLAGS, _SRC, "-o", tmp, "-lm"], check=True)
+    subprocess.run(["gcc", *CFLAGS, *_SRCS, "-o", tmp, "-lm"], check=True)
     os.replace(tmp, _LIB)
     return _LIB
 
@@ -66,6 +68,10 @@ def _load():
         lib.dao_softmax_weights.restype = i32
         lib.dao_projected_chain.argtypes = [i32] * 6 + [vp, vp, f32, f32, vp, vp, vp, vp, vp]
         lib.dao_projected_chain.restype = i32
+        lib.wao_warpaffine_u8.argtypes = [i32] * 5 + [vp, vp, ctypes.c_uint8, vp]
+        lib.wao_warpaffine_u8.restype = i32
+        lib.wao_warpaffine_preprocess.argtypes = [i32] * 5 + [vp, vp, ctypes.c_uint8, vp, vp, vp]
+        lib.wao_warpaffine_preprocess.restype = i32
         lib.dao_bilinear.argtypes = [vp, i32, i32, i32, i32, ctypes.c_float, ctypes.c_float]
         lib.dao_bilinear.restype = ctypes.c_double
         _lib = lib
@@ -256,6 +262,35 @@ def backward_projected(feat, spatial_shape, level_start_index, keypoints, projec
     gf, gl, gw = backward(feat, spatial_shape, level_start_index, loc, w, grad_out)
     gkp, glg = projected_chain(keypoints, projection, image_w, image_h, w, gl, gw)
     return gf, gl, gw, gkp, glg
+
+
+def warpaffine_u8(src, d2i, dst_hw, fill: int) -> np.ndarray:
+    """src [B, H, W, 3] uint8, d2i [B, 6] (destination -> source) -> [B, Hd, Wd, 3] uint8."""
+    src = np.ascontiguousarray(src, dtype=np.uint8)
+    d2i = np.ascontiguousarray(d2i, dtype=np.float32).reshape(-1, 6)
+    B, H, W, C = src.shape
+    assert C == 3 and d2i.shape[0] == B
+    Hd, Wd = dst_hw
+    dst = np.empty((B, Hd, Wd, 3), np.uint8)
+    if _load().wao_warpaffine_u8(B, H, W, Hd, Wd, _ptr(src), _ptr(d2i), int(fill), _ptr(dst)) != 0:
+        raise ValueError("oracle warpaffine rejected its arguments")
+    return dst
+
+
+def warpaffine_preprocess(src, d2i, dst_hw, fill: int, mean, std) -> np.ndarray:
+    """The fused preprocessing: [B, 3, Hd, Wd] float32, RGB planes normalised."""
+    src = np.ascontiguousarray(src, dtype=np.uint8)
+    d2i = np.ascontiguousarray(d2i, dtype=np.float32).reshape(-1, 6)
+    mean = np.ascontiguousarray(mean, dtype=np.float32)
+    std = np.ascontiguousarray(std, dtype=np.float32)
+    B, H, W, C = src.shape
+    assert C == 3 and d2i.shape[0] == B and mean.shape == (3,) and std.shape == (3,)
+    Hd, Wd = dst_hw
+    dst = np.empty((B, 3, Hd, Wd), np.float32)
+    if _load().wao_warpaffine_preprocess(B, H, W, Hd, Wd, _ptr(src), _ptr(d2i), int(fill), _ptr(mean), _ptr(std),
+                                         _ptr(dst)) != 0:
+        raise ValueError("oracle preprocess rejected its arguments")
+    return dst
 
 
 def bilinear(fmap: np.ndarray, c: int, x: float, y: float) -> float:
