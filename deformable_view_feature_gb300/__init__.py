@@ -27,7 +27,7 @@ import torch
 from . import build as _build
 
 __all__ = ["da_forward", "da_backward", "da_forward_fused", "da_backward_fused", "da_forward_projected",
-           "da_backward_projected", "backward_workspace_size",
+           "da_backward_projected", "warpaffine_u8", "warpaffine_preprocess", "backward_workspace_size",
            "DeformableAggregationFunction", "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
 
 DA_F32, DA_BF16, DA_F16 = 0, 1, 2
@@ -49,6 +49,11 @@ class DaDims(ctypes.Structure):
                 ("num_groups", ctypes.c_int32), ("num_anchors", ctypes.c_int32),
                 ("num_pts", ctypes.c_int32), ("feat_dtype", ctypes.c_int32),
                 ("num_feat_rows", ctypes.c_int64)]
+
+
+class WaDims(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int32), ("src_h", ctypes.c_int32), ("src_w", ctypes.c_int32),
+                ("dst_h", ctypes.c_int32), ("dst_w", ctypes.c_int32)]
 
 
 _lib = None
@@ -87,6 +92,10 @@ def load_library():
     lib.da_backward_projected.argtypes = ([ctypes.POINTER(DaDims), vp, vp, vp, vp, vp, f32, f32]
                                           + [vp] * 9 + [ctypes.c_size_t, ctypes.c_uint32, vp])
     lib.da_backward_projected.restype = ctypes.c_int
+    lib.wa_warpaffine_u8.argtypes = [ctypes.POINTER(WaDims), vp, vp, ctypes.c_uint8, vp, vp]
+    lib.wa_warpaffine_u8.restype = ctypes.c_int
+    lib.wa_preprocess.argtypes = [ctypes.POINTER(WaDims), vp, vp, ctypes.c_uint8, vp, vp, vp, vp]
+    lib.wa_preprocess.restype = ctypes.c_int
     lib.da_backward_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
     lib.da_backward_workspace_size.restype = ctypes.c_int
     lib.da_status_string.argtypes = [ctypes.c_int]
@@ -480,6 +489,42 @@ def da_backward_projected(mc_ms_feat, spatial_shape, level_start_index, keypoint
                                      _dptr(grad_out), _dptr(gf), _dptr(gl), _dptr(gw), _dptr(gkp), _dptr(glg),
                                      ws_ptr, ws_bytes, 1 if deterministic else 0, sh))
     return gf, gl, gw, gkp, glg
+
+
+def _wa_args(src: torch.Tensor, d2i: torch.Tensor, dst_hw) -> WaDims:
+    if src.dim() != 4 or src.shape[-1] != 3 or src.dtype != torch.uint8:
+        raise ValueError("src must be uint8 [B, H, W, 3]")
+    B, H, W, _ = src.shape
+    if tuple(d2i.shape) != (B, 6) or d2i.dtype != torch.float32:
+        raise ValueError("d2i must be float32 [B, 6]")
+    return WaDims(B, H, W, int(dst_hw[0]), int(dst_hw[1]))
+
+
+def warpaffine_u8(src: torch.Tensor, d2i: torch.Tensor, dst_hw, fill: int = 114, stream=None) -> torch.Tensor:
+    """wa_warpaffine_u8: frames [B, H, W, 3] uint8 warped by the destination ->
+    source matrices d2i [B, 6] into [B, Hd, Wd, 3] uint8."""
+    lib = load_library()
+    d = _wa_args(src, d2i, dst_hw)
+    dst = torch.empty(d.batch, d.dst_h, d.dst_w, 3, dtype=torch.uint8, device=src.device)
+    _check(lib.wa_warpaffine_u8(ctypes.byref(d), _dptr(src), _dptr(d2i), int(fill), _dptr(dst),
+                                _stream_handle(stream)))
+    return dst
+
+
+def warpaffine_preprocess(src: torch.Tensor, d2i: torch.Tensor, dst_hw, fill: int = 114, mean=(0.406, 0.456, 0.485),
+                          std=(0.225, 0.224, 0.229), stream=None) -> torch.Tensor:
+    """wa_preprocess: warp, BGR -> RGB, (v/255 - mean)/std, HWC -> CHW: [B, 3, Hd, Wd] float32.
+    mean and std are in the source's (BGR) channel order."""
+    lib = load_library()
+    d = _wa_args(src, d2i, dst_hw)
+    m = torch.tensor(mean, dtype=torch.float32)
+    s = torch.tensor(std, dtype=torch.float32)
+    if m.numel() != 3 or s.numel() != 3:
+        raise ValueError("mean and std take 3 values")
+    dst = torch.empty(d.batch, 3, d.dst_h, d.dst_w, dtype=torch.float32, device=src.device)
+    _check(lib.wa_preprocess(ctypes.byref(d), _dptr(src), _dptr(d2i), int(fill), m.data_ptr(), s.data_ptr(),
+                             _dptr(dst), _stream_handle(stream)))
+    return dst
 
 
 class DeformableAggregationFunction(torch.autograd.Function):

@@ -29,17 +29,22 @@ def lib():
 
 
 def _declared_functions():
-    text = open(HEADER).read()
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(da_[a-z_]+)\s*\(", text)))
+    names = set()
+    for h in sorted(os.listdir(os.path.dirname(HEADER))):
+        if h.endswith(".h"):
+            text = open(os.path.join(os.path.dirname(HEADER), h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names |= set(re.findall(r"\b((?:da|wa)_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
 
 
 def test_library_exports_every_declared_function(lib):
     names = _declared_functions()
-    assert {"da_forward", "da_backward", "da_status_string", "da_last_error", "da_version"} <= set(names)
+    assert {"da_forward", "da_backward", "da_status_string", "da_last_error", "da_version",
+            "wa_warpaffine_u8", "wa_preprocess"} <= set(names)
     out = subprocess.run(["nm", "-D", "--defined-only", da.library_path()], capture_output=True,
                          text=True, check=True).stdout
-    exported = set(re.findall(r"\bT (da_\w+)", out))
+    exported = set(re.findall(r"\bT ((?:da|wa)_\w+)", out))
     missing = [n for n in names if n not in exported]
     assert not missing, f"declared in da.h but not exported: {missing}"
     for n in names:
@@ -48,7 +53,8 @@ def test_library_exports_every_declared_function(lib):
 
 def test_header_compiles_as_plain_c(tmp_path):
     src = tmp_path / "use.c"
-    src.write_text('#include "da.h"\nint main(void){ da_dims d = {0}; (void)d; return (int)DA_OK; }\n')
+    src.write_text('#include "da.h"\n#include "wa.h"\n'
+                   'int main(void){ da_dims d = {0}; wa_dims w = {0}; (void)d; (void)w; return (int)DA_OK; }\n')
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-I", os.path.dirname(HEADER), "-c",
                     str(src), "-o", str(tmp_path / "use.o")], check=True)
 
@@ -249,3 +255,18 @@ def test_binding_signatures_reach_validation(lib):
                                     None) == DA_ERR_SHAPE
     assert bl.da_backward_ex(d, F, ss, ls, F, F, F, F, F, F, None, 0, 2, None) == DA_ERR_SHAPE
     assert b"flags" in bl.da_last_error()
+
+
+def test_warpaffine_validation_without_gpu(lib):
+    bl = da.load_library()
+    bad = da.WaDims(1, 0, 4, 2, 2)  # zero source height
+    assert bl.wa_warpaffine_u8(ctypes.byref(bad), FAKE, FAKE, 0, FAKE, None) == DA_ERR_SHAPE
+    ok = da.WaDims(1, 4, 4, 2, 2)
+    assert bl.wa_warpaffine_u8(ctypes.byref(ok), FAKE, FAKE + 2, 0, FAKE, None) == DA_ERR_ALIGN
+    assert bl.wa_warpaffine_u8(ctypes.byref(ok), None, FAKE, 0, FAKE, None) == DA_ERR_NULL
+    mean = (ctypes.c_float * 3)(0.5, 0.5, 0.5)
+    std = (ctypes.c_float * 3)(0.2, -1.0, 0.2)
+    assert bl.wa_preprocess(ctypes.byref(ok), FAKE, FAKE, 0, mean, std, FAKE, None) == DA_ERR_SHAPE
+    assert bl.wa_preprocess(ctypes.byref(ok), FAKE, FAKE, 0, mean, mean, FAKE + 2, None) == DA_ERR_ALIGN
+    empty = da.WaDims(0, 4, 4, 2, 2)
+    assert bl.wa_warpaffine_u8(ctypes.byref(empty), None, None, 0, None, None) == DA_OK
