@@ -6,7 +6,8 @@
 // (b, a) into camera k and takes a softmax of the logits over the P*K*S
 // samples of each (b, a, g). Its derivatives:
 //   grad_logits = w * (grad_weight - sum over (p,k,s) of w * grad_weight),
-//     per (b, a, g): one warp per task, a shuffle sum;
+//     per (b, a, g): one warp per anchor (all groups, coalesced) when G
+//     divides 32, else one warp per (anchor, group); shuffle sums;
 //   grad_keypoints[b,a,p,:] = sum over k of J_k^T grad_loc[b,a,p,k,:], with
 //     x = (ud/d)/image_w, y = (vd/d)/image_h and u = ud/d, v = vd/d:
 //     dx/dX_i = (m0i - u*m2i) / (d*image_w), dy/dX_i = (m1i - v*m2i) / (d*image_h),
@@ -37,6 +38,24 @@ __global__ void __launch_bounds__(256) logits_grad_kernel(const Problem pb, cons
         const int64_t e = base + static_cast<int64_t>(j) * pb.G;
         glog[e] = w[e] * (gw[e] - dot);
     }
+}
+
+// The same for G dividing 32, coalesced: one warp per anchor reads its
+// P*K*S*G contiguous weights as whole 128-byte lines. Lane l only ever sees
+// group l % G, so the per-group sums are lane partials summed over the lanes
+// of that group (xor shuffles over the bits above log2(G)).
+__global__ void __launch_bounds__(256) logits_grad_anchor_kernel(const Problem pb, const float *w, const float *gw,
+                                                                 float *glog)
+{
+    const int64_t ba = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (ba >= pb.num_ba) return;  // whole warps leave together
+    const int64_t n = static_cast<int64_t>(pb.pks) * pb.G;
+    const int64_t base = ba * n;
+    float dot = 0.f;
+    for (int64_t e = lane; e < n; e += 32) dot = fmaf(w[base + e], gw[base + e], dot);
+    for (int o = pb.G; o < 32; o <<= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    for (int64_t e = lane; e < n; e += 32) glog[base + e] = w[base + e] * (gw[base + e] - dot);
 }
 
 __global__ void __launch_bounds__(256) keypoint_grad_kernel(const Problem pb, const float *grad_loc, float *gkp)
@@ -73,8 +92,12 @@ cudaError_t launch_projected_chain(const Problem &pb, const float *weights, cons
 {
     const int64_t tasks = static_cast<int64_t>(pb.num_ba) * pb.G;
     if (tasks > 0 && pb.pks > 0) {
-        logits_grad_kernel<<<static_cast<unsigned>((tasks * 32 + 255) / 256), 256, 0, st>>>(pb, weights, grad_weight,
-                                                                                          grad_logits);
+        if (32 % pb.G == 0)
+            logits_grad_anchor_kernel<<<static_cast<unsigned>((static_cast<int64_t>(pb.num_ba) * 32 + 255) / 256), 256,
+                                        0, st>>>(pb, weights, grad_weight, grad_logits);
+        else
+            logits_grad_kernel<<<static_cast<unsigned>((tasks * 32 + 255) / 256), 256, 0, st>>>(pb, weights, grad_weight,
+                                                                                              grad_logits);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

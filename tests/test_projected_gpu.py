@@ -113,12 +113,15 @@ def test_small_shape_both_backward_paths(da, path, deterministic):
     _check(inp, _run(da, inp, path=path, deterministic=deterministic))
 
 
-def test_one_camera_one_scale_bf16(da):
+# G = 3 takes the per-(anchor, group) logits kernel; C = 48 is not a power of
+# two, so its backward takes the scatter path.
+@pytest.mark.parametrize("C,G,path", [(64, 4, "binned"), (48, 3, "scatter")])
+def test_one_camera_one_scale_bf16(da, C, G, path):
     wl = da_inputs.WORKLOADS["sp4d_proj"].replace(name="proj_k1", batch=1, num_cams=1, shapes=((32, 80),),
-                                                  num_embeds=64, num_groups=4, num_anchors=50, num_pts=7,
+                                                  num_embeds=C, num_groups=G, num_anchors=50, num_pts=7,
                                                   feat_dtype="bf16")
     inp = da_inputs.make_projected_inputs(wl, seed=10)
-    _check(inp, _run(da, inp))
+    _check(inp, _run(da, inp, path=path))
 
 
 def test_forward_without_kept_samples_gives_the_same_out(da):
