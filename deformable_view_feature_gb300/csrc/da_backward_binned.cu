@@ -610,8 +610,13 @@ __global__ void __launch_bounds__(kPullThreads) pull_kernel(const PullArgs args)
     const int q = lane / LPR, sub = lane % LPR;
     const int g = sub / LPG, gsub = sub % LPG;
     const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5;
-    const int64_t R = args.row_begin + warp_id * RPW + q;
-    const bool active = R < args.row_end;
+    // Rows are taken from the end: each camera's block of rows ends with its
+    // coarsest maps, whose rows hold the most records (a sample lands in
+    // every scale, and a coarse map has few pixels). Taken last to first,
+    // the long rows start early and the launch ends on short rows, not on a
+    // tail of long ones (2 % of the backward at the 6-camera training shape).
+    const int64_t R = args.row_end - 1 - (warp_id * RPW + q);
+    const bool active = R >= args.row_begin;
     const int b = active ? static_cast<int>(pb.div_rows.div(static_cast<uint32_t>(R))) : 0;
     const int jb = active ? (R > 0 ? w.row_off[R - 1] : 0) : 0;
     const int je = active ? w.row_off[R] : 0;
