@@ -96,6 +96,8 @@ def load_library():
     lib.wa_warpaffine_u8.restype = ctypes.c_int
     lib.wa_preprocess.argtypes = [ctypes.POINTER(WaDims), vp, vp, ctypes.c_uint8, vp, vp, vp, vp]
     lib.wa_preprocess.restype = ctypes.c_int
+    lib.da_backward_fused_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
+    lib.da_backward_fused_workspace_size.restype = ctypes.c_int
     lib.da_backward_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
     lib.da_backward_workspace_size.restype = ctypes.c_int
     lib.da_status_string.argtypes = [ctypes.c_int]
@@ -398,8 +400,10 @@ def da_forward_fused(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
 def da_backward_fused(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index, loc_weight: torch.Tensor,
                       grad_out: torch.Tensor, grad_feat: Optional[torch.Tensor] = None,
                       grad_loc_weight: Optional[torch.Tensor] = None,
-                      stream=None) -> Tuple[torch.Tensor, torch.Tensor]:
-    """Backward of the DCNv4 form; returns (grad_feat fp32, grad_loc_weight)."""
+                      stream=None, path: str = "scatter") -> Tuple[torch.Tensor, torch.Tensor]:
+    """Backward of the DCNv4 form; returns (grad_feat fp32, grad_loc_weight).
+    path="binned" takes the gather-form backward (a workspace from torch,
+    reused per stream), path="scatter" the vector-reduction one."""
     lib = load_library()
     ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
     d = _dims_fused(mc_ms_feat, ss, loc_weight)
@@ -414,9 +418,18 @@ def da_backward_fused(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index
         raise ValueError("grad_feat must be float32 with mc_ms_feat's shape")
     if grad_loc_weight.shape != loc_weight.shape or grad_loc_weight.dtype != torch.float32:
         raise ValueError("grad_loc_weight must be float32 with loc_weight's shape")
+    sh = _stream_handle(stream)
+    ws_ptr, ws_bytes = None, 0
+    if path == "binned":
+        n = ctypes.c_size_t(0)
+        _check(lib.da_backward_fused_workspace_size(ctypes.byref(d), ctypes.byref(n)))
+        ws = _workspace(dev, sh, n.value)
+        ws_ptr, ws_bytes = _dptr(ws), ws.numel()
+    elif path != "scatter":
+        raise ValueError("path must be 'binned' or 'scatter'")
     _check(lib.da_backward_fused(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
                                  ls.data_ptr() if ls.numel() else None, _dptr(loc_weight), _dptr(grad_out),
-                                 _dptr(grad_feat), _dptr(grad_loc_weight), None, 0, _stream_handle(stream)))
+                                 _dptr(grad_feat), _dptr(grad_loc_weight), ws_ptr, ws_bytes, sh))
     return grad_feat, grad_loc_weight
 
 

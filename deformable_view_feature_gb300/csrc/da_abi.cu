@@ -104,6 +104,7 @@ da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const
     pb.num_ba = static_cast<int32_t>(num_ba);
     pb.anchors_per_cta = d.num_groups < da::kWarps ? da::kWarps / d.num_groups : 1;
     pb.nmaps = static_cast<int32_t>(nmaps);
+    pb.gsplit = 1;
     pb.div_S = da::FastDiv::make(d.num_scales > 0 ? d.num_scales : 1);
     pb.div_K = da::FastDiv::make(d.num_cams > 0 ? d.num_cams : 1);
     pb.div_G = da::FastDiv::make(d.num_groups);
@@ -286,6 +287,34 @@ da_status prepare_projected(const da_dims *dims, const void *feat, const int32_t
     return DA_OK;
 }
 
+// The binned backward of the fused layout runs on a rewrite of the problem:
+// one group of D channels, A*G anchors (a' = a*G + g) and rows*G virtual
+// rows (pixel row r of group g is virtual row r*G + g, at feat + (r*G + g)*D;
+// anchor a' reads grad_out at a'*D). Every address stays the same.
+da_status fused_binned_problem(const da_dims &d, const da::Problem &pb, da_dims &vd, da::Problem &pv)
+{
+    const int64_t A2 = static_cast<int64_t>(d.num_anchors) * d.num_groups;
+    const int64_t rows2 = d.num_feat_rows * d.num_groups;
+    if (A2 > INT32_MAX || rows2 > INT32_MAX)
+        return fail(DA_ERR_UNSUPPORTED, "binned fused backward: anchors*groups or rows*groups exceeds int32");
+    vd = d;
+    vd.num_anchors = static_cast<int32_t>(A2);
+    vd.num_groups = 1;
+    vd.num_embeds = d.num_embeds / d.num_groups;
+    vd.num_feat_rows = rows2;
+    pv = pb;
+    pv.A = static_cast<int32_t>(A2);
+    pv.G = 1;
+    pv.C = pb.D;
+    pv.rows = rows2;
+    pv.num_ba = static_cast<int32_t>(static_cast<int64_t>(d.batch) * A2);
+    pv.gsplit = d.num_groups;
+    pv.div_A = da::FastDiv::make(A2 > 0 ? static_cast<uint32_t>(A2) : 1);
+    pv.div_G = da::FastDiv::make(1);
+    pv.div_rows = da::FastDiv::make(rows2 > 0 ? static_cast<uint32_t>(rows2) : 1);
+    return DA_OK;
+}
+
 // Device address of g_noalloc_scratch on the current device.
 constexpr int kMaxDevices = 256;
 std::mutex g_noalloc_mu;
@@ -334,6 +363,26 @@ da_status da_backward_workspace_size(const da_dims *dims, size_t *bytes)
         return fail(DA_ERR_SHAPE, "invalid dims");
     da::BinLayout L;
     const da_status st = binned_layout(d, L);
+    if (st != DA_OK) return st;
+    *bytes = L.bytes;
+    return DA_OK;
+}
+
+da_status da_backward_fused_workspace_size(const da_dims *dims, size_t *bytes)
+{
+    if (!dims || !bytes) return fail(DA_ERR_NULL, "dims / bytes is NULL");
+    const da_dims d = *dims;
+    if (d.batch < 0 || d.num_cams < 0 || d.num_scales < 0 || d.num_anchors < 0 || d.num_pts < 0 ||
+        d.num_embeds < 1 || d.num_groups < 1 || d.num_embeds % d.num_groups != 0 || d.num_feat_rows < 0 ||
+        d.num_feat_rows > DA_MAX_ROWS)
+        return fail(DA_ERR_SHAPE, "invalid dims");
+    da::Problem pb{}, pv{};
+    pb.D = d.num_embeds / d.num_groups;
+    da_dims vd;
+    da_status st = fused_binned_problem(d, pb, vd, pv);
+    if (st != DA_OK) return st;
+    da::BinLayout L;
+    st = binned_layout(vd, L);
     if (st != DA_OK) return st;
     *bytes = L.bytes;
     return DA_OK;
@@ -395,10 +444,15 @@ da_status da_backward_fused(const da_dims *dims, const void *mc_ms_feat, const i
     const int64_t n_glw = static_cast<int64_t>(pb.num_ba) * pb.G * pb.pk * (2 + pb.S);
     if (n_glw > 0 && !grad_loc_weight) return fail(DA_ERR_NULL, "grad_loc_weight is NULL");
     if (!aligned(grad_loc_weight, 4)) return fail(DA_ERR_ALIGN, "grad_loc_weight must be 4-byte aligned");
-    if (workspace || workspace_bytes)
-        return fail(DA_ERR_UNSUPPORTED, "the fused layout has the scatter backward only (pass no workspace)");
     a.grad_loc = grad_loc_weight;
     a.grad_weight = nullptr;
+    if (workspace || workspace_bytes) {
+        da_dims vd;
+        da::BwdArgs av = a;
+        const da_status sv = fused_binned_problem(*dims, a.pb, vd, av.pb);
+        if (sv != DA_OK) return sv;
+        return backward_impl(vd, av, chunks, grad_out, grad_feat, workspace, workspace_bytes, 0u, stream);
+    }
     return backward_impl(*dims, a, chunks, grad_out, grad_feat, nullptr, 0, 0u, stream);
 }
 

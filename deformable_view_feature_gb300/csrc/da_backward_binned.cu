@@ -92,6 +92,7 @@ struct BinCta {
     int b, k, q;         // batch item, camera, (a*P + p) of this thread
     bool valid;          // q < A*P
     int64_t pk;          // location id ((b*A + a)*P + p)*K + k
+    int vg;              // a % gsplit: the group of this anchor's virtual rows
 };
 
 __device__ __forceinline__ BinCta bin_cta(const Problem &pb, int ctas_per_view)
@@ -106,7 +107,29 @@ __device__ __forceinline__ BinCta bin_cta(const Problem &pb, int ctas_per_view)
     const int a = c.valid ? static_cast<int>(pb.div_P.div(c.q)) : 0;
     const int p = c.q - a * pb.P;
     c.pk = ((static_cast<int64_t>(c.b) * pb.A + a) * pb.P + p) * pb.K + c.k;
+    c.vg = a % pb.gsplit;
     return c;
+}
+
+// Location (x, y) of location id pk: [.., 2] in the standard layout, the
+// first two of 2 + S entries in the fused one.
+__device__ __forceinline__ float2 bin_xy(const Problem &pb, int64_t pk)
+{
+    if (pb.layout == kLayoutFused) {
+        const float *e = pb.loc + pk * (2 + pb.S);
+        return make_float2(e[0], e[1]);
+    }
+    return *reinterpret_cast<const float2 *>(pb.loc + pk * 2);
+}
+
+// Weight of sample sid (G = 1 in the fused rewrite) for group g.
+__device__ __forceinline__ float bin_weight(const Problem &pb, int sid, int g)
+{
+    if (pb.layout == kLayoutFused) {
+        const int pk = static_cast<int>(pb.div_S.div(sid));
+        return pb.loc[static_cast<int64_t>(pk) * (2 + pb.S) + 2 + (sid - pk * pb.S)];
+    }
+    return pb.weights[static_cast<int64_t>(sid) * pb.G + g];
 }
 
 // Shared-memory offsets of the small maps of camera k (-1: counted globally).
@@ -115,7 +138,7 @@ __device__ __forceinline__ void small_map_offsets(const Problem &pb, const MapIn
 {
     int off = 0;
     for (int s = 0; s < pb.S; ++s) {
-        const int n = maps_s[k * pb.S + s].H * maps_s[k * pb.S + s].W;
+        const int n = maps_s[k * pb.S + s].H * maps_s[k * pb.S + s].W * pb.gsplit;
         if (off + n <= kBinSmemRows) {
             hoff[s] = off;
             off += n;
@@ -134,9 +157,10 @@ __device__ __forceinline__ void flush_small_counts(const Problem &pb, const MapI
     for (int s = 0; s < pb.S; ++s) {
         if (hoff[s] < 0) continue;
         const MapInfo m = maps_s[k * pb.S + s];
-        for (int r = threadIdx.x; r < m.H * m.W; r += kBinThreads) {
+        const int n = m.H * m.W * pb.gsplit;
+        for (int r = threadIdx.x; r < n; r += kBinThreads) {
             const int v = hist[hoff[s] + r];
-            if (v) atomicAdd(row_base + m.start + r, v);
+            if (v) atomicAdd(row_base + m.start * pb.gsplit + r, v);
         }
     }
 }
@@ -156,8 +180,9 @@ __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb
     for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
     __syncthreads();
     int32_t *cnt = w.row_off + static_cast<int64_t>(c.b) * pb.rows;
+    const int gs = pb.gsplit;
     if (c.valid) {
-        const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + c.pk * 2);
+        const float2 xy = bin_xy(pb, c.pk);
         for (int s = 0; s < pb.S; ++s) {
             const MapInfo m = maps_s[c.k * pb.S + s];
             Footprint f;
@@ -166,8 +191,8 @@ __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 if (f.row[cc] < 0) continue;
-                if (ho >= 0) atomicAdd(&hist[ho + f.row[cc] - m.start], 1);
-                else atomicAdd(cnt + f.row[cc], 1);
+                if (ho >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + c.vg], 1);
+                else atomicAdd(cnt + f.row[cc] * gs + c.vg, 1);
             }
         }
     }
@@ -270,8 +295,9 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
     for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
     __syncthreads();
     float2 xy = make_float2(0.f, 0.f);
+    const int gs = pb.gsplit;
     if (c.valid) {
-        xy = *reinterpret_cast<const float2 *>(pb.loc + c.pk * 2);
+        xy = bin_xy(pb, c.pk);
         for (int s = 0; s < pb.S; ++s) {
             const int ho = hoff[s];
             if (ho < 0) continue;
@@ -280,7 +306,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
             footprint(xy.x, xy.y, m, f);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
-                if (f.row[cc] >= 0) atomicAdd(&hist[ho + f.row[cc] - m.start], 1);
+                if (f.row[cc] >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + c.vg], 1);
         }
     }
     __syncthreads();
@@ -289,9 +315,10 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
     for (int s = 0; s < pb.S; ++s) {
         if (hoff[s] < 0) continue;
         const MapInfo m = maps_s[c.k * pb.S + s];
-        for (int r = threadIdx.x; r < m.H * m.W; r += kBinThreads) {
+        const int n = m.H * m.W * gs;
+        for (int r = threadIdx.x; r < n; r += kBinThreads) {
             const int v = hist[hoff[s] + r];
-            if (v) hist[hoff[s] + r] = atomicAdd(cursor + m.start + r, v);
+            if (v) hist[hoff[s] + r] = atomicAdd(cursor + m.start * gs + r, v);
         }
     }
     __syncthreads();
@@ -308,7 +335,8 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
         for (int cc = 0; cc < 4; ++cc) {
             pos[cc] = -1;
             if (f.row[cc] >= 0)
-                pos[cc] = ho >= 0 ? atomicAdd(&hist[ho + f.row[cc] - m.start], 1) : atomicAdd(cursor + f.row[cc], 1);
+                pos[cc] = ho >= 0 ? atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + c.vg], 1)
+                                  : atomicAdd(cursor + f.row[cc] * gs + c.vg, 1);
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -656,7 +684,7 @@ __global__ void __launch_bounds__(kPullThreads) pull_kernel(const PullArgs args)
             const int sid = r[u].x >> 2;
             const int a = static_cast<int>(pb.div_PKS.div(sid)) - abase;
             const bool valid = k0 + u < n;
-            const float wt = valid ? __ldg(&pb.weights[static_cast<int64_t>(sid) * pb.G + g]) : 0.f;
+            const float wt = valid ? bin_weight(pb, sid, g) : 0.f;
             tw[u] = __int_as_float(r[u].y) * wt;
             gp[u] = go_b + static_cast<int64_t>(valid ? a : 0) * pb.C;
         }
@@ -739,6 +767,47 @@ __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const B
         grad_loc[pk64 * 2] = gx;
         grad_loc[pk64 * 2 + 1] = gy;
     }
+}
+
+// The fused layout's rewrite (G = 1): a location has S samples of one group,
+// too few for a warp, so one thread takes a location. The gradients go to
+// grad_loc_weight [.., 2 + S]: (dL/dx, dL/dy, dL/dw_0 .. dL/dw_{S-1}).
+__global__ void __launch_bounds__(256) epilogue_fused_kernel(const Problem pb, const BinArgs w, float *glw,
+                                                             int64_t npk)
+{
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    stage_maps(pb, maps_s);
+    __syncthreads();
+    const int64_t pk64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (pk64 >= npk) return;
+    const int pk = static_cast<int>(pk64);
+    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
+    const int k = pk - bap * pb.K;
+    const int bq = static_cast<int>(pb.div_P.div(bap));  // b*A + a
+    const int b = static_cast<int>(pb.div_A.div(bq));
+    const int q = bap - b * pb.A * pb.P;  // a*P + p
+    const int64_t vsid0 = ((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * pb.S;
+    const int E = 2 + pb.S;
+    float *e = glw + pk64 * E;
+    const float *le = pb.loc + pk64 * E;
+    const float x = le[0], y = le[1];
+    float gx = 0.f, gy = 0.f;
+    for (int s = 0; s < pb.S; ++s) {
+        const MapInfo m = maps_s[k * pb.S + s];
+        Footprint f;
+        footprint(x, y, m, f);
+        const float wt = le[2 + s];
+        const int4 pos = reinterpret_cast<const int4 *>(w.pos4)[vsid0 + s];
+        const float d0 = pos.x >= 0 ? w.dpix[pos.x] : 0.f;
+        const float d1 = pos.y >= 0 ? w.dpix[pos.y] : 0.f;
+        const float d2 = pos.z >= 0 ? w.dpix[pos.z] : 0.f;
+        const float d3 = pos.w >= 0 ? w.dpix[pos.w] : 0.f;
+        e[2 + s] = f.cw[0] * d0 + f.cw[1] * d1 + f.cw[2] * d2 + f.cw[3] * d3;
+        gx += static_cast<float>(m.W) * wt * (f.lh * (d3 - d2) + f.hh * (d1 - d0));
+        gy += static_cast<float>(m.H) * wt * (f.lw * (d3 - d1) + f.hw * (d2 - d0));
+    }
+    e[0] = gx;
+    e[1] = gy;
 }
 
 // ---------------------------------------------------------------- launch
@@ -842,7 +911,10 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
         if (e != cudaSuccess) return e;
     }
     // 5. grad_weight and grad_loc
-    if (npk > 0) {
+    if (npk > 0 && pb.layout == kLayoutFused) {
+        epilogue_fused_kernel<<<static_cast<unsigned>((npk + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc, npk);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    } else if (npk > 0) {
         epilogue_kernel<<<static_cast<unsigned>((npk * 32 + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc,
                                                                                          a.grad_weight, 0, npk);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;

@@ -66,6 +66,11 @@ struct Problem {
     int32_t anchors_per_cta;  // anchors (or views) owned by one CTA, all groups
     int32_t nmaps;            // K*S
     int32_t layout;           // kLayoutStd, kLayoutFused or kLayoutProj
+    // Binned backward of the fused layout: the problem is rewritten with one
+    // group (G = 1, C = D), A*G anchors (a' = a*G + g) and rows*G virtual
+    // rows; pixel row r of group g is virtual row r*gsplit + g, whose D
+    // channels sit at feat + (virtual row)*D. gsplit is 1 otherwise.
+    int32_t gsplit;
     FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS, div_rows;
     MapInfo maps[DA_MAX_MAPS];
 };

@@ -230,13 +230,20 @@ da_status da_backward_ex(const da_dims *dims,
  * da_forward_fused: arguments and rules of da_forward, with loc_weight in
  * place of sampling_location and weights.
  *
- * da_backward_fused: arguments and rules of da_backward's scatter path, with
+ * da_backward_fused: arguments and rules of da_backward, with
  * grad_loc_weight [B, A, G, P, K, 2 + S] fp32 (4-byte aligned, overwritten)
  * in place of grad_loc and grad_weight: entries 0, 1 hold dL/dx, dL/dy
  * (scaled by W and H, summed over the scales and the group's channels) and
- * entry 2 + s holds dL/dw_s. The binned path does not serve this layout:
- * workspace must be NULL and workspace_bytes 0 (else DA_ERR_UNSUPPORTED).
+ * entry 2 + s holds dL/dw_s. With a workspace of at least
+ * da_backward_fused_workspace_size bytes it takes the binned path, which
+ * treats the D channels of each (pixel, group) as a row of their own and
+ * each (anchor, group) as an anchor; it needs D a power of two in [8, 256]
+ * (else DA_ERR_UNSUPPORTED). Without one, the scatter path.
+ *
+ * da_backward_fused_workspace_size: the binned path's workspace for dims,
+ * about 4*B*A*G*P*K*S*16.5 bytes plus 4*G bytes per feature row.
  */
+da_status da_backward_fused_workspace_size(const da_dims *dims, size_t *bytes);
 da_status da_forward_fused(const da_dims *dims,
                            const void *mc_ms_feat,
                            const int32_t *spatial_shape,

@@ -270,3 +270,18 @@ def test_warpaffine_validation_without_gpu(lib):
     assert bl.wa_preprocess(ctypes.byref(ok), FAKE, FAKE, 0, mean, mean, FAKE + 2, None) == DA_ERR_ALIGN
     empty = da.WaDims(0, 4, 4, 2, 2)
     assert bl.wa_warpaffine_u8(ctypes.byref(empty), None, None, 0, None, None) == DA_OK
+
+
+def test_fused_workspace_size(lib):
+    bl = da.load_library()
+    n = ctypes.c_size_t(0)
+    # The DCNv4 page's benchmark: B=64, one 56x56 map, C=128, G=4, 3136 anchors, 9 points.
+    d = _dims(batch=64, num_cams=1, num_scales=1, num_embeds=128, num_groups=4, num_anchors=3136, num_pts=9,
+              num_feat_rows=3136)
+    assert bl.da_backward_fused_workspace_size(ctypes.byref(d), ctypes.byref(n)) == DA_OK
+    nsid = 64 * 3136 * 4 * 9  # samples of the rewrite: one per (anchor, group, point)
+    ncap = 4 * nsid
+    base = ncap * (8 + 4 + 4) + 4 * (ncap // 9 + ncap // 129 + ncap // 2049 + 3)
+    assert base <= n.value < base + 4 * 64 * 3136 * 4 + (8 << 20)
+    bad = _dims(num_embeds=48, num_groups=4)  # D = 12: not a power of two
+    assert bl.da_backward_fused_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == DA_ERR_UNSUPPORTED

@@ -29,11 +29,17 @@ def da():
     return m
 
 
-def _run(da, inp):
+def _binned_ok(inp):
+    """The binned path serves D = C/G a power of two in [8, 256]."""
+    D = inp.wl.num_embeds // inp.wl.num_groups
+    return 8 <= D <= 256 and D & (D - 1) == 0
+
+
+def _run(da, inp, path="scatter"):
     dev = torch.device("cuda")
     feat, lw, go = inp.feat.to(dev), inp.loc_weight.to(dev), inp.grad_out.to(dev)
     out = da.da_forward_fused(feat, inp.spatial_shape, inp.level_start_index, lw)
-    gf, glw = da.da_backward_fused(feat, inp.spatial_shape, inp.level_start_index, lw, go)
+    gf, glw = da.da_backward_fused(feat, inp.spatial_shape, inp.level_start_index, lw, go, path=path)
     torch.cuda.synchronize()
     return {"out": to_np(out), "grad_feat": to_np(gf), "grad_loc_weight": to_np(glw)}
 
@@ -81,25 +87,36 @@ def _check(inp, got):
     assert not msgs, f"{inp.wl.name}: " + " | ".join(msgs)
 
 
+PATHS = ("scatter", "binned")
+
+
+@pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
-def test_dcnv4_full_size(da, dtype):
+def test_dcnv4_full_size(da, dtype, path):
     wl = da_inputs.WORKLOADS["dcnv4"].replace(feat_dtype=dtype)
     inp = da_inputs.make_fused_inputs(wl)
-    _check(inp, _run(da, inp))
+    _check(inp, _run(da, inp, path))
 
 
-def test_sparse4d_shape_per_group_points(da):
+@pytest.mark.parametrize("path", PATHS)
+def test_sparse4d_shape_per_group_points(da, path):
     inp = da_inputs.make_fused_inputs(da_inputs.small_variant("sp4d_train", batch=2, num_anchors=30))
-    _check(inp, _run(da, inp))
+    _check(inp, _run(da, inp, path))
 
 
-@pytest.mark.parametrize("C,G,dtype", [(24, 3, "f32"), (64, 16, "f32"), (128, 2, "f16"), (32, 4, "bf16")])
-def test_ragged_shapes(da, C, G, dtype):
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("C,G,dtype", [(24, 3, "f32"), (64, 16, "f32"), (128, 2, "f16"), (32, 4, "bf16"),
+                                       (64, 4, "f32")])
+def test_ragged_shapes(da, C, G, dtype, path):
     wl = da_inputs.WORKLOADS["tiny"].replace(name=f"tiny_c{C}g{G}", num_embeds=C, num_groups=G, batch=2,
                                              num_anchors=13, num_pts=5, shapes=((9, 7), (3, 4)),
                                              num_cams=2, feat_dtype=dtype)
     inp = da_inputs.make_fused_inputs(wl, seed=7)
-    _check(inp, _run(da, inp))
+    if path == "binned" and not _binned_ok(inp):
+        with pytest.raises(da.DaError, match="DA_ERR_UNSUPPORTED"):
+            _run(da, inp, path)
+        return
+    _check(inp, _run(da, inp, path))
 
 
 def test_shared_points_match_standard_forward_bits(da):
@@ -117,20 +134,24 @@ def test_shared_points_match_standard_forward_bits(da):
     assert torch.equal(a, b)
 
 
-def test_empty_and_workspace_refused(da):
+@pytest.mark.parametrize("path", PATHS)
+def test_empty_batch(da, path):
     wl = da_inputs.WORKLOADS["tiny"].replace(name="tiny_b0", batch=0)
     inp = da_inputs.make_fused_inputs(wl)
-    got = _run(da, inp)
+    got = _run(da, inp, path)
     assert all(v.size == 0 for v in got.values())
+
+
+def test_binned_workspace_too_small_refused(da):
+    import ctypes
     inp = da_inputs.make_fused_inputs(da_inputs.WORKLOADS["tiny"])
     dev = torch.device("cuda")
     lib = da.load_library()
     d = da._dims_fused(inp.feat, da._host_i32(inp.spatial_shape), inp.loc_weight)
     feat, lw, go = inp.feat.to(dev), inp.loc_weight.to(dev), inp.grad_out.to(dev)
     gf, glw = torch.empty_like(feat), torch.empty_like(lw)
-    ws = torch.empty(1 << 20, dtype=torch.uint8, device=dev)
+    ws = torch.empty(4096, dtype=torch.uint8, device=dev)
     ss, ls = da._host_i32(inp.spatial_shape), da._host_i32(inp.level_start_index)
-    import ctypes
     st = lib.da_backward_fused(ctypes.byref(d), feat.data_ptr(), ss.data_ptr(), ls.data_ptr(), lw.data_ptr(),
                                go.data_ptr(), gf.data_ptr(), glw.data_ptr(), ws.data_ptr(), ws.numel(), None)
-    assert st == 4  # DA_ERR_UNSUPPORTED
+    assert st == 6  # DA_ERR_WORKSPACE
