@@ -439,6 +439,9 @@ def run_fused(a, wl):
     stream = torch.cuda.Stream(device=dev)
     fwd_bytes = tensor_bytes(feat, lw) + out.numel() * 4
     bwd_bytes = tensor_bytes(feat, lw, go) + 2 * gf.numel() * 4 + glw.numel() * 4
+    # Default scatter: the binned rewrite measured slower on the DCNv4 shapes
+    # (its 56x56 maps times 4 groups exceed the shared-memory binning).
+    bwd_path = a.bwd_path if a.bwd_path in ("binned", "scatter") else "scatter"
 
     def step(ev=None):
         if ev is not None:
@@ -447,7 +450,8 @@ def run_fused(a, wl):
         if ev is not None:
             ev[1].record(stream)
         if wl.backward:
-            da.da_backward_fused(feat, ss, ls, lw, go, grad_feat=gf, grad_loc_weight=glw, stream=stream)
+            da.da_backward_fused(feat, ss, ls, lw, go, grad_feat=gf, grad_loc_weight=glw, stream=stream,
+                                 path=bwd_path)
             if ev is not None:
                 ev[2].record(stream)
 
@@ -473,7 +477,7 @@ def run_fused(a, wl):
     fwd_ms = statistics.mean(evs[i][0].elapsed_time(evs[i][1]) for i in range(a.steps))
     bwd_ms = statistics.mean(evs[i][1].elapsed_time(evs[i][2]) for i in range(a.steps)) if wl.backward else None
     peak, peak_kind = peaks()
-    dom_ms, dom_bytes, dom = (bwd_ms, bwd_bytes, "da_backward_fused") if wl.backward else \
+    dom_ms, dom_bytes, dom = (bwd_ms, bwd_bytes, f"da_backward_fused ({bwd_path} path)") if wl.backward else \
         (fwd_ms, fwd_bytes, "da_forward_fused")
     achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     line = {
@@ -494,7 +498,8 @@ def run_fused(a, wl):
                                  "(another machine; context, not a target)",
                          "a100_kernel_ms": {"f32": 0.606, "f16": 0.404}.get(wl.feat_dtype),
                          "ours_fwd_ms": fwd_ms} if wl.name.startswith("dcnv4_table10") else None,
-        "gpu_launches": a.steps * (1 + (2 if wl.backward else 0)),
+        "gpu_launches": a.steps * (1 + ((BWD_LAUNCHES[bwd_path]) if wl.backward else 0)),
+        "bwd_path": bwd_path,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
     print(json.dumps(line), flush=True)
@@ -643,12 +648,14 @@ def main():
                          "warpaffine: the frame preprocessing")
     ap.add_argument("--feat-dtype", choices=["f32", "bf16", "f16"], default=None,
                     help="override the workload's feature type (--op fused)")
-    ap.add_argument("--bwd-path", choices=["binned", "binned-det", "scatter"], default="binned",
+    ap.add_argument("--bwd-path", choices=["binned", "binned-det", "scatter"], default=None,
                     help="backward algorithm (binned needs a device workspace; binned-det is its "
-                         "deterministic mode)")
+                         "deterministic mode). Default: binned for --op da, scatter for --op fused")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if a.bwd_path is None and a.op == "da":
+        a.bwd_path = "binned"
     if a.op in ("projected", "warpaffine"):
         if a.impl == "reference" or a.gpus != 1:
             ap.error(f"--op {a.op} runs our implementation on one GPU")
