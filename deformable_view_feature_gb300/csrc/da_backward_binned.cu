@@ -107,15 +107,16 @@ __device__ __forceinline__ BinCta bin_cta(const Problem &pb, int ctas_per_view)
     const int a = c.valid ? static_cast<int>(pb.div_P.div(c.q)) : 0;
     const int p = c.q - a * pb.P;
     c.pk = ((static_cast<int64_t>(c.b) * pb.A + a) * pb.P + p) * pb.K + c.k;
-    c.vg = a % pb.gsplit;
+    c.vg = pb.gsplit > 1 ? a % pb.gsplit : 0;
     return c;
 }
 
 // Location (x, y) of location id pk: [.., 2] in the standard layout, the
 // first two of 2 + S entries in the fused one.
+template <bool FUSED>
 __device__ __forceinline__ float2 bin_xy(const Problem &pb, int64_t pk)
 {
-    if (pb.layout == kLayoutFused) {
+    if constexpr (FUSED) {
         const float *e = pb.loc + pk * (2 + pb.S);
         return make_float2(e[0], e[1]);
     }
@@ -123,22 +124,23 @@ __device__ __forceinline__ float2 bin_xy(const Problem &pb, int64_t pk)
 }
 
 // Weight of sample sid (G = 1 in the fused rewrite) for group g.
+template <bool FUSED>
 __device__ __forceinline__ float bin_weight(const Problem &pb, int sid, int g)
 {
-    if (pb.layout == kLayoutFused) {
+    if constexpr (FUSED) {
         const int pk = static_cast<int>(pb.div_S.div(sid));
-        return pb.loc[static_cast<int64_t>(pk) * (2 + pb.S) + 2 + (sid - pk * pb.S)];
+        return __ldg(&pb.loc[static_cast<int64_t>(pk) * (2 + pb.S) + 2 + (sid - pk * pb.S)]);
     }
-    return pb.weights[static_cast<int64_t>(sid) * pb.G + g];
+    return __ldg(&pb.weights[static_cast<int64_t>(sid) * pb.G + g]);
 }
 
 // Shared-memory offsets of the small maps of camera k (-1: counted globally).
 __device__ __forceinline__ void small_map_offsets(const Problem &pb, const MapInfo *maps_s, int k, int *hoff,
-                                                  int &nsmall)
+                                                  int &nsmall, int gs)
 {
     int off = 0;
     for (int s = 0; s < pb.S; ++s) {
-        const int n = maps_s[k * pb.S + s].H * maps_s[k * pb.S + s].W * pb.gsplit;
+        const int n = maps_s[k * pb.S + s].H * maps_s[k * pb.S + s].W * gs;
         if (off + n <= kBinSmemRows) {
             hoff[s] = off;
             off += n;
@@ -152,19 +154,20 @@ __device__ __forceinline__ void small_map_offsets(const Problem &pb, const MapIn
 // Adds the shared counts of the small maps into row_off: one global atomic
 // per touched row. Needs a __syncthreads() before it.
 __device__ __forceinline__ void flush_small_counts(const Problem &pb, const MapInfo *maps_s, const int *hoff,
-                                                   int k, const int *hist, int32_t *row_base)
+                                                   int k, const int *hist, int32_t *row_base, int gs)
 {
     for (int s = 0; s < pb.S; ++s) {
         if (hoff[s] < 0) continue;
         const MapInfo m = maps_s[k * pb.S + s];
-        const int n = m.H * m.W * pb.gsplit;
+        const int n = m.H * m.W * gs;
         for (int r = threadIdx.x; r < n; r += kBinThreads) {
             const int v = hist[hoff[s] + r];
-            if (v) atomicAdd(row_base + m.start * pb.gsplit + r, v);
+            if (v) atomicAdd(row_base + m.start * gs + r, v);
         }
     }
 }
 
+template <bool FUSED>
 __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb, const BinArgs w,
                                                                  int ctas_per_view)
 {
@@ -175,14 +178,16 @@ __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb
     stage_maps(pb, maps_s);
     const BinCta c = bin_cta(pb, ctas_per_view);
     __syncthreads();
-    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s);
+    // Virtual rows per pixel row: gsplit in the fused rewrite, else 1.
+    const int gs = FUSED ? pb.gsplit : 1;
+    const int vg = FUSED ? c.vg : 0;
+    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s, gs);
     __syncthreads();
     for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
     __syncthreads();
     int32_t *cnt = w.row_off + static_cast<int64_t>(c.b) * pb.rows;
-    const int gs = pb.gsplit;
     if (c.valid) {
-        const float2 xy = bin_xy(pb, c.pk);
+        const float2 xy = bin_xy<FUSED>(pb, c.pk);
         for (int s = 0; s < pb.S; ++s) {
             const MapInfo m = maps_s[c.k * pb.S + s];
             Footprint f;
@@ -191,13 +196,13 @@ __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 if (f.row[cc] < 0) continue;
-                if (ho >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + c.vg], 1);
-                else atomicAdd(cnt + f.row[cc] * gs + c.vg, 1);
+                if (ho >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + vg], 1);
+                else atomicAdd(cnt + f.row[cc] * gs + vg, 1);
             }
         }
     }
     __syncthreads();
-    flush_small_counts(pb, maps_s, hoff, c.k, hist, cnt);
+    flush_small_counts(pb, maps_s, hoff, c.k, hist, cnt, gs);
 }
 
 // ---------------------------------------------------------------- 2. scan
@@ -280,6 +285,7 @@ __global__ void __launch_bounds__(256) scan_add_kernel(int32_t *data, const int3
 // global atomic, and then hands out slots inside the range with shared
 // atomics. Every corner of a large map claims its slot with a global atomic.
 // pos4 is stored view-major: index ((b*K + k)*A*P + a*P + p)*S + s.
+template <bool FUSED>
 __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb, const BinArgs w,
                                                                 int ctas_per_view)
 {
@@ -290,14 +296,16 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
     stage_maps(pb, maps_s);
     const BinCta c = bin_cta(pb, ctas_per_view);
     __syncthreads();
-    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s);
+    // Virtual rows per pixel row: gsplit in the fused rewrite, else 1.
+    const int gs = FUSED ? pb.gsplit : 1;
+    const int vg = FUSED ? c.vg : 0;
+    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s, gs);
     __syncthreads();
     for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
     __syncthreads();
     float2 xy = make_float2(0.f, 0.f);
-    const int gs = pb.gsplit;
     if (c.valid) {
-        xy = bin_xy(pb, c.pk);
+        xy = bin_xy<FUSED>(pb, c.pk);
         for (int s = 0; s < pb.S; ++s) {
             const int ho = hoff[s];
             if (ho < 0) continue;
@@ -306,7 +314,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
             footprint(xy.x, xy.y, m, f);
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc)
-                if (f.row[cc] >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + c.vg], 1);
+                if (f.row[cc] >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + vg], 1);
         }
     }
     __syncthreads();
@@ -335,8 +343,8 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
         for (int cc = 0; cc < 4; ++cc) {
             pos[cc] = -1;
             if (f.row[cc] >= 0)
-                pos[cc] = ho >= 0 ? atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + c.vg], 1)
-                                  : atomicAdd(cursor + f.row[cc] * gs + c.vg, 1);
+                pos[cc] = ho >= 0 ? atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + vg], 1)
+                                  : atomicAdd(cursor + f.row[cc] * gs + vg, 1);
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
@@ -627,7 +635,7 @@ __device__ __forceinline__ float record_fma(const float (&v)[8], const float4 x,
 // LPR = C/8 lanes own one feature row, 8 channels each, all groups; a warp
 // holds 32/LPR rows. LPG = D/8 lanes hold one group. Records are taken four
 // at a time, so the loads of the four are independent and issue together.
-template <typename T, int LPR, int LPG>
+template <typename T, int LPR, int LPG, bool FUSED>
 __global__ void __launch_bounds__(kPullThreads) pull_kernel(const PullArgs args)
 {
     constexpr int RPW = 32 / LPR;
@@ -684,7 +692,7 @@ __global__ void __launch_bounds__(kPullThreads) pull_kernel(const PullArgs args)
             const int sid = r[u].x >> 2;
             const int a = static_cast<int>(pb.div_PKS.div(sid)) - abase;
             const bool valid = k0 + u < n;
-            const float wt = valid ? bin_weight(pb, sid, g) : 0.f;
+            const float wt = valid ? bin_weight<FUSED>(pb, sid, g) : 0.f;
             tw[u] = __int_as_float(r[u].y) * wt;
             gp[u] = go_b + static_cast<int64_t>(valid ? a : 0) * pb.C;
         }
@@ -822,7 +830,10 @@ cudaError_t launch_pull(const PullArgs &pa, cudaStream_t st)
         const int64_t warps = (pa.row_end - pa.row_begin + RPW - 1) / RPW;
         const int64_t grid = (warps + kPullThreads / 32 - 1) / (kPullThreads / 32);
         if (grid == 0) return cudaSuccess;
-        pull_kernel<T, LPR, LPG><<<static_cast<unsigned>(grid), kPullThreads, 0, st>>>(pa);
+        if (pa.pb.layout == kLayoutFused)
+            pull_kernel<T, LPR, LPG, true><<<static_cast<unsigned>(grid), kPullThreads, 0, st>>>(pa);
+        else
+            pull_kernel<T, LPR, LPG, false><<<static_cast<unsigned>(grid), kPullThreads, 0, st>>>(pa);
         return cudaGetLastError();
     }
 }
@@ -868,7 +879,10 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     const int ctas_per_view = (pb.A * pb.P + kBinThreads - 1) / kBinThreads;
     const int64_t bin_grid = static_cast<int64_t>(pb.B) * pb.K * ctas_per_view;
     if (w.nsid > 0) {
-        bin_count_kernel<<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+        if (pb.layout == kLayoutFused)
+            bin_count_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+        else
+            bin_count_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 2. offsets
@@ -883,7 +897,10 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     }
     // 3. records
     if (w.nsid > 0) {
-        bin_fill_kernel<<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+        if (pb.layout == kLayoutFused)
+            bin_fill_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+        else
+            bin_fill_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 3b. deterministic order inside every row
