@@ -39,10 +39,7 @@
 namespace da {
 namespace {
 
-// Anchor of a task within its CTA.
-__device__ __forceinline__ int tq_of(int task, const Problem &pb) { return static_cast<int>(pb.div_G.div(task)); }
-
-template <typename T, int CH, int LAYOUT>
+template <typename T, int CH, bool FUSED>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 {
     using Ck = Chunk<T>;
@@ -55,10 +52,121 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 
     __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
-    // Projected layout only (dynamic): the CTA's projected locations
-    // [anchors_per_cta][P*K], then per warp the softmax numerators of its
-    // task's P*K*S samples.
-    extern __shared__ float2 proj_s[];
+    stage_maps(pb, maps_s);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int chunk = lane % CH;
+    const int corner = (lane / CH) & 3;
+    const int slot = lane / (4 * CH);
+
+    const int ba0 = static_cast<int>(blockIdx.x) * pb.anchors_per_cta;
+    const int na = min(pb.anchors_per_cta, pb.num_ba - ba0);
+    const int ntask = na * pb.G;
+    const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
+
+    for (int task = warp; task < ntask; task += kWarps) {
+        const int tq = static_cast<int>(pb.div_G.div(task));
+        const int g = task - tq * pb.G;
+        const int ba = ba0 + tq;
+        const int b = static_cast<int>(pb.div_A.div(ba));
+        const char *base = static_cast<const char *>(pb.feat) +
+                           (static_cast<int64_t>(b) * pb.rows * pb.C + static_cast<int64_t>(g) * pb.D) * ESZ +
+                           chunk * 16;
+        float acc[VEC];
+#pragma unroll
+        for (int v = 0; v < VEC; ++v) acc[v] = 0.f;
+
+        for (int j0 = 0; j0 < pb.pks; j0 += 32) {
+            const int n = min(32, pb.pks - j0);
+            {
+                int row[4] = {-1, -1, -1, -1};
+                float tw[4] = {0.f, 0.f, 0.f, 0.f};
+                if (lane < n) {
+                    const int j = j0 + lane;
+                    const int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k
+                    const int s = j - jk * pb.S;
+                    const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
+                    float2 xy;
+                    float w;
+                    sample_xyw<FUSED>(pb, ba, g, jk, s, xy, w);
+                    Footprint f;
+                    footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        row[c] = f.row[c];
+                        tw[c] = w * f.cw[c];
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tab[warp][c][lane] = make_int2(row[c], __float_as_int(tw[c]));
+            }
+            __syncwarp();
+
+            for (int i0 = 0; i0 < n; i0 += U * SPP) {
+                const int i = i0 + U * slot;
+                int r[U];
+                float cw[U];
+#pragma unroll
+                for (int h = 0; h < U / 2; ++h) {
+                    const int4 e = *reinterpret_cast<const int4 *>(&tab[warp][corner][i + 2 * h]);
+                    r[2 * h] = e.x;
+                    cw[2 * h] = __int_as_float(e.y);
+                    r[2 * h + 1] = e.z;
+                    cw[2 * h + 1] = __int_as_float(e.w);
+                }
+                uint4 raw[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    float v[VEC];
+                    Ck::unpack(raw[u], v);
+#pragma unroll
+                    for (int q = 0; q < VEC; ++q) acc[q] = fmaf(cw[u], v[q], acc[q]);
+                }
+            }
+            __syncwarp();
+        }
+
+        // Sum the corner and slot partials: lanes that differ only above the
+        // chunk bits hold the same channels.
+#pragma unroll
+        for (int m = CH; m < 32; m <<= 1) {
+#pragma unroll
+            for (int q = 0; q < VEC; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], m);
+        }
+        if (lane < CH) {
+            float4 *o = reinterpret_cast<float4 *>(args.out + static_cast<int64_t>(ba) * pb.C +
+                                                   static_cast<int64_t>(g) * pb.D + chunk * VEC);
+#pragma unroll
+            for (int q = 0; q < VEC / 4; ++q)
+                o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+        }
+    }
+}
+
+// Anchor of a task within its CTA.
+__device__ __forceinline__ int tq_of(int task, const Problem &pb) { return static_cast<int>(pb.div_G.div(task)); }
+
+// The projected layout's kernel: fwd_kernel's decomposition, with the
+// projection and the softmax in front. (Kept apart from fwd_kernel: folding
+// it into that template as a compile-time branch slowed the standard
+// instance by 6 % at the 6-camera training shape.)
+template <typename T, int CH>
+__global__ void __launch_bounds__(kThreads) fwd_proj_kernel(const FwdArgs args)
+{
+    using Ck = Chunk<T>;
+    constexpr int VEC = Ck::kVec;   // channels per 16-byte chunk
+    constexpr int ESZ = 16 / VEC;   // bytes per feature element
+    constexpr int SPP = 8 / CH;     // samples per warp-wide load
+    // Samples per lane per step; a warp-wide step covers U * SPP <= 32.
+    constexpr int U = DA_FWD_UNROLL * SPP <= 32 ? DA_FWD_UNROLL : 32 / SPP;
+    const Problem &pb = args.pb;
+
+    __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
 
     const int warp = threadIdx.x >> 5;
@@ -71,8 +179,12 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     const int na = min(pb.anchors_per_cta, pb.num_ba - ba0);
     const int ntask = na * pb.G;
     const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
-    float *ebuf = nullptr;
-    if constexpr (LAYOUT == kLayoutProj) {
+    // Dynamic shared memory: the CTA's projected locations
+    // [anchors_per_cta][P*K], then per warp the softmax numerators of its
+    // task's P*K*S samples.
+    extern __shared__ float2 proj_s[];
+    float *const ebuf = reinterpret_cast<float *>(proj_s + pb.anchors_per_cta * pb.pk) + warp * pb.pks;
+    {
         // Each (anchor, point, camera) is projected once for all G groups.
         for (int i = threadIdx.x; i < na * pb.pk; i += kThreads) {
             const int tq = i / pb.pk;
@@ -91,7 +203,6 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                 o[1] = xy.y;
             }
         }
-        ebuf = reinterpret_cast<float *>(proj_s + pb.anchors_per_cta * pb.pk) + warp * pb.pks;
     }
     __syncthreads();
 
@@ -110,7 +221,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
         // Projected layout: the softmax over the task's samples. The
         // numerators exp(z - max) go to the warp's buffer; 1/sum scales them.
         float inv_sum = 1.f;
-        if constexpr (LAYOUT == kLayoutProj) {
+        {
             const float *z = pb.logits + static_cast<int64_t>(ba) * pb.pks * pb.G + g;
             float m = -INFINITY;
             for (int j = lane; j < pb.pks; j += 32) m = fmaxf(m, z[static_cast<int64_t>(j) * pb.G]);
@@ -140,14 +251,10 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                     const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
                     float2 xy;
                     float w;
-                    if constexpr (LAYOUT == kLayoutProj) {
-                        xy = proj_s[tq_of(task, pb) * pb.pk + jk];
-                        w = ebuf[j] * inv_sum;
-                        if (args.weights_out)
-                            args.weights_out[((static_cast<int64_t>(ba) * pb.pk + jk) * pb.S + s) * pb.G + g] = w;
-                    } else {
-                        sample_xyw<LAYOUT>(pb, ba, g, jk, s, xy, w);
-                    }
+                    xy = proj_s[tq_of(task, pb) * pb.pk + jk];
+                    w = ebuf[j] * inv_sum;
+                    if (args.weights_out)
+                        args.weights_out[((static_cast<int64_t>(ba) * pb.pk + jk) * pb.S + s) * pb.G + g] = w;
                     Footprint f;
                     footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
 #pragma unroll
@@ -263,7 +370,7 @@ __global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args,
                 const int k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
                 float2 xy;
                 float w;
-                sample_xyw<FUSED ? kLayoutFused : kLayoutStd>(pb, it_ba, it_g, jk, s, xy, w);
+                sample_xyw<FUSED>(pb, it_ba, it_g, jk, s, xy, w);
                 Footprint f;
                 footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
 #pragma unroll
@@ -339,19 +446,19 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
     const int64_t grid = sampling_grid(a.pb);
     if (grid == 0) return cudaSuccess;
     switch (a.pb.layout) {
-        case kLayoutFused: fwd_kernel<T, CH, kLayoutFused><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
+        case kLayoutFused: fwd_kernel<T, CH, true><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
         case kLayoutProj: {
             const size_t smem = projected_smem_bytes(a.pb);
             if (smem > 48 * 1024) {
-                const cudaError_t e = cudaFuncSetAttribute(fwd_kernel<T, CH, kLayoutProj>,
+                const cudaError_t e = cudaFuncSetAttribute(fwd_proj_kernel<T, CH>,
                                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                            static_cast<int>(smem));
                 if (e != cudaSuccess) return e;
             }
-            fwd_kernel<T, CH, kLayoutProj><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
+            fwd_proj_kernel<T, CH><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
             break;
         }
-        default: fwd_kernel<T, CH, kLayoutStd><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
+        default: fwd_kernel<T, CH, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
     }
     return cudaGetLastError();
 }

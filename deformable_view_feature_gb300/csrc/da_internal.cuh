@@ -54,10 +54,6 @@ struct Problem {
     // and the weights are a softmax of logits [B,A,P,K,S,G].
     const float *loc;
     const float *weights;
-    const float *keypoints;
-    const float *projection;
-    const float *logits;
-    float image_w, image_h;
     int64_t rows;             // feature rows per batch item
     int32_t B, A, P, K, S, C, G, D;
     int32_t pks;              // P*K*S samples per (b, a, g)
@@ -73,6 +69,11 @@ struct Problem {
     int32_t gsplit;
     FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS, div_rows;
     MapInfo maps[DA_MAX_MAPS];
+    // Projected layout only (after the fields every kernel reads).
+    const float *keypoints;
+    const float *projection;
+    const float *logits;
+    float image_w, image_h;
 };
 
 struct FwdArgs {
