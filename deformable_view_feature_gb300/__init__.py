@@ -28,7 +28,7 @@ from . import build as _build
 
 __all__ = ["da_forward", "da_backward", "da_forward_fused", "da_backward_fused", "da_forward_projected",
            "da_backward_projected", "warpaffine_u8", "warpaffine_preprocess", "backward_workspace_size",
-           "DeformableAggregationFunction", "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
+           "da_backward_bin", "DeformableAggregationFunction", "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
 
 DA_F32, DA_BF16, DA_F16 = 0, 1, 2
 _STATUS = {0: "DA_OK", 1: "DA_ERR_NULL", 2: "DA_ERR_SHAPE", 3: "DA_ERR_ALIGN",
@@ -96,6 +96,8 @@ def load_library():
     lib.wa_warpaffine_u8.restype = ctypes.c_int
     lib.wa_preprocess.argtypes = [ctypes.POINTER(WaDims), vp, vp, ctypes.c_uint8, vp, vp, vp, vp]
     lib.wa_preprocess.restype = ctypes.c_int
+    lib.da_backward_bin.argtypes = [ctypes.POINTER(DaDims), vp, vp, vp, vp, ctypes.c_size_t, ctypes.c_uint32, vp]
+    lib.da_backward_bin.restype = ctypes.c_int
     lib.da_backward_fused_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
     lib.da_backward_fused_workspace_size.restype = ctypes.c_int
     lib.da_backward_workspace_size.argtypes = [ctypes.POINTER(DaDims), ctypes.POINTER(ctypes.c_size_t)]
@@ -217,12 +219,34 @@ def _workspace(device: torch.device, stream_handle, nbytes: int) -> torch.Tensor
     return ws
 
 
+def da_backward_bin(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index, sampling_location: torch.Tensor,
+                    weights: torch.Tensor, workspace: Optional[torch.Tensor] = None, deterministic: bool = False,
+                    stream=None) -> torch.Tensor:
+    """da_backward_bin: the location-only half of the binned backward, into
+    workspace (allocated if None; returned). mc_ms_feat and weights only give
+    the sizes. Finish with da_backward(..., path="binned", workspace=...,
+    binned_ready=True) ordered after it."""
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims(mc_ms_feat, ss, sampling_location, weights)
+    need = backward_workspace_size(d)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=sampling_location.device)
+    if workspace.numel() < need:
+        raise ValueError(f"workspace holds {workspace.numel()} bytes; {need} are needed")
+    _check(lib.da_backward_bin(ctypes.byref(d), ss.data_ptr() if ss.numel() else None,
+                               ls.data_ptr() if ls.numel() else None, _dptr(sampling_location), _dptr(workspace),
+                               workspace.numel(), 1 if deterministic else 0, _stream_handle(stream)))
+    return workspace
+
+
 def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
                 sampling_location: torch.Tensor, weights: torch.Tensor, grad_out: torch.Tensor,
                 grad_feat: Optional[torch.Tensor] = None, grad_loc: Optional[torch.Tensor] = None,
                 grad_weight: Optional[torch.Tensor] = None, stream=None, path: str = "scatter",
                 workspace: Optional[torch.Tensor] = None,
-                deterministic: bool = False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
+                deterministic: bool = False,
+                binned_ready: bool = False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Backward pass; returns (grad_feat fp32, grad_loc, grad_weight).
 
     path="scatter" (default) needs no workspace and scatters grad_feat with
@@ -232,8 +256,10 @@ def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
     (binned only) fixes the order of every row's contributions, so the
     gradients are the same bit for bit on every run (DA_BACKWARD_DETERMINISTIC).
     """
-    if deterministic and path != "binned":
-        raise ValueError("deterministic=True needs path='binned'")
+    if (deterministic or binned_ready) and path != "binned":
+        raise ValueError("deterministic=True and binned_ready=True need path='binned'")
+    if binned_ready and workspace is None:
+        raise ValueError("binned_ready=True needs the workspace da_backward_bin filled")
     lib = load_library()
     ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
     d = _dims(mc_ms_feat, ss, sampling_location, weights)
@@ -266,7 +292,8 @@ def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
     _check(lib.da_backward_ex(ctypes.byref(d), _dptr(mc_ms_feat), ss.data_ptr() if ss.numel() else None,
                               ls.data_ptr() if ls.numel() else None, _dptr(sampling_location),
                               _dptr(weights), _dptr(grad_out), _dptr(grad_feat), _dptr(grad_loc),
-                              _dptr(grad_weight), ws_ptr, ws_bytes, 1 if deterministic else 0, sh))
+                              _dptr(grad_weight), ws_ptr, ws_bytes,
+                              (1 if deterministic else 0) | (2 if binned_ready else 0), sh))
     return grad_feat, grad_loc, grad_weight
 
 

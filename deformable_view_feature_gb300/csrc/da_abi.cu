@@ -182,11 +182,13 @@ da_status forward_impl(const da_dims &d, da::FwdArgs &a, int chunks, float *out,
 da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const float *grad_out, float *grad_feat,
                         void *workspace, size_t workspace_bytes, uint32_t flags, da_stream_t stream)
 {
-    if (flags & ~static_cast<uint32_t>(DA_BACKWARD_DETERMINISTIC))
+    if (flags & ~static_cast<uint32_t>(DA_BACKWARD_DETERMINISTIC | DA_BACKWARD_BINNED_READY))
         return fail(DA_ERR_SHAPE, "unknown flags 0x%x", flags);
     const bool deterministic = (flags & DA_BACKWARD_DETERMINISTIC) != 0;
-    if (deterministic && !workspace && !workspace_bytes)
-        return fail(DA_ERR_WORKSPACE, "DA_BACKWARD_DETERMINISTIC needs the binned path's workspace");
+    const bool ready = (flags & DA_BACKWARD_BINNED_READY) != 0;
+    if ((deterministic || ready) && !workspace && !workspace_bytes)
+        return fail(DA_ERR_WORKSPACE, "DA_BACKWARD_DETERMINISTIC / DA_BACKWARD_BINNED_READY need the binned "
+                                      "path's workspace");
     const da::Problem &pb = a.pb;
     const int64_t n_out = static_cast<int64_t>(pb.num_ba) * pb.C;
     const int64_t n_gf = static_cast<int64_t>(pb.B) * pb.rows * pb.C;
@@ -227,7 +229,8 @@ da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const floa
             w.cap_s = L.cap_s;
             w.cap_g = L.cap_g;
         }
-        const cudaError_t e = da::launch_backward_binned(a, w, d.feat_dtype, s);
+        const cudaError_t e =
+            da::launch_backward_binned(a, w, d.feat_dtype, s, ready ? da::kStagePull : da::kStageAll);
         if (e != cudaSuccess) return cuda_fail(e, "binned backward launch");
         return DA_OK;
     }
@@ -418,6 +421,50 @@ da_status da_backward_ex(const da_dims *dims, const void *mc_ms_feat, const int3
     a.grad_loc = grad_loc;
     a.grad_weight = grad_weight;
     return backward_impl(*dims, a, chunks, grad_out, grad_feat, workspace, workspace_bytes, flags, stream);
+}
+
+da_status da_backward_bin(const da_dims *dims, const int32_t *spatial_shape, const int32_t *level_start_index,
+                          const float *sampling_location, void *workspace, size_t workspace_bytes, uint32_t flags,
+                          da_stream_t stream)
+{
+    if (flags & ~static_cast<uint32_t>(DA_BACKWARD_DETERMINISTIC))
+        return fail(DA_ERR_SHAPE, "da_backward_bin takes DA_BACKWARD_DETERMINISTIC only (flags 0x%x)", flags);
+    da::BwdArgs a{};
+    int chunks = 0;
+    da_status st = da::prepare_shape(dims, spatial_shape, level_start_index, a.pb, chunks);
+    if (st != DA_OK) return st;
+    const int64_t n_loc = static_cast<int64_t>(a.pb.num_ba) * a.pb.pk;
+    if (n_loc > 0 && !sampling_location) return fail(DA_ERR_NULL, "sampling_location is NULL");
+    if (!aligned(sampling_location, 8)) return fail(DA_ERR_ALIGN, "sampling_location must be 8-byte aligned");
+    a.pb.loc = sampling_location;
+    da::BinLayout L;
+    st = binned_layout(*dims, L);
+    if (st != DA_OK) return st;
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < L.bytes)
+        return fail(DA_ERR_WORKSPACE, "workspace must be 256-byte aligned and hold %zu bytes (got %zu)", L.bytes,
+                    workspace_bytes);
+    char *ws = static_cast<char *>(workspace);
+    da::BinArgs w{};
+    w.row_off = reinterpret_cast<int32_t *>(ws + L.off_row_off);
+    w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
+    w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
+    w.pos4 = reinterpret_cast<int32_t *>(ws + L.off_pos4);
+    w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
+    w.rows_total = L.rows_total;
+    w.nsid = L.nsid;
+    w.ncap = L.ncap;
+    w.ntiles = L.ntiles;
+    if (flags & DA_BACKWARD_DETERMINISTIC) {
+        w.sort_lists = reinterpret_cast<int32_t *>(ws + L.off_lists);
+        w.sort_counts = w.row_off + L.ntiles * da::kScanTile + 4;
+        w.cap_m = L.cap_m;
+        w.cap_s = L.cap_s;
+        w.cap_g = L.cap_g;
+    }
+    const cudaError_t e = da::launch_backward_binned(a, w, dims->feat_dtype, reinterpret_cast<cudaStream_t>(stream),
+                                                     da::kStageBin);
+    if (e != cudaSuccess) return cuda_fail(e, "binning launch");
+    return DA_OK;
 }
 
 da_status da_forward_fused(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,

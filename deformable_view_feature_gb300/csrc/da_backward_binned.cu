@@ -875,16 +875,18 @@ cudaError_t dispatch_pull(const PullArgs &pa, cudaStream_t st)
 
 }  // namespace
 
-cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st)
+cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st, int stages)
 {
     const Problem &pb = a.pb;
     cudaError_t e;
+    const int64_t npk = static_cast<int64_t>(pb.num_ba) * pb.P * pb.K;
+    if (!(stages & kStageBin)) goto pull_stage;
     // 1. counts
     if (w.ntiles > 0) {
         e = launch_zero_fill(reinterpret_cast<float *>(w.row_off), w.ntiles * kScanTile + kRowOffTail, st);
         if (e != cudaSuccess) return e;
     }
-    const int64_t npk = static_cast<int64_t>(pb.num_ba) * pb.P * pb.K;
+    {
     const int ctas_per_view = (pb.A * pb.P + kBinThreads - 1) / kBinThreads;
     const int64_t bin_grid = static_cast<int64_t>(pb.B) * pb.K * ctas_per_view;
     if (w.nsid > 0) {
@@ -928,6 +930,9 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
         sort_long_rows_kernel<<<static_cast<unsigned>(sms), 1024, 0, st>>>(pb, w);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
+    }
+pull_stage:
+    if (!(stages & kStagePull)) return cudaSuccess;
     // 4. grad_feat and d
     if (w.rows_total > 0) {
         const PullArgs pa{pb, a.grad_out, a.grad_feat, w, 0, w.rows_total};

@@ -150,7 +150,12 @@ struct BinArgs {
 // `chunks` = D * sizeof(feature) / 16, one of 1, 2, 4, 8.
 cudaError_t launch_forward(const FwdArgs &a, int feat_dtype, int chunks, cudaStream_t st);
 cudaError_t launch_backward(const BwdArgs &a, int feat_dtype, int chunks, cudaStream_t st);
-cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st);
+// Stages of the binned backward: the binning (count, scan, fill, and the
+// deterministic sort when asked for) depends on the locations only; the pull
+// and epilogue need grad_out.
+constexpr int kStageBin = 1, kStagePull = 2, kStageAll = 3;
+cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st,
+                                   int stages = kStageAll);
 cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st);
 // Chain rule of the projected layout: grad_logits and grad_keypoints from the
 // operator's grad_loc and grad_weight (pb holds keypoints, projection, image

@@ -188,9 +188,19 @@ da_status da_backward(const da_dims *dims,
  *       time, more when many samples crowd a few pixels.
  *
  * Other arguments are those of da_backward. Unknown flags give
- * DA_ERR_SHAPE. da_backward(...) is da_backward_ex(..., 0, stream).
+ * DA_ERR_SHAPE. da_backward(...) is da_backward_ex(..., 0, stream). With
+ * DA_BACKWARD_BINNED_READY, DA_BACKWARD_DETERMINISTIC has no further effect
+ * (the order was fixed, or not, by da_backward_bin).
  */
 #define DA_BACKWARD_DETERMINISTIC 1u
+/*
+ *   DA_BACKWARD_BINNED_READY  the workspace already holds the binning of
+ *       these sampling locations, made by da_backward_bin (with the same
+ *       dims, map tables and locations, and DA_BACKWARD_DETERMINISTIC there
+ *       if a fixed order is wanted); only the steps that need grad_out run.
+ *       The call must be ordered after that da_backward_bin on the GPU.
+ */
+#define DA_BACKWARD_BINNED_READY 2u
 da_status da_backward_ex(const da_dims *dims,
                          const void *mc_ms_feat,
                          const int32_t *spatial_shape,
@@ -334,6 +344,29 @@ da_status da_backward_projected(const da_dims *dims,
                                 size_t workspace_bytes,
                                 uint32_t flags,
                                 da_stream_t stream);
+
+/*
+ * da_backward_bin: the first half of the binned backward, the part that
+ * depends on the sampling locations only: it sorts the corner contributions
+ * by feature row into the workspace (counts, prefix sums, records, and with
+ * DA_BACKWARD_DETERMINISTIC the fixed order inside each row). A later
+ * da_backward_ex with DA_BACKWARD_BINNED_READY and the same workspace does
+ * the rest. The pages have no counterpart: it lets a training step run the
+ * binning on another stream while da_forward runs, since neither needs the
+ * other's results.
+ *   dims, spatial_shape, level_start_index, sampling_location: as for
+ *   da_backward (mc_ms_feat, weights and grad_out are not read).
+ *   workspace, workspace_bytes: as for da_backward's binned path.
+ * The workspace must not be in use by another call on the GPU meanwhile.
+ */
+da_status da_backward_bin(const da_dims *dims,
+                          const int32_t *spatial_shape,
+                          const int32_t *level_start_index,
+                          const float *sampling_location,
+                          void *workspace,
+                          size_t workspace_bytes,
+                          uint32_t flags,
+                          da_stream_t stream);
 
 /*
  * da_backward_noalloc: the binned backward, with its scratch in a fixed

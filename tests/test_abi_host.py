@@ -177,7 +177,7 @@ def test_backward_ex_flags(lib):
     def call(flags, ws=None, ws_bytes=0):
         return lib.da_backward_ex(ctypes.byref(_dims()), FAKE, ss, ls, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws,
                                   ws_bytes, flags, None)
-    assert call(2) == DA_ERR_SHAPE  # unknown flag
+    assert call(4) == DA_ERR_SHAPE  # unknown flag
     assert b"flags" in lib.da_last_error()
     assert call(1) == 6  # deterministic without a workspace
     assert b"DETERMINISTIC" in lib.da_last_error()
@@ -253,7 +253,7 @@ def test_binding_signatures_reach_validation(lib):
     assert bl.da_forward_projected(d, F, ss, ls, F, F, 0.0, 4.0, F, F, None, None, None) == DA_ERR_SHAPE
     assert bl.da_backward_projected(d, F, ss, ls, F, F, 0.0, 4.0, F, F, F, F, F, F, F, F, None, 0, 0,
                                     None) == DA_ERR_SHAPE
-    assert bl.da_backward_ex(d, F, ss, ls, F, F, F, F, F, F, None, 0, 2, None) == DA_ERR_SHAPE
+    assert bl.da_backward_ex(d, F, ss, ls, F, F, F, F, F, F, None, 0, 4, None) == DA_ERR_SHAPE
     assert b"flags" in bl.da_last_error()
 
 
@@ -285,3 +285,14 @@ def test_fused_workspace_size(lib):
     assert base <= n.value < base + 4 * 64 * 3136 * 4 + (8 << 20)
     bad = _dims(num_embeds=48, num_groups=4)  # D = 12: not a power of two
     assert bl.da_backward_fused_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == DA_ERR_UNSUPPORTED
+
+
+def test_binning_entry_validation(lib):
+    bl = da.load_library()
+    ss, ls = _tables()
+    d = ctypes.byref(_dims())
+    assert bl.da_backward_bin(d, ss, ls, FAKE, FAKE, 1 << 30, 2, None) == DA_ERR_SHAPE  # READY is not a bin flag
+    assert bl.da_backward_bin(d, ss, ls, FAKE + 4, FAKE, 1 << 30, 0, None) == DA_ERR_ALIGN
+    assert bl.da_backward_bin(d, ss, ls, FAKE, FAKE, 16, 0, None) == 6  # workspace too small
+    # READY without a workspace
+    assert bl.da_backward_ex(d, FAKE, ss, ls, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 2, None) == 6

@@ -129,3 +129,28 @@ def test_deterministic_needs_binned(da):
     with pytest.raises(ValueError):
         da.da_backward(inp.feat.to(dev), inp.spatial_shape, inp.level_start_index, inp.loc.to(dev),
                        inp.weights.to(dev), inp.grad_out.to(dev), path="scatter", deterministic=True)
+
+
+@pytest.mark.parametrize("name", ["sp4d_train", "tiny"])
+def test_binning_on_a_side_stream_during_the_forward(da, name):
+    """da_backward_bin on a second stream while da_forward runs, then the rest
+    of the backward with binned_ready: with the deterministic order on both
+    sides, the same bits as the one-call deterministic backward."""
+    inp = da_inputs.make_inputs(name)
+    dev = torch.device("cuda")
+    feat, loc, w, go = (t.to(dev) for t in (inp.feat, inp.loc, inp.weights, inp.grad_out))
+    ss, ls = inp.spatial_shape, inp.level_start_index
+    ref = _backward(da, inp, garbage_seed=7)
+    main, side = torch.cuda.Stream(), torch.cuda.Stream()
+    ws = None
+    for rep in range(2):  # the second round re-bins into a workspace the first round used
+        torch.cuda.synchronize()
+        ws = da.da_backward_bin(feat, ss, ls, loc, w, workspace=ws, deterministic=True, stream=side)
+        done = torch.cuda.Event()
+        done.record(side)
+        da.da_forward(feat, ss, ls, loc, w, stream=main)
+        main.wait_event(done)
+        gf, gl, gw = da.da_backward(feat, ss, ls, loc, w, go, path="binned", workspace=ws, binned_ready=True,
+                                    stream=main)
+        torch.cuda.synchronize()
+        _same_bits(ref, dict(zip(NAMES, (to_np(t) for t in (gf, gl, gw)))))
