@@ -283,6 +283,49 @@ def config_of(wl, l2):
 
 # ----------------------------------------------------------------------------- our arm
 
+def run_e2e(a, wl, inp, dev, world, dev_tensors, ss, ls):
+    """End to end through the public API: pinned host tensors and the library's
+    host pipeline (da_pipeline_*), whose copies in both directions and kernels
+    overlap across consecutive steps. The timed region holds every step's
+    host->device input copies, kernels and device->host output copies."""
+    import deformable_view_feature_gb300 as da
+    feat, loc, w, go, out, gf, gl, gw = dev_tensors
+    h_in = [t.pin_memory() for t in (inp.feat, inp.loc, inp.weights, inp.grad_out)]
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, gf, gl, gw)]
+    if not wl.backward:
+        h_in, h_out = h_in[:3], h_out[:1]
+    e2e_steps = max(1, min(a.steps, a.e2e_steps))
+    pipe = da.HostPipeline(da._dims(feat, da._host_i32(ss), loc, w), ss, ls, backward=wl.backward,
+                           depth=2, device=dev)
+
+    def e2e_step():
+        hf, hl, hw = h_in[:3]
+        if wl.backward:
+            pipe.submit(hf, hl, hw, h_out[0], grad_out=h_in[3], grad_feat=h_out[1], grad_loc=h_out[2],
+                        grad_weight=h_out[3])
+        else:
+            pipe.submit(hf, hl, hw, h_out[0])
+
+    for _ in range(3):
+        e2e_step()
+    pipe.sync()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    pipe.sync()
+    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world)
+    pipe.close()
+    barrier(world)
+    h2d = tensor_bytes(*h_in)
+    d2h = tensor_bytes(*h_out)
+    e2e = {"value": wl.num_samples * e2e_steps * world / (e2e_ms / 1e3), "unit": "samples/s",
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+           "api": "HostPipeline (da_pipeline_submit, depth 2), pinned host tensors, wall clock"}
+
+    return e2e
+
+
 def run_ours(a, wl):
     import deformable_view_feature_gb300 as da
     da.load_library()
@@ -370,42 +413,14 @@ def run_ours(a, wl):
     # host pipeline (da_pipeline_*), whose copies in both directions and
     # kernels overlap across consecutive steps. The timed region holds every
     # step's host->device input copies, kernels and device->host output copies.
-    h_in = [t.pin_memory() for t in (inp.feat, inp.loc, inp.weights, inp.grad_out)]
-    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, gf, gl, gw)]
-    if not wl.backward:
-        h_in, h_out = h_in[:3], h_out[:1]
-    e2e_steps = max(1, min(a.steps, a.e2e_steps))
-    pipe = da.HostPipeline(da._dims(feat, da._host_i32(ss), loc, w), ss, ls, backward=wl.backward,
-                           depth=2, device=dev)
-
-    def e2e_step():
-        hf, hl, hw = h_in[:3]
-        if wl.backward:
-            pipe.submit(hf, hl, hw, h_out[0], grad_out=h_in[3], grad_feat=h_out[1], grad_loc=h_out[2],
-                        grad_weight=h_out[3])
-        else:
-            pipe.submit(hf, hl, hw, h_out[0])
-
-    for _ in range(3):
-        e2e_step()
-    pipe.sync()
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        e2e_step()
-    pipe.sync()
-    e2e_ms = max_over_ranks((time.perf_counter() - t0) * 1e3, world)
-    pipe.close()
-    barrier(world)
-    h2d = tensor_bytes(*h_in)
-    d2h = tensor_bytes(*h_out)
-    e2e = {"value": wl.num_samples * e2e_steps * world / (e2e_ms / 1e3), "unit": "samples/s",
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
-           "api": "HostPipeline (da_pipeline_submit, depth 2), pinned host tensors, wall clock"}
+    e2e = None
+    if a.e2e_steps > 0:
+        e2e = run_e2e(a, wl, inp, dev, world, (feat, loc, w, go, out, gf, gl, gw), ss, ls)
 
     if rank != 0:
         return
     peak, peak_kind = peaks()
+
     if wl.backward:
         dom_ms, dom_bytes, dom = statistics.mean(bwd_ms), bwd_bytes, "da_backward"
         traffic = ncu_traffic(wl.name, f"da_backward[{a.bwd_path}]")
@@ -655,7 +670,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="sp4d_train", choices=list(da_inputs.WORKLOADS))
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="steps of the end-to-end (host tensors) measurement; 0 skips it (profiling runs)")
     ap.add_argument("--cpu-anchors", type=int, default=1800,
                     help="anchors in the CPU-baseline sample")
     ap.add_argument("--ref-anchors", type=int, default=300,
