@@ -786,6 +786,81 @@ __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const B
     }
 }
 
+// The same with one lane per (location, scale), carrying all G groups in
+// 16-byte vectors (G = 4 or 8, S dividing 32): a warp covers 32/S
+// locations. The weights of a sample, its grad_weight and each corner's d
+// are G contiguous floats, so every access is a 16- or 32-byte vector, and
+// the footprint and the bookkeeping run once per sample instead of once per
+// (sample, group). The S lanes of a location sum grad_loc with shuffles.
+template <int G>
+__global__ void __launch_bounds__(256) epilogue_vec_kernel(const Problem pb, const BinArgs w, float *grad_loc,
+                                                           float *grad_weight, int64_t npk, int s_log2)
+{
+    static_assert(G == 4 || G == 8, "16-byte vectors of G floats");
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    stage_maps(pb, maps_s);
+    __syncthreads();
+    const int S = pb.S;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t pk64 = t >> s_log2;
+    const int s = static_cast<int>(t & (S - 1));
+    const bool live = pk64 < npk;
+    // Lanes past the end run on the last location (whole locations, so the
+    // shuffles stay within live lanes) and store nothing.
+    const int pk = static_cast<int>(live ? pk64 : npk - 1);
+    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
+    const int k = pk - bap * pb.K;
+    const int bq = static_cast<int>(pb.div_P.div(bap));  // b*A + a
+    const int b = static_cast<int>(pb.div_A.div(bq));
+    const int q = bap - b * pb.A * pb.P;  // a*P + p
+    const int64_t vsid = ((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * S + s;
+    const int64_t sid = static_cast<int64_t>(pk) * S + s;
+    const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + static_cast<int64_t>(pk) * 2);
+    const MapInfo m = maps_s[k * S + s];
+    Footprint f;
+    footprint(xy.x, xy.y, m, f);
+    const int4 pos = reinterpret_cast<const int4 *>(w.pos4)[vsid];
+    const int pc[4] = {pos.x, pos.y, pos.z, pos.w};
+    float wt[G], d[4][G];
+#pragma unroll
+    for (int h = 0; h < G / 4; ++h) {
+        const float4 v = __ldg(reinterpret_cast<const float4 *>(pb.weights + sid * G) + h);
+        wt[4 * h] = v.x; wt[4 * h + 1] = v.y; wt[4 * h + 2] = v.z; wt[4 * h + 3] = v.w;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+#pragma unroll
+        for (int h = 0; h < G / 4; ++h) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (pc[c] >= 0) v = __ldg(reinterpret_cast<const float4 *>(w.dpix + static_cast<int64_t>(pc[c]) * G) + h);
+            d[c][4 * h] = v.x; d[c][4 * h + 1] = v.y; d[c][4 * h + 2] = v.z; d[c][4 * h + 3] = v.w;
+        }
+    }
+    float gw[G];
+    float gx = 0.f, gy = 0.f;
+    const float fw = static_cast<float>(m.W), fh = static_cast<float>(m.H);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        gw[g] = f.cw[0] * d[0][g] + f.cw[1] * d[1][g] + f.cw[2] * d[2][g] + f.cw[3] * d[3][g];
+        gx += fw * wt[g] * (f.lh * (d[3][g] - d[2][g]) + f.hh * (d[1][g] - d[0][g]));
+        gy += fh * wt[g] * (f.lw * (d[3][g] - d[1][g]) + f.hw * (d[2][g] - d[0][g]));
+    }
+    if (live) {
+#pragma unroll
+        for (int h = 0; h < G / 4; ++h)
+            reinterpret_cast<float4 *>(grad_weight + sid * G)[h] =
+                make_float4(gw[4 * h], gw[4 * h + 1], gw[4 * h + 2], gw[4 * h + 3]);
+    }
+    for (int o = 1; o < S; o <<= 1) {
+        gx += __shfl_xor_sync(0xffffffffu, gx, o);
+        gy += __shfl_xor_sync(0xffffffffu, gy, o);
+    }
+    if (live && s == 0) {
+        grad_loc[static_cast<int64_t>(pk) * 2] = gx;
+        grad_loc[static_cast<int64_t>(pk) * 2 + 1] = gy;
+    }
+}
+
 // The fused layout's rewrite (G = 1): a location has S samples of one group,
 // too few for a warp, so one thread takes a location. The gradients go to
 // grad_loc_weight [.., 2 + S]: (dL/dx, dL/dy, dL/dw_0 .. dL/dw_{S-1}).
@@ -946,8 +1021,28 @@ pull_stage:
         epilogue_fused_kernel<<<static_cast<unsigned>((npk + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc, npk);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     } else if (npk > 0) {
-        epilogue_kernel<<<static_cast<unsigned>((npk * 32 + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc,
-                                                                                         a.grad_weight, 0, npk);
+#ifndef DA_EPI_VEC
+#define DA_EPI_VEC 1
+#endif
+        // The vector kernel reads weights and writes grad_weight as 16-byte
+        // vectors; the interface promises only 4-byte alignment for those.
+        const bool aligned16 = (reinterpret_cast<uintptr_t>(pb.weights) % 16) == 0 &&
+                               (reinterpret_cast<uintptr_t>(a.grad_weight) % 16) == 0;
+        const bool vec = DA_EPI_VEC && aligned16 && (pb.G == 4 || pb.G == 8) && pb.S >= 1 && pb.S <= 32 &&
+                         (32 % pb.S) == 0;
+        if (vec) {
+            int s_log2 = 0;
+            while ((1 << s_log2) < pb.S) ++s_log2;
+            const int64_t threads = npk << s_log2;
+            const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
+            if (pb.G == 8)
+                epilogue_vec_kernel<8><<<grid, 256, 0, st>>>(pb, w, a.grad_loc, a.grad_weight, npk, s_log2);
+            else
+                epilogue_vec_kernel<4><<<grid, 256, 0, st>>>(pb, w, a.grad_loc, a.grad_weight, npk, s_log2);
+        } else {
+            epilogue_kernel<<<static_cast<unsigned>((npk * 32 + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc,
+                                                                                             a.grad_weight, 0, npk);
+        }
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     return cudaSuccess;

@@ -259,3 +259,26 @@ def test_invalid_arguments_raise_before_launch(da):
     with pytest.raises(ValueError):
         da.da_forward(feat.cpu(), inp.spatial_shape, inp.level_start_index, loc, w)
     torch.cuda.synchronize()
+
+
+def test_binned_with_weights_only_4_byte_aligned(da):
+    """weights and grad_weight 4 bytes off a 16-byte boundary (the interface
+    allows it): the binned backward's epilogue must not use its 16-byte
+    vector form, and the results still match the oracle."""
+    inp = _custom(31, [[(10, 12), (5, 6)], [(8, 8), (4, 4)]], 2, 256, 8, 13, 13, "f32")
+    dev = torch.device("cuda")
+    feat, loc, go = inp.feat.to(dev), inp.loc.to(dev), inp.grad_out.to(dev)
+    n = inp.weights.numel()
+    wbuf = torch.empty(n + 1, device=dev)
+    w = wbuf[1:].view(inp.weights.shape)
+    w.copy_(inp.weights.to(dev))
+    gbuf = torch.full((n + 1,), float("nan"), device=dev)
+    gw = gbuf[1:].view(inp.weights.shape)
+    assert w.data_ptr() % 16 == 4 and gw.data_ptr() % 16 == 4
+    gf, gl, _ = da.da_backward(feat, inp.spatial_shape, inp.level_start_index, loc, w, go, grad_weight=gw,
+                               path="binned")
+    torch.cuda.synchronize()
+    got = {"grad_feat": to_np(gf), "grad_loc": to_np(gl), "grad_weight": to_np(gw)}
+    ref = oracle.run_inputs(inp)
+    ref.pop("out")
+    _compare(inp, got, ref)
