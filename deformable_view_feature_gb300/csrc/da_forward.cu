@@ -48,6 +48,8 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     constexpr int SPP = 8 / CH;     // samples per warp-wide load
     // Samples per lane per step; a warp-wide step covers U * SPP <= 32.
     constexpr int U = DA_FWD_UNROLL * SPP <= 32 ? DA_FWD_UNROLL : 32 / SPP;
+    // The steps of U*SPP samples must tile the 32 table entries exactly.
+    static_assert(U % 2 == 0 && 32 % (U * SPP) == 0, "unroll must divide the 32-sample table");
     const Problem &pb = args.pb;
 
     __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
@@ -163,6 +165,8 @@ __global__ void __launch_bounds__(kThreads) fwd_proj_kernel(const FwdArgs args)
     constexpr int SPP = 8 / CH;     // samples per warp-wide load
     // Samples per lane per step; a warp-wide step covers U * SPP <= 32.
     constexpr int U = DA_FWD_UNROLL * SPP <= 32 ? DA_FWD_UNROLL : 32 / SPP;
+    // The steps of U*SPP samples must tile the 32 table entries exactly.
+    static_assert(U % 2 == 0 && 32 % (U * SPP) == 0, "unroll must divide the 32-sample table");
     const Problem &pb = args.pb;
 
     __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
