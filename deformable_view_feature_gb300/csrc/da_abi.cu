@@ -237,6 +237,15 @@ da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const floa
     cudaError_t e = da::launch_zero_fill(grad_feat, n_gf, s);
     if (e != cudaSuccess) return cuda_fail(e, "grad_feat zero-fill");
     if (n_out == 0) return DA_OK;
+    if (pb.pks == 0) {
+        // No samples, but with S = 0 scales the location entries still exist:
+        // their gradients are 0. (The sampling kernels write grad_loc only
+        // while walking samples.)
+        const int64_t n_loc =
+            static_cast<int64_t>(pb.num_ba) * pb.pk * (pb.layout == da::kLayoutFused ? 2 * pb.G : 2);
+        if (n_loc > 0) e = cudaMemsetAsync(a.grad_loc, 0, static_cast<size_t>(n_loc) * sizeof(float), s);
+        return e == cudaSuccess ? DA_OK : cuda_fail(e, "grad_loc zero-fill");
+    }
     e = da::launch_backward(a, d.feat_dtype, chunks, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
     return DA_OK;

@@ -155,3 +155,20 @@ def test_binned_workspace_too_small_refused(da):
     st = lib.da_backward_fused(ctypes.byref(d), feat.data_ptr(), ss.data_ptr(), ls.data_ptr(), lw.data_ptr(),
                                go.data_ptr(), gf.data_ptr(), glw.data_ptr(), ws.data_ptr(), ws.numel(), None)
     assert st == 6  # DA_ERR_WORKSPACE
+
+
+@pytest.mark.parametrize("path", PATHS)
+def test_no_scales(da, path):
+    """S = 0: loc_weight [B,A,G,P,K,2] holds locations with no weights; the
+    output is 0 and so is every location gradient."""
+    g = torch.Generator().manual_seed(51)
+    B, A, G, P, K, C = 2, 5, 4, 3, 2, 64
+    dev = torch.device("cuda")
+    feat = torch.randn(B, 6, C, generator=g).to(dev)
+    ss, ls = torch.zeros(K, 0, 2, dtype=torch.int32), torch.zeros(K, 0, dtype=torch.int32)
+    lw = torch.rand(B, A, G, P, K, 2, generator=g).to(dev)
+    go = torch.randn(B, A, C, generator=g).to(dev)
+    out = da.da_forward_fused(feat, ss, ls, lw)
+    gf, glw = da.da_backward_fused(feat, ss, ls, lw, go, path=path)
+    torch.cuda.synchronize()
+    assert torch.all(out == 0) and torch.all(gf == 0) and torch.all(glw == 0)
