@@ -1021,14 +1021,11 @@ pull_stage:
         epilogue_fused_kernel<<<static_cast<unsigned>((npk + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc, npk);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     } else if (npk > 0) {
-#ifndef DA_EPI_VEC
-#define DA_EPI_VEC 1
-#endif
         // The vector kernel reads weights and writes grad_weight as 16-byte
         // vectors; the interface promises only 4-byte alignment for those.
         const bool aligned16 = (reinterpret_cast<uintptr_t>(pb.weights) % 16) == 0 &&
                                (reinterpret_cast<uintptr_t>(a.grad_weight) % 16) == 0;
-        const bool vec = DA_EPI_VEC && aligned16 && (pb.G == 4 || pb.G == 8) && pb.S >= 1 && pb.S <= 32 &&
+        const bool vec = aligned16 && (pb.G == 4 || pb.G == 8) && pb.S >= 1 && pb.S <= 32 &&
                          (32 % pb.S) == 0;
         if (vec) {
             int s_log2 = 0;
