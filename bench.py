@@ -8,9 +8,13 @@ One step is one pass of the whole path: da_forward, then da_backward (the
 grad_feat zero-fill plus the gradient kernel). Inputs are synthetic and seeded
 (da_inputs), and resident in HBM when the timed region starts. The feature
 tensor alone (551 MB) is larger than L2, so no L2 flush is done between
-steps.
+steps. Other workloads (--workload) whose feature map is under twice the L2
+size get an L2 flush before every step by default (--l2 auto): a write of
+twice the L2 size, outside the step's own events, which then give the step
+time.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--l2 auto|flush|none]
 
 Prints ONE JSON line on rank 0. It holds:
   * value: samples/s over all ranks;
@@ -352,7 +356,15 @@ def run_ours(a, wl):
     # The binning half of the binned backward needs the locations only: it runs
     # on a side stream while the forward runs (da_backward_bin), after the
     # previous step's backward has released the workspace.
-    overlap = wl.backward and path == "binned" and not a.no_bin_overlap
+    # L2 policy: flush before every step when the maps would otherwise stay
+    # in L2 between steps.
+    l2_bytes = torch.cuda.get_device_properties(dev).L2_cache_size
+    feat_bytes = inp.feat.numel() * inp.feat.element_size()
+    flush = a.l2 == "flush" or (a.l2 == "auto" and feat_bytes < 2 * l2_bytes)
+    flush_buf = torch.empty(2 * l2_bytes // 4, dtype=torch.float32, device=dev) if flush else None
+    # In flush mode the step time is the sum of its own events, so the
+    # binning runs inside da_backward rather than beside the flush.
+    overlap = wl.backward and path == "binned" and not a.no_bin_overlap and not flush
     # Default priority: a high-priority side stream interleaves the binning
     # with the forward's blocks, but the forward then slows by as much as the
     # backward gains (measured); at equal priority the binning fills the
@@ -362,6 +374,9 @@ def run_ours(a, wl):
     det = a.bwd_path == "binned-det"
 
     def step(ev=None):
+        if flush:
+            with torch.cuda.stream(stream):
+                flush_buf.fill_(float(ev is not None))
         if overlap:
             side.wait_event(bwd_done)
             da.da_backward_bin(feat, ss, ls, loc, w, workspace=ws, deterministic=det, stream=side)
@@ -402,10 +417,12 @@ def run_ours(a, wl):
     barrier(world)
     time.sleep(0.1)
     clocks.stop()
-    ms = start.elapsed_time(end)
-    ms_max = max_over_ranks(ms, world)
     fwd_ms = [evs[i][0].elapsed_time(evs[i][1]) for i in range(a.steps)]
     bwd_ms = [evs[i][1].elapsed_time(evs[i][2]) for i in range(a.steps)] if wl.backward else []
+    # Without a flush the steps run back to back and the whole region counts;
+    # with one, only each step's own events (the flush between them does not).
+    ms = start.elapsed_time(end) if not flush else sum(fwd_ms) + sum(bwd_ms)
+    ms_max = max_over_ranks(ms, world)
 
     value = job_throughput(wl.num_samples, a.steps, world, ms_max)
 
@@ -435,8 +452,16 @@ def run_ours(a, wl):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32"
         if wl.feat_dtype == "f32" else "bf16-features/f32",
         "data": "synthetic (seeded da_inputs draw with the workload's shapes and distributions)",
-        "config": config_of(wl, "inputs larger than L2 (feature map "
-                                f"{inp.feat.numel() * inp.feat.element_size() / 1e6:.0f} MB), no flush"),
+        "config": config_of(wl, (f"L2 flushed before every step (a {2 * l2_bytes / 1e6:.0f} MB write outside "
+                                 "the step's events; feature map "
+                                 f"{feat_bytes / 1e6:.0f} MB)") if flush else
+                            (f"no flush: feature map {feat_bytes / 1e6:.0f} MB"
+                             + (" larger than L2" if feat_bytes >= 2 * l2_bytes else " (warm L2)"))),
+        "channel_samples_per_s": value * (wl.num_embeds // wl.num_groups),
+        # Effective gather bandwidth: every sample reads its four corner rows
+        # (D channels each) once per pass when nothing is reused.
+        "gather_gbs": (2 if wl.backward else 1) * wl.num_samples * 4 * (wl.num_embeds // wl.num_groups)
+        * inp.feat.element_size() / (step_ms / 1e3) / 1e9,
         "gbs_step": (fwd_bytes + (bwd_bytes if wl.backward else 0)) / (step_ms / 1e3) / 1e9,
         "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms) if bwd_ms else None,
         "roofline": {"bound": "hbm", "kernel": dom + (f" ({a.bwd_path} path, all its kernels)"
@@ -677,6 +702,8 @@ def main():
     ap.add_argument("--ref-anchors", type=int, default=300,
                     help="anchors per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
+                    help="L2 flush before every step: auto = when the feature map is under twice the L2 size")
     ap.add_argument("--no-bin-overlap", action="store_true",
                     help="run the binned backward's binning inside da_backward instead of on a side stream "
                          "during the forward")
