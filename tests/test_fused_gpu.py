@@ -172,3 +172,30 @@ def test_no_scales(da, path):
     gf, glw = da.da_backward_fused(feat, ss, ls, lw, go, path=path)
     torch.cuda.synchronize()
     assert torch.all(out == 0) and torch.all(gf == 0) and torch.all(glw == 0)
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_random_shapes(da, i):
+    """Seeded random shapes of the DCNv4 form through both backward paths (the
+    binned one where it is served): K, S in 1..4 with map sides 1..20, a group
+    width of 16/32/64/128 bytes, G in 1..8, B in 1..3, A in 1..30, P in 1..13;
+    per-group points in [-0.3, 1.3] and softmax weights."""
+    r = np.random.default_rng(3000 + i)
+    dtype = ["f32", "bf16", "f16"][r.integers(3)]
+    elem = 4 if dtype == "f32" else 2
+    while True:
+        D = int(r.choice([16, 32, 64, 128])) // elem
+        G = int(r.choice([1, 2, 3, 4, 8]))
+        if D * G <= 256:
+            break
+    S = int(r.integers(1, 5))
+    wl = da_inputs.WORKLOADS["tiny"].replace(
+        name=f"fused_random{i}", batch=int(r.integers(1, 4)), num_cams=int(r.integers(1, 5)),
+        shapes=tuple((int(r.integers(1, 21)), int(r.integers(1, 21))) for _ in range(S)),
+        num_embeds=D * G, num_groups=G, num_anchors=int(r.integers(1, 31)), num_pts=int(r.integers(1, 14)),
+        feat_dtype=dtype, loc_lo=-0.3, loc_hi=1.3, weight_kind="softmax")
+    inp = da_inputs.make_fused_inputs(wl, seed=4000 + i)
+    for path in PATHS:
+        if path == "binned" and not _binned_ok(inp):
+            continue
+        _check(inp, _run(da, inp, path))

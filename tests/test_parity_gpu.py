@@ -284,6 +284,14 @@ def test_binned_with_weights_only_4_byte_aligned(da):
     _compare(inp, got, ref)
 
 
+def _softmax_weights(inp):
+    """Replace the weights by a softmax over each (b, a, g)'s P*K*S samples,
+    as the Sparse4D workloads draw them."""
+    B, A, P, K, S, G = inp.weights.shape
+    w = inp.weights.permute(0, 1, 5, 2, 3, 4).reshape(B, A, G, -1).softmax(-1)
+    inp.weights = w.reshape(B, A, G, P, K, S).permute(0, 1, 3, 4, 5, 2).contiguous()
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("K,S,G", [(8, 8, 8), (64, 1, 2), (1, 64, 4)])
 def test_maximum_map_count(da, K, S, G, path):
@@ -291,13 +299,11 @@ def test_maximum_map_count(da, K, S, G, path):
     Map sizes vary per camera, so no two cameras share a layout."""
     shapes = [[(2 + (3 * k + s) % 6, 1 + (k + 2 * s) % 7) for s in range(S)] for k in range(K)]
     inp = _custom(40 + K, shapes, 2, 64, G, 7, 3)
-    # Weights normalised as in the Sparse4D workloads (a softmax over each
-    # (b, a, g)'s P*K*S samples): unit weights over N(0,1) features would sum
-    # 192 terms that cancel far below their size, and this case is about the
-    # map tables, not conditioning; the forward keeps its 1e-5 relative bound.
-    B_, A_, P_, K_, S_, G_ = inp.weights.shape
-    w = inp.weights.permute(0, 1, 5, 2, 3, 4).reshape(B_, A_, G_, -1).softmax(-1)
-    inp.weights = w.reshape(B_, A_, G_, P_, K_, S_).permute(0, 1, 3, 4, 5, 2).contiguous()
+    # Weights normalised as in the Sparse4D workloads: unit weights over
+    # N(0,1) features would sum 192 terms that cancel far below their size,
+    # and this case is about the map tables, not conditioning; the forward
+    # keeps its 1e-5 relative bound.
+    _softmax_weights(inp)
     got = _run_gpu(da, inp, path=path)
     _compare(inp, got, oracle.run_inputs(inp))
 
@@ -322,3 +328,35 @@ def test_no_maps(da, K, S, path):
     assert got["grad_weight"].size == 0
     ref = oracle.run_inputs(inp)
     assert np.all(ref["out"] == 0) and np.all(ref["grad_feat"] == 0) and np.all(ref["grad_loc"] == 0)
+
+
+def _random_case(i):
+    """Shapes, dtype and sizes of random case i (seeded): K, S in 1..4 with map
+    sides 1..20, a group width of 16/32/64/128 bytes, G in 1..8 with C <= 256,
+    B in 1..3, A in 1..40, P in 1..13."""
+    r = np.random.default_rng(1000 + i)
+    dtype = ["f32", "bf16", "f16"][r.integers(3)]
+    elem = 4 if dtype == "f32" else 2
+    while True:
+        D = int(r.choice([16, 32, 64, 128])) // elem
+        G = int(r.choice([1, 2, 3, 4, 8]))
+        if D * G <= 256:
+            break
+    K, S = int(r.integers(1, 5)), int(r.integers(1, 5))
+    shapes = [[(int(r.integers(1, 21)), int(r.integers(1, 21))) for _ in range(S)] for _ in range(K)]
+    return dict(seed=2000 + i, shapes=shapes, B=int(r.integers(1, 4)), C=D * G, G=G,
+                A=int(r.integers(1, 41)), P=int(r.integers(1, 14)), dtype=dtype)
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_shapes(da, i):
+    """Seeded random shapes through both backward paths (the binned one where
+    it is served) against the oracle."""
+    c = _random_case(i)
+    inp = _custom(c["seed"], c["shapes"], c["B"], c["C"], c["G"], c["A"], c["P"], c["dtype"])
+    _softmax_weights(inp)
+    ref = oracle.run_inputs(inp)
+    for path in PATHS:
+        if path == "binned" and not binned_supported(c["C"], c["G"]):
+            continue
+        _compare(inp, _run_gpu(da, inp, path=path), ref)
