@@ -426,6 +426,39 @@ def run_ours(a, wl):
 
     value = job_throughput(wl.num_samples, a.steps, world, ms_max)
 
+    # The same step captured once in a CUDA graph (the binning forked to the
+    # side stream and joined inside the capture) and replayed.
+    graph = None
+    if a.graph and not flush:
+        def graph_step():
+            if wl.backward and path == "binned":
+                side.wait_stream(stream)
+                da.da_backward_bin(feat, ss, ls, loc, w, workspace=ws, deterministic=det, stream=side)
+            da.da_forward(feat, ss, ls, loc, w, out=out, stream=stream)
+            if wl.backward:
+                if path == "binned":
+                    stream.wait_stream(side)
+                da.da_backward(feat, ss, ls, loc, w, go, grad_feat=gf, grad_loc=gl, grad_weight=gw, stream=stream,
+                               path=path, workspace=ws, deterministic=det, binned_ready=path == "binned")
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            graph_step()
+        for _ in range(a.warmup):
+            g.replay()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        g0.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(a.steps):
+                g.replay()
+        g1.record(stream)
+        torch.cuda.synchronize(dev)
+        gms = max_over_ranks(g0.elapsed_time(g1), world)
+        graph = {"ms_per_step": gms / a.steps, "value": job_throughput(wl.num_samples, a.steps, world, gms),
+                 "unit": "samples/s", "note": "one step captured in a CUDA graph, replayed back to back"}
+
     # End to end through the public API: pinned host tensors and the library's
     # host pipeline (da_pipeline_*), whose copies in both directions and
     # kernels overlap across consecutive steps. The timed region holds every
@@ -476,6 +509,8 @@ def run_ours(a, wl):
         "workspace_bytes": int(ws.numel()) if ws is not None else 0,
         "clocks": clocks.summary(t_wall0, t_wall1),
     }
+    if graph is not None:
+        line["graph"] = graph
     if world == 1 and not a.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(inp, a.cpu_anchors)
     print(json.dumps(line), flush=True)
@@ -702,6 +737,8 @@ def main():
     ap.add_argument("--ref-anchors", type=int, default=300,
                     help="anchors per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the step captured in a CUDA graph (without an L2 flush)")
     ap.add_argument("--l2", choices=["auto", "flush", "none"], default="auto",
                     help="L2 flush before every step: auto = when the feature map is under twice the L2 size")
     ap.add_argument("--no-bin-overlap", action="store_true",
