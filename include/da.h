@@ -184,8 +184,9 @@ da_status da_backward(const da_dims *dims,
  *       the binned path (a workspace); without one the call returns
  *       DA_ERR_WORKSPACE. The corner contributions of every feature row are
  *       put in a fixed order (by sample and corner) before they are summed.
- *       This costs four more kernels and a few percent of the backward's
- *       time, more when many samples crowd a few pixels.
+ *       This costs four more kernels: about a sixth more backward time
+ *       at the 6-camera Sparse4D training shape, more when many samples
+ *       crowd a few pixels.
  *
  * Other arguments are those of da_backward. Unknown flags give
  * DA_ERR_SHAPE. da_backward(...) is da_backward_ex(..., 0, stream). With
