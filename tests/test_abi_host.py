@@ -296,3 +296,29 @@ def test_binning_entry_validation(lib):
     assert bl.da_backward_bin(d, ss, ls, FAKE, FAKE, 16, 0, None) == 6  # workspace too small
     # READY without a workspace
     assert bl.da_backward_ex(d, FAKE, ss, ls, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 0, 2, None) == 6
+
+
+def test_last_error_is_per_thread(lib):
+    """da_last_error() reports the calling thread's own last failure: threads
+    that fail at the same time with different sizes each read their own
+    message (ctypes releases the GIL during the calls, so they interleave)."""
+    import threading
+    bad = []
+
+    def worker(i):
+        rows = -(1000 + i)
+        d = _dims(num_feat_rows=rows)
+        for _ in range(300):
+            if _fwd(lib, d) != DA_ERR_SHAPE:
+                bad.append((i, "status"))
+                return
+            if str(rows).encode() not in lib.da_last_error():
+                bad.append((i, lib.da_last_error()))
+                return
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(8)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not bad, bad[:3]

@@ -360,3 +360,40 @@ def test_random_shapes(da, i):
         if path == "binned" and not binned_supported(c["C"], c["G"]):
             continue
         _compare(inp, _run_gpu(da, inp, path=path), ref)
+
+
+def test_concurrent_calls_on_two_streams(da):
+    """Calls on different streams may run at the same time (da.h). Two
+    different problems, each with its own workspace, are enqueued alternately
+    on two streams with no synchronisation between them; every output equals
+    the same call made alone (deterministic backward, so bit for bit)."""
+    dev = torch.device("cuda")
+    cases = [_custom(60, [[(12, 14), (6, 7)], [(9, 9), (3, 3)]], 2, 64, 2, 40, 9),
+             da_inputs.make_inputs(da_inputs.small_variant("sp4d_train", batch=2, num_anchors=50))]
+
+    def run(inp, stream):
+        feat, loc, w, go = (t.to(dev) for t in (inp.feat, inp.loc, inp.weights, inp.grad_out))
+        out = da.da_forward(feat, inp.spatial_shape, inp.level_start_index, loc, w, stream=stream)
+        d = da._dims(feat, da._host_i32(inp.spatial_shape), loc, w)
+        ws = torch.empty(max(da.backward_workspace_size(d), 256), dtype=torch.uint8, device=dev)
+        grads = da.da_backward(feat, inp.spatial_shape, inp.level_start_index, loc, w, go, stream=stream,
+                               path="binned", workspace=ws, deterministic=True)
+        return [out, *grads], (feat, loc, w, go, ws)
+
+    alone = []
+    for inp in cases:
+        res, _ = run(inp, torch.cuda.current_stream())
+        torch.cuda.synchronize()
+        alone.append([t.clone() for t in res])
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    together, keep = [], []
+    for rep in range(3):
+        for inp, s in zip(cases, streams):
+            with torch.cuda.stream(s):
+                res, bufs = run(inp, s)
+            together.append(res)
+            keep.append(bufs)  # inputs stay alive until the streams finish
+    torch.cuda.synchronize()
+    for i, res in enumerate(together):
+        for x, y in zip(res, alone[i % 2]):
+            assert torch.equal(x, y)
