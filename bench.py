@@ -18,8 +18,10 @@ time.
 
 Prints ONE JSON line on rank 0. It holds:
   * value: samples/s over all ranks;
-  * roofline: algorithmic bytes of the dominant call (da_backward) divided by
-    its CUDA-event time, against the measured HBM copy bandwidth;
+  * roofline: the step's algorithmic bytes (every tensor of the forward and
+    backward read or written once) divided by the step's CUDA-event time,
+    against the measured HBM copy bandwidth; with the forward's and the
+    backward's own figures under "parts";
   * e2e: the same metric with host buffers and host<->device copies inside
     the timed region;
   * cpu_baseline: the CPU oracle timed on a bounded sample of anchors;
@@ -471,14 +473,32 @@ def run_ours(a, wl):
         return
     peak, peak_kind = peaks()
 
-    if wl.backward:
-        dom_ms, dom_bytes, dom = statistics.mean(bwd_ms), bwd_bytes, "da_backward"
-        traffic = ncu_traffic(wl.name, f"da_backward[{a.bwd_path}]")
-    else:
-        dom_ms, dom_bytes, dom = statistics.mean(fwd_ms), fwd_bytes, "da_forward"
-        traffic = ncu_traffic(wl.name, "da_forward")
-    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+    # The roofline is the whole step's: every kernel of da_forward and
+    # da_backward (the side-stream binning included, since the step's events
+    # cover it), against the step's compulsory bytes.
     step_ms = ms_max / a.steps
+    step_bytes = fwd_bytes + (bwd_bytes if wl.backward else 0)
+    achieved = step_bytes / (step_ms / 1e3) / 1e9
+    if wl.backward:
+        t_f, t_b = ncu_traffic(wl.name, "da_forward"), ncu_traffic(wl.name, f"da_backward[{a.bwd_path}]")
+        traffic = t_f + t_b if t_f is not None and t_b is not None else None
+        step_kernel = (f"one step: da_forward + da_backward ({a.bwd_path} path), every kernel of both"
+                       + (", the binning on a side stream during the forward" if overlap else ""))
+    else:
+        traffic = ncu_traffic(wl.name, "da_forward")
+        step_kernel = "one step: da_forward"
+    fwd_mean = statistics.mean(fwd_ms)
+    parts = {"da_forward": {"ms": fwd_mean, "algorithmic_bytes": fwd_bytes,
+                            "frac": fwd_bytes / (fwd_mean / 1e3) / 1e9 / peak}}
+    if wl.backward:
+        bwd_mean = statistics.mean(bwd_ms)
+        # The binned path writes every grad_feat row once: no zero-fill.
+        bwd_own = bwd_bytes - (inp.feat.numel() * 4 if a.bwd_path != "scatter" else 0)
+        parts["da_backward"] = {
+            "ms": bwd_mean, "algorithmic_bytes": bwd_bytes, "frac": bwd_bytes / (bwd_mean / 1e3) / 1e9 / peak,
+            "algorithmic_bytes_own_path": bwd_own, "frac_own_path": bwd_own / (bwd_mean / 1e3) / 1e9 / peak,
+            "span": "from the end of the forward to the end of the backward"
+                    + ("; includes the part of the side-stream binning the forward did not hide" if overlap else "")}
     line = {
         "metric": METRIC, "value": value, "unit": "samples/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": step_ms,
@@ -497,11 +517,11 @@ def run_ours(a, wl):
         * inp.feat.element_size() / (step_ms / 1e3) / 1e9,
         "gbs_step": (fwd_bytes + (bwd_bytes if wl.backward else 0)) / (step_ms / 1e3) / 1e9,
         "fwd_ms": statistics.mean(fwd_ms), "bwd_ms": statistics.mean(bwd_ms) if bwd_ms else None,
-        "roofline": {"bound": "hbm", "kernel": dom + (f" ({a.bwd_path} path, all its kernels)"
-                                                       if dom == "da_backward" else ""),
+        "roofline": {"bound": "hbm", "kernel": step_kernel,
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
-                     "algorithmic_bytes": dom_bytes, "traffic": traffic},
+                     "algorithmic_bytes": step_bytes, "traffic": traffic,
+                     "parts": parts},
         "e2e": e2e,
         "gpu_launches": a.steps * (1 + (BWD_LAUNCHES[a.bwd_path] if wl.backward else 0)),
         "bwd_path": a.bwd_path,
@@ -750,6 +770,9 @@ def main():
                          "warpaffine: the frame preprocessing")
     ap.add_argument("--feat-dtype", choices=["f32", "bf16", "f16"], default=None,
                     help="override the workload's feature type (--op fused)")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (smaller cases for profiler captures; "
+                         "the headline uses the workload's own)")
     ap.add_argument("--bwd-path", choices=["binned", "binned-det", "scatter"], default=None,
                     help="backward algorithm (binned needs a device workspace; binned-det is its "
                          "deterministic mode). Default: binned for --op da, scatter for --op fused")
@@ -775,6 +798,8 @@ def main():
         run_fused(a, wl)
         return
     wl = da_inputs.WORKLOADS[a.workload]
+    if a.batch is not None:
+        wl = wl.replace(name=f"{wl.name}_b{a.batch}", batch=a.batch)
     if a.impl == "reference":
         run_reference(a, wl)
     else:

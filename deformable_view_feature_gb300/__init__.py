@@ -28,7 +28,7 @@ from . import build as _build
 
 __all__ = ["da_forward", "da_backward", "da_forward_fused", "da_backward_fused", "da_forward_projected",
            "da_backward_projected", "warpaffine_u8", "warpaffine_preprocess", "backward_workspace_size",
-           "da_backward_bin", "DeformableAggregationFunction", "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
+           "backward_path", "da_backward_bin", "DeformableAggregationFunction", "HostPipeline", "DaError", "library_path", "load_library", "da_version"]
 
 DA_F32, DA_BF16, DA_F16 = 0, 1, 2
 _STATUS = {0: "DA_OK", 1: "DA_ERR_NULL", 2: "DA_ERR_SHAPE", 3: "DA_ERR_ALIGN",
@@ -240,29 +240,50 @@ def da_backward_bin(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index, 
     return workspace
 
 
+# Samples per (anchor, group) up to which the scatter backward is the faster
+# one: its small-task kernels serve these shapes (the DCNv4 form's 3x3 points,
+# the tiny test shapes), and a binned pass costs more than it saves there.
+SMALL_TASK_SAMPLES = 16
+
+
+def backward_path(dims: DaDims) -> str:
+    """The backward algorithm path="auto" takes for these sizes: "binned"
+    when the binned kernels serve them (C a power of two in [8, 256], D a
+    multiple of 8, record indices within int32) and each (anchor, group) has
+    more than SMALL_TASK_SAMPLES samples; "scatter" otherwise."""
+    if dims.num_pts * dims.num_cams * dims.num_scales <= SMALL_TASK_SAMPLES:
+        return "scatter"
+    n = ctypes.c_size_t(0)
+    st = load_library().da_backward_workspace_size(ctypes.byref(dims), ctypes.byref(n))
+    return "binned" if st == 0 else "scatter"
+
+
 def da_backward(mc_ms_feat: torch.Tensor, spatial_shape, level_start_index,
                 sampling_location: torch.Tensor, weights: torch.Tensor, grad_out: torch.Tensor,
                 grad_feat: Optional[torch.Tensor] = None, grad_loc: Optional[torch.Tensor] = None,
-                grad_weight: Optional[torch.Tensor] = None, stream=None, path: str = "scatter",
+                grad_weight: Optional[torch.Tensor] = None, stream=None, path: str = "auto",
                 workspace: Optional[torch.Tensor] = None,
                 deterministic: bool = False,
                 binned_ready: bool = False) -> Tuple[torch.Tensor, torch.Tensor, torch.Tensor]:
     """Backward pass; returns (grad_feat fp32, grad_loc, grad_weight).
 
-    path="scatter" (default) needs no workspace and scatters grad_feat with
-    vector reductions; path="binned" sorts the corner contributions by
-    feature row in a device workspace (allocated through torch and reused, or
-    passed in) and writes every grad_feat row once. deterministic=True
-    (binned only) fixes the order of every row's contributions, so the
-    gradients are the same bit for bit on every run (DA_BACKWARD_DETERMINISTIC).
+    path="binned" sorts the corner contributions by feature row in a device
+    workspace (allocated through torch and reused, or passed in) and writes
+    every grad_feat row once; path="scatter" needs no workspace and scatters
+    grad_feat with vector reductions; path="auto" (default) takes the one
+    backward_path() names for the sizes. deterministic=True (binned only)
+    fixes the order of every row's contributions, so the gradients are the
+    same bit for bit on every run (DA_BACKWARD_DETERMINISTIC).
     """
+    lib = load_library()
+    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
+    d = _dims(mc_ms_feat, ss, sampling_location, weights)
+    if path == "auto":
+        path = "binned" if (deterministic or binned_ready) else backward_path(d)
     if (deterministic or binned_ready) and path != "binned":
         raise ValueError("deterministic=True and binned_ready=True need path='binned'")
     if binned_ready and workspace is None:
         raise ValueError("binned_ready=True needs the workspace da_backward_bin filled")
-    lib = load_library()
-    ss, ls = _host_i32(spatial_shape), _host_i32(level_start_index)
-    d = _dims(mc_ms_feat, ss, sampling_location, weights)
     dev = mc_ms_feat.device
     if tuple(grad_out.shape) != (d.batch, d.num_anchors, d.num_embeds) or grad_out.dtype != torch.float32:
         raise ValueError("grad_out must be float32 [B, A, C]")
@@ -569,7 +590,9 @@ def warpaffine_preprocess(src: torch.Tensor, d2i: torch.Tensor, dst_hw, fill: in
 
 class DeformableAggregationFunction(torch.autograd.Function):
     """Autograd wrapper with the argument list of Sparse4D's op:
-    (mc_ms_feat, spatial_shape, scale_start_index, sampling_location, weights)."""
+    (mc_ms_feat, spatial_shape, scale_start_index, sampling_location, weights).
+    The backward takes da_backward's path="auto": the binned algorithm at the
+    Sparse4D shapes, the scatter one for a few samples per anchor and group."""
 
     @staticmethod
     def forward(ctx, mc_ms_feat, spatial_shape, scale_start_index, sampling_location, weights):
@@ -586,7 +609,7 @@ class DeformableAggregationFunction(torch.autograd.Function):
         mc_ms_feat, sampling_location, weights = ctx.saved_tensors
         ss, ls = ctx.tables
         gf, gl, gw = da_backward(mc_ms_feat, ss, ls, sampling_location, weights,
-                                 grad_output.contiguous().float())
+                                 grad_output.contiguous().float(), path="auto")
         if mc_ms_feat.dtype != torch.float32:
             gf = gf.to(mc_ms_feat.dtype)
         return gf, None, None, gl, gw

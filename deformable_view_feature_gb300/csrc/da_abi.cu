@@ -11,14 +11,13 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
-#include <mutex>
 
 #include "da_internal.cuh"
 
 // Scratch of da_backward_noalloc: a fixed array in device memory, present
 // on every device that loads the library. In host code its name only stands
-// in for it; the device address comes from cudaGetSymbolAddress, looked up
-// once per device with that device current.
+// in for it; the device address comes from cudaGetSymbolAddress, called
+// with the device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DA_NOALLOC_SCRATCH_BYTES];
 
 namespace da {
@@ -327,25 +326,18 @@ da_status fused_binned_problem(const da_dims &d, const da::Problem &pb, da_dims 
     return DA_OK;
 }
 
-// Device address of g_noalloc_scratch on the current device.
-constexpr int kMaxDevices = 256;
-std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[kMaxDevices] = {};
-
+// Device address of g_noalloc_scratch in the current device's context. It is
+// looked up on every call rather than cached: a cached address would dangle
+// after cudaDeviceReset or any other teardown and re-creation of the
+// device's primary context, which loads the module (and the array) again at
+// a possibly different address. After the first call on a device the lookup
+// is a host-side table query.
 da_status noalloc_scratch(void **out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kMaxDevices) return fail(DA_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
-    std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
-        g_noalloc_ptr[dev] = p;
-    }
-    *out = g_noalloc_ptr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the built-in scratch");
+    *out = p;
     return DA_OK;
 }
 

@@ -123,17 +123,6 @@ __device__ __forceinline__ float2 bin_xy(const Problem &pb, int64_t pk)
     return *reinterpret_cast<const float2 *>(pb.loc + pk * 2);
 }
 
-// Weight of sample sid (G = 1 in the fused rewrite) for group g.
-template <bool FUSED>
-__device__ __forceinline__ float bin_weight(const Problem &pb, int sid, int g)
-{
-    if constexpr (FUSED) {
-        const int pk = static_cast<int>(pb.div_S.div(sid));
-        return __ldg(&pb.loc[static_cast<int64_t>(pk) * (2 + pb.S) + 2 + (sid - pk * pb.S)]);
-    }
-    return __ldg(&pb.weights[static_cast<int64_t>(sid) * pb.G + g]);
-}
-
 // Shared-memory offsets of the small maps of camera k (-1: counted globally).
 __device__ __forceinline__ void small_map_offsets(const Problem &pb, const MapInfo *maps_s, int k, int *hoff,
                                                   int &nsmall, int gs)
@@ -542,205 +531,6 @@ __global__ void __launch_bounds__(1024) sort_long_rows_kernel(const Problem pb, 
     }
 }
 
-// ---------------------------------------------------------------- 4. pull
-
-// Sum d[0..3] over the L lanes of one group, as in the gather kernels: each
-// halving step sends half of the values still held. The lane left holding
-// record u's sum stores it to dst[u * stride] when u < nvalid.
-template <int L>
-__device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, int nvalid, float *dst,
-                                                int stride)
-{
-    if constexpr (L >= 4) {
-        const bool hA = (sub & (L / 2)) != 0;
-        float a0 = hA ? d[2] : d[0], a1 = hA ? d[3] : d[1];
-        const float s0 = hA ? d[0] : d[2], s1 = hA ? d[1] : d[3];
-        a0 += __shfl_xor_sync(0xffffffffu, s0, L / 2);
-        a1 += __shfl_xor_sync(0xffffffffu, s1, L / 2);
-        const bool hB = (sub & (L / 4)) != 0;
-        float r = hB ? a1 : a0;
-        const float t = hB ? a0 : a1;
-        r += __shfl_xor_sync(0xffffffffu, t, L / 4);
-#pragma unroll
-        for (int m = L / 8; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
-        const int u = (hA ? 2 : 0) + (hB ? 1 : 0);
-        if ((sub & (L / 4 - 1)) == 0 && u < nvalid) dst[u * stride] = r;
-    } else if constexpr (L == 2) {
-        const bool h = (sub & 1) != 0;
-        float a0 = h ? d[2] : d[0], a1 = h ? d[3] : d[1];
-        const float s0 = h ? d[0] : d[2], s1 = h ? d[1] : d[3];
-        a0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-        a1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-        const int u0 = h ? 2 : 0;
-        if (u0 < nvalid) dst[u0 * stride] = a0;
-        if (u0 + 1 < nvalid) dst[(u0 + 1) * stride] = a1;
-    } else {
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (u < nvalid) dst[u * stride] = d[u];
-    }
-}
-
-// Eight feature values of one lane, widened to fp32.
-template <typename T>
-__device__ __forceinline__ void load_feat8(const void *p, float (&v)[8]);
-
-template <>
-__device__ __forceinline__ void load_feat8<float>(const void *p, float (&v)[8])
-{
-    const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
-    const float4 c = __ldg(reinterpret_cast<const float4 *>(p) + 1);
-    v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-    v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
-}
-
-template <>
-__device__ __forceinline__ void load_feat8<Bf16Tag>(const void *p, float (&v)[8])
-{
-    Chunk<Bf16Tag>::unpack(__ldg(reinterpret_cast<const uint4 *>(p)), v);
-}
-
-template <>
-__device__ __forceinline__ void load_feat8<F16Tag>(const void *p, float (&v)[8])
-{
-    Chunk<F16Tag>::unpack(__ldg(reinterpret_cast<const uint4 *>(p)), v);
-}
-
-struct PullArgs {
-    Problem pb;
-    const float *grad_out;
-    float *grad_feat;
-    BinArgs w;
-    int64_t row_begin, row_end;  // feature rows this launch covers
-};
-
-// 4 warps per CTA. The register-limited occupancy (32 warps per SM) is the
-// same for any CTA size, but rows hold from 1 to a few hundred records and a
-// CTA retires with its slowest warp: smaller CTAs free their slots sooner.
-// Training shape: 775 us with 128 threads, 805 with 256, 917 with 512
-// (787 with 64 and 781 with 32).
-constexpr int kPullThreads = 128;
-
-
-// One record's contribution to a lane's 8 channels: acc += tw * go, and the
-// lane's part of d = feat_row . go. Packed two-wide fp32 FMAs (each half
-// rounded on its own) halve the instruction count of this, the pull's
-// innermost step; the dot product runs as two partial sums (even and odd
-// channels) added at the end.
-__device__ __forceinline__ float record_fma2(const float2 (&v)[4], const float4 x, const float4 y, float tw,
-                                             float2 (&acc)[4])
-{
-    const float2 go[4] = {make_float2(x.x, x.y), make_float2(x.z, x.w), make_float2(y.x, y.y),
-                          make_float2(y.z, y.w)};
-    const float2 t = make_float2(tw, tw);
-    float2 dd = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        dd = __ffma2_rn(v[m], go[m], dd);
-        acc[m] = __ffma2_rn(t, go[m], acc[m]);
-    }
-    return dd.x + dd.y;
-}
-
-// LPR = C/8 lanes own one feature row, 8 channels each, all groups; a warp
-// holds 32/LPR rows. LPG = D/8 lanes hold one group. Records are taken four
-// at a time, so the loads of the four are independent and issue together.
-template <typename T, int LPR, int LPG, bool FUSED>
-__global__ void __launch_bounds__(kPullThreads) pull_kernel(const PullArgs args)
-{
-    constexpr int RPW = 32 / LPR;
-    constexpr int ESZ = sizeof(T) == 4 ? 4 : 2;
-    const Problem &pb = args.pb;
-    const BinArgs &w = args.w;
-    const int lane = threadIdx.x & 31;
-    const int q = lane / LPR, sub = lane % LPR;
-    const int g = sub / LPG, gsub = sub % LPG;
-    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5;
-    // Rows are taken from the end: each camera's block of rows ends with its
-    // coarsest maps, whose rows hold the most records (a sample lands in
-    // every scale, and a coarse map has few pixels). Taken last to first,
-    // the long rows start early and the launch ends on short rows, not on a
-    // tail of long ones (2 % of the backward at the 6-camera training shape).
-    const int64_t R = args.row_end - 1 - (warp_id * RPW + q);
-    const bool active = R >= args.row_begin;
-    const int b = active ? static_cast<int>(pb.div_rows.div(static_cast<uint32_t>(R))) : 0;
-    const int jb = active ? (R > 0 ? w.row_off[R - 1] : 0) : 0;
-    const int je = active ? w.row_off[R] : 0;
-    const int n = je - jb;
-
-    float v[8];
-    if (active) {
-        load_feat8<T>(static_cast<const char *>(pb.feat) + (R * pb.C + sub * 8) * ESZ, v);
-    } else {
-#pragma unroll
-        for (int m = 0; m < 8; ++m) v[m] = 0.f;
-    }
-    float2 v2[4], acc2[4];
-#pragma unroll
-    for (int m = 0; m < 4; ++m) {
-        v2[m] = make_float2(v[2 * m], v[2 * m + 1]);
-        acc2[m] = make_float2(0.f, 0.f);
-    }
-
-    int nmax = n;
-    if constexpr (RPW > 1) {
-#pragma unroll
-        for (int o = 16; o >= LPR; o >>= 1) nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
-    }
-    const float *go_b = args.grad_out + static_cast<int64_t>(b) * pb.A * pb.C + sub * 8;
-    const int abase = b * pb.A;
-    float *dp = w.dpix + static_cast<int64_t>(jb) * pb.G + g;
-
-    for (int k0 = 0; k0 < nmax; k0 += 4) {
-        // Every lane decodes the four records itself (the lanes of a row load
-        // the same addresses). The four record loads issue together, then the
-        // four weight loads, then the grad_out rows: three waits per batch of
-        // four records, not twelve.
-        int2 r[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) r[u] = (k0 + u < n) ? __ldg(&w.rec[jb + k0 + u]) : make_int2(0, 0);
-        float tw[4];
-        const float *gp[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int sid = r[u].x >> 2;
-            const int a = static_cast<int>(pb.div_PKS.div(sid)) - abase;
-            const bool valid = k0 + u < n;
-            const float wt = valid ? bin_weight<FUSED>(pb, sid, g) : 0.f;
-            tw[u] = __int_as_float(r[u].y) * wt;
-            gp[u] = go_b + static_cast<int64_t>(valid ? a : 0) * pb.C;
-        }
-        float d[4];
-        if (RPW == 1 && k0 + 4 <= n) {  // a full batch, the same for the whole warp
-            float4 x[4], y[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                x[u] = __ldg(reinterpret_cast<const float4 *>(gp[u]));
-                y[u] = __ldg(reinterpret_cast<const float4 *>(gp[u]) + 1);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) d[u] = record_fma2(v2, x[u], y[u], tw[u], acc2);
-        } else {
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
-                if (k0 + u < n) {
-                    x = __ldg(reinterpret_cast<const float4 *>(gp[u]));
-                    y = __ldg(reinterpret_cast<const float4 *>(gp[u]) + 1);
-                }
-                d[u] = record_fma2(v2, x, y, tw[u], acc2);
-            }
-        }
-        group_sum_store<LPG>(d, gsub, n - k0, dp + static_cast<int64_t>(k0) * pb.G, pb.G);
-    }
-
-    if (active) {
-        float4 *gf = reinterpret_cast<float4 *>(args.grad_feat + R * pb.C + sub * 8);
-        gf[0] = make_float4(acc2[0].x, acc2[0].y, acc2[1].x, acc2[1].y);
-        gf[1] = make_float4(acc2[2].x, acc2[2].y, acc2[3].x, acc2[3].y);
-    }
-}
-
 // ---------------------------------------------------------------- 5. epilogue
 
 __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const BinArgs w, float *grad_loc,
@@ -909,50 +699,6 @@ __global__ void __launch_bounds__(256) epilogue_fused_kernel(const Problem pb, c
 
 // ---------------------------------------------------------------- launch
 
-template <typename T, int LPR, int LPG>
-cudaError_t launch_pull(const PullArgs &pa, cudaStream_t st)
-{
-    if constexpr (LPG > LPR) {
-        return cudaErrorInvalidValue;
-    } else {
-        constexpr int RPW = 32 / LPR;
-        const int64_t warps = (pa.row_end - pa.row_begin + RPW - 1) / RPW;
-        const int64_t grid = (warps + kPullThreads / 32 - 1) / (kPullThreads / 32);
-        if (grid == 0) return cudaSuccess;
-        if (pa.pb.layout == kLayoutFused)
-            pull_kernel<T, LPR, LPG, true><<<static_cast<unsigned>(grid), kPullThreads, 0, st>>>(pa);
-        else
-            pull_kernel<T, LPR, LPG, false><<<static_cast<unsigned>(grid), kPullThreads, 0, st>>>(pa);
-        return cudaGetLastError();
-    }
-}
-
-template <typename T, int LPR>
-cudaError_t dispatch_lpg(const PullArgs &pa, cudaStream_t st)
-{
-    switch (pa.pb.D / 8) {
-        case 1: return launch_pull<T, LPR, 1>(pa, st);
-        case 2: return launch_pull<T, LPR, 2>(pa, st);
-        case 4: return launch_pull<T, LPR, 4>(pa, st);
-        case 8: return launch_pull<T, LPR, 8>(pa, st);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <typename T>
-cudaError_t dispatch_pull(const PullArgs &pa, cudaStream_t st)
-{
-    switch (pa.pb.C / 8) {
-        case 1: return dispatch_lpg<T, 1>(pa, st);
-        case 2: return dispatch_lpg<T, 2>(pa, st);
-        case 4: return dispatch_lpg<T, 4>(pa, st);
-        case 8: return dispatch_lpg<T, 8>(pa, st);
-        case 16: return dispatch_lpg<T, 16>(pa, st);
-        case 32: return dispatch_lpg<T, 32>(pa, st);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
 }  // namespace
 
 cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st, int stages)
@@ -1020,10 +766,7 @@ pull_stage:
     if (!(stages & kStagePull)) return cudaSuccess;
     // 4. grad_feat and d
     if (w.rows_total > 0) {
-        const PullArgs pa{pb, a.grad_out, a.grad_feat, w, 0, w.rows_total};
-        e = feat_dtype == DA_BF16  ? dispatch_pull<Bf16Tag>(pa, st)
-            : feat_dtype == DA_F16 ? dispatch_pull<F16Tag>(pa, st)
-                                   : dispatch_pull<float>(pa, st);
+        e = launch_pull(a, w, feat_dtype, st);
         if (e != cudaSuccess) return e;
     }
     // 5. grad_weight and grad_loc

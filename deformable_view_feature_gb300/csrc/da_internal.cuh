@@ -157,6 +157,9 @@ constexpr int kStageBin = 1, kStagePull = 2, kStageAll = 3;
 cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st,
                                    int stages = kStageAll);
 cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st);
+// The pull step of the binned backward (da_pull.cu): grad_feat, and d of
+// every record and group in dpix.
+cudaError_t launch_pull(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st);
 // Chain rule of the projected layout: grad_logits and grad_keypoints from the
 // operator's grad_loc and grad_weight (pb holds keypoints, projection, image
 // size).
@@ -243,6 +246,19 @@ __device__ __forceinline__ void sample_xyw(const Problem &pb, int64_t ba, int g,
         xy = *reinterpret_cast<const float2 *>(pb.loc + locid * 2);
         w = pb.weights[(locid * pb.S + s) * pb.G + g];
     }
+}
+
+// Weight of sample sid (a sample of all groups) for group g in the binned
+// backward: weights[sid, g], or in the fused layout's rewrite (G = 1) the
+// entry 2 + s of the sample's location.
+template <bool FUSED>
+__device__ __forceinline__ float bin_weight(const Problem &pb, int sid, int g)
+{
+    if constexpr (FUSED) {
+        const int pk = static_cast<int>(pb.div_S.div(sid));
+        return __ldg(&pb.loc[static_cast<int64_t>(pk) * (2 + pb.S) + 2 + (sid - pk * pb.S)]);
+    }
+    return __ldg(&pb.weights[static_cast<int64_t>(sid) * pb.G + g]);
 }
 
 // Bilinear footprint of one sample. The steps are those of the page "Inside

@@ -1,0 +1,371 @@
+// Pull step of the binned backward of the deformable-aggregation operator:
+// grad_feat (the page "Inside Sparse4D's CUDA core", §4.1: every corner
+// adds w_i * grad_out * w to its feature row) computed row by row from the
+// corner contributions that the binning (da_backward_binned.cu) sorted by
+// feature row, together with d = feat_row . grad_out per record and group,
+// from which grad_weight and grad_loc follow.
+#include "da_internal.cuh"
+
+namespace da {
+
+namespace {
+
+// Sum d[0..3] over the L lanes of one group, as in the gather kernels: each
+// halving step sends half of the values still held. The lane left holding
+// record u's sum stores it to dst[u * stride] when u < nvalid.
+template <int L>
+__device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, int nvalid, float *dst,
+                                                int stride)
+{
+    if constexpr (L >= 4) {
+        const bool hA = (sub & (L / 2)) != 0;
+        float a0 = hA ? d[2] : d[0], a1 = hA ? d[3] : d[1];
+        const float s0 = hA ? d[0] : d[2], s1 = hA ? d[1] : d[3];
+        a0 += __shfl_xor_sync(0xffffffffu, s0, L / 2);
+        a1 += __shfl_xor_sync(0xffffffffu, s1, L / 2);
+        const bool hB = (sub & (L / 4)) != 0;
+        float r = hB ? a1 : a0;
+        const float t = hB ? a0 : a1;
+        r += __shfl_xor_sync(0xffffffffu, t, L / 4);
+#pragma unroll
+        for (int m = L / 8; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
+        const int u = (hA ? 2 : 0) + (hB ? 1 : 0);
+        if ((sub & (L / 4 - 1)) == 0 && u < nvalid) dst[u * stride] = r;
+    } else if constexpr (L == 2) {
+        const bool h = (sub & 1) != 0;
+        float a0 = h ? d[2] : d[0], a1 = h ? d[3] : d[1];
+        const float s0 = h ? d[0] : d[2], s1 = h ? d[1] : d[3];
+        a0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        a1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        const int u0 = h ? 2 : 0;
+        if (u0 < nvalid) dst[u0 * stride] = a0;
+        if (u0 + 1 < nvalid) dst[(u0 + 1) * stride] = a1;
+    } else {
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            if (u < nvalid) dst[u * stride] = d[u];
+    }
+}
+
+// 32 contiguous bytes (8 floats) at a 32-byte aligned address, in one
+// 256-bit read-only load (sm_100 and later).
+__device__ __forceinline__ void ldg_v8(const void *p, float4 &x, float4 &y)
+{
+    asm("ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+        : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w), "=f"(y.x), "=f"(y.y), "=f"(y.z), "=f"(y.w)
+        : "l"(p));
+}
+
+// 8 floats to a 32-byte aligned address in one 256-bit store.
+__device__ __forceinline__ void stg_v8(void *p, const float4 x, const float4 y)
+{
+    asm volatile("st.global.v8.f32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};"
+                 :
+                 : "l"(p), "f"(x.x), "f"(x.y), "f"(x.z), "f"(x.w), "f"(y.x), "f"(y.y), "f"(y.z), "f"(y.w)
+                 : "memory");
+}
+
+// The 8 floats at p: one 256-bit load when V8 (p 32-byte aligned), else two
+// 128-bit loads. With a lane's 8 channels contiguous and the lanes of a row
+// side by side, the 256-bit form reads a whole row segment in one warp-wide
+// instruction whose every 32-byte sector is fully used; the two 128-bit
+// loads each touch every sector of the segment half.
+template <bool V8>
+__device__ __forceinline__ void ldg_f32x8(const float *p, float4 &x, float4 &y)
+{
+    if constexpr (V8) {
+        ldg_v8(p, x, y);
+    } else {
+        x = __ldg(reinterpret_cast<const float4 *>(p));
+        y = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+    }
+}
+
+// Eight feature values of one lane, widened to fp32.
+template <typename T, bool V8>
+__device__ __forceinline__ void load_feat8(const void *p, float (&v)[8])
+{
+    if constexpr (sizeof(T) == 4) {
+        float4 a, c;
+        ldg_f32x8<V8>(static_cast<const float *>(p), a, c);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+    } else {
+        Chunk<T>::unpack(__ldg(reinterpret_cast<const uint4 *>(p)), v);
+    }
+}
+
+struct PullArgs {
+    Problem pb;
+    const float *grad_out;
+    float *grad_feat;
+    BinArgs w;
+    int64_t row_begin, row_end;  // feature rows this launch covers
+    int weights_v8;              // G == 8 and weights 32-byte aligned: one 256-bit load per sample
+};
+
+// 4 warps per CTA. The register-limited occupancy (32 warps per SM) is the
+// same for any CTA size, but rows hold from 1 to a few hundred records and a
+// CTA retires with its slowest warp: smaller CTAs free their slots sooner.
+// Training shape: 775 us with 128 threads, 805 with 256, 917 with 512
+// (787 with 64 and 781 with 32).
+constexpr int kPullThreads = 128;
+
+
+// One record's contribution to a lane's 8 channels: acc += tw * go, and the
+// lane's part of d = feat_row . go. Packed two-wide fp32 FMAs (each half
+// rounded on its own) halve the instruction count of this, the pull's
+// innermost step; the dot product runs as two partial sums (even and odd
+// channels) added at the end.
+__device__ __forceinline__ float record_fma2(const float2 (&v)[4], const float4 x, const float4 y, float tw,
+                                             float2 (&acc)[4])
+{
+    const float2 go[4] = {make_float2(x.x, x.y), make_float2(x.z, x.w), make_float2(y.x, y.y),
+                          make_float2(y.z, y.w)};
+    const float2 t = make_float2(tw, tw);
+    float2 dd = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        dd = __ffma2_rn(v[m], go[m], dd);
+        acc[m] = __ffma2_rn(t, go[m], acc[m]);
+    }
+    return dd.x + dd.y;
+}
+
+// Shared memory of one pull warp, per chunk: for each of its RPW rows, CH
+// records (see pull_kernel), each with
+//   meta  {anchor a of the record within its batch item, corner weight bits},
+//   wsm   the G weights of the record's sample, group-major: wsm[g][slot],
+//   dsm   d of every group, record-major: dsm[slot][g] (pitch G).
+// slot = row in warp * CH + record in chunk.
+__host__ __device__ inline size_t pull_smem_per_warp(int slots, int G)
+{
+    return static_cast<size_t>(slots) * (2 + 2 * static_cast<size_t>(G)) * 4;
+}
+
+// LPR = C/8 lanes own one feature row, 8 channels each, all groups; a warp
+// holds RPW = 32/LPR rows. LPG = D/8 lanes hold one group. The records of a
+// row are taken in chunks of CH = max(LPR, 4):
+//   1. each lane of the row decodes CH/LPR records of the chunk: the
+//      record, its anchor, its sample's G weights. The loads of one lane are
+//      independent of every other lane's, so the chunk costs one round trip
+//      of record loads and one of weight loads, and each record is decoded
+//      once instead of by every lane of the row. The results go to the
+//      warp's shared-memory table;
+//   2. the lanes walk the chunk four records at a time: shared-memory reads
+//      of the table, the four anchors' grad_out rows (independent loads that
+//      issue together), then acc += (w * w_i) * grad_out and the lane's part
+//      of d = feat_row . grad_out, summed over a group's lanes by shuffles
+//      into the table;
+//   3. each decoding lane stores the G values of d of its records as one
+//      contiguous row of dpix.
+// Slots past a row's last record hold anchor 0 and weight 0: their loads
+// are of a valid row and their products add zero, so the walk needs no
+// predicates.
+// V8: grad_out, grad_feat (and fp32 features) are 32-byte aligned, so each
+// lane moves its 8 channels with one 256-bit access.
+template <typename T, int LPR, int LPG, bool FUSED, bool V8>
+__global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs args)
+{
+    constexpr int RPW = 32 / LPR;
+    constexpr int CH = LPR >= 4 ? LPR : 4;
+    constexpr int RPL = CH / LPR;  // records each lane decodes per chunk
+    constexpr int SLOTS = RPW * CH;
+    constexpr int ESZ = sizeof(T) == 4 ? 4 : 2;
+    extern __shared__ __align__(16) unsigned char pull_smem[];
+    const Problem &pb = args.pb;
+    const BinArgs &w = args.w;
+    const int G = pb.G;
+    const int lane = threadIdx.x & 31;
+    const int q = lane / LPR, sub = lane % LPR;
+    const int g = sub / LPG, gsub = sub % LPG;
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5;
+    int2 *meta = reinterpret_cast<int2 *>(pull_smem + (threadIdx.x >> 5) * pull_smem_per_warp(SLOTS, G));
+    float *wsm = reinterpret_cast<float *>(meta + SLOTS);
+    float *dsm = wsm + SLOTS * G;
+    // Rows are taken from the end: each camera's block of rows ends with its
+    // coarsest maps, whose rows hold the most records (a sample lands in
+    // every scale, and a coarse map has few pixels). Taken last to first,
+    // the long rows start early and the launch ends on short rows, not on a
+    // tail of long ones (2 % of the backward at the 6-camera training shape).
+    // Consecutive rows go to the warps of one CTA: neighbouring pixels share
+    // samples, whose grad_out rows the CTA's warps then find in L1 (a
+    // footprint covers 2x2 pixels). Walking 2x2 pixel blocks one pixel after
+    // another in one warp instead measured slower (L1 hit rate 21 % against
+    // 38 %): the reuse comes from warps running side by side.
+    const int64_t R = args.row_end - 1 - (warp_id * RPW + q);
+    const bool active = R >= args.row_begin;
+    const int b = active ? static_cast<int>(pb.div_rows.div(static_cast<uint32_t>(R))) : 0;
+    const int jb = active ? (R > 0 ? w.row_off[R - 1] : 0) : 0;
+    const int je = active ? w.row_off[R] : 0;
+    const int n = je - jb;
+    const float *go_b = args.grad_out + static_cast<int64_t>(b) * pb.A * pb.C + sub * 8;
+    const int abase = b * pb.A;
+    const int row_slot = q * CH;
+
+    float v[8];
+    if (active) {
+        load_feat8<T, V8>(static_cast<const char *>(pb.feat) + (R * pb.C + sub * 8) * ESZ, v);
+    } else {
+#pragma unroll
+        for (int m = 0; m < 8; ++m) v[m] = 0.f;
+    }
+    float2 v2[4], acc2[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        v2[m] = make_float2(v[2 * m], v[2 * m + 1]);
+        acc2[m] = make_float2(0.f, 0.f);
+    }
+
+    int nmax = n;
+    if constexpr (RPW > 1) {
+#pragma unroll
+        for (int o = 16; o >= LPR; o >>= 1) nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
+    }
+
+    for (int k0 = 0; k0 < nmax; k0 += CH) {
+        // 1. decode: lane sub takes records k0 + sub + LPR*j of its row.
+#pragma unroll
+        for (int j = 0; j < RPL; ++j) {
+            const int c = sub + LPR * j;
+            const bool valid = k0 + c < n;
+            const int2 r = valid ? __ldg(&w.rec[jb + k0 + c]) : make_int2(0, 0);
+            const int sid = r.x >> 2;
+            const int a = valid ? static_cast<int>(pb.div_PKS.div(sid)) - abase : 0;
+            meta[row_slot + c] = make_int2(a, r.y);
+            if constexpr (!FUSED) {
+                const float *wp = pb.weights + static_cast<int64_t>(sid) * G;
+                if (args.weights_v8) {
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+                    if (valid) ldg_v8(wp, x, y);
+                    const float wv[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+                    for (int gg = 0; gg < 8; ++gg) wsm[gg * SLOTS + row_slot + c] = wv[gg];
+                } else {
+                    for (int gg = 0; gg < G; ++gg) wsm[gg * SLOTS + row_slot + c] = valid ? __ldg(wp + gg) : 0.f;
+                }
+            } else {
+                wsm[row_slot + c] = valid ? bin_weight<true>(pb, sid, 0) : 0.f;
+            }
+        }
+        __syncwarp();
+        // 2. walk the chunk four records at a time.
+        const int nb = min(CH, nmax - k0);
+        const float *wrow = wsm + g * SLOTS + row_slot;
+        for (int u0 = 0; u0 < nb; u0 += 4) {
+            const int4 m01 = *reinterpret_cast<const int4 *>(meta + row_slot + u0);
+            const int4 m23 = *reinterpret_cast<const int4 *>(meta + row_slot + u0 + 2);
+            const float4 w4 = *reinterpret_cast<const float4 *>(wrow + u0);
+            const int an[4] = {m01.x, m01.z, m23.x, m23.z};
+            const float tw[4] = {__int_as_float(m01.y) * w4.x, __int_as_float(m01.w) * w4.y,
+                                 __int_as_float(m23.y) * w4.z, __int_as_float(m23.w) * w4.w};
+            float4 x[4], y[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) ldg_f32x8<V8>(go_b + static_cast<int64_t>(an[u]) * pb.C, x[u], y[u]);
+            float d[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) d[u] = record_fma2(v2, x[u], y[u], tw[u], acc2);
+            group_sum_store<LPG>(d, gsub, 4, dsm + (row_slot + u0) * G + g, G);
+        }
+        __syncwarp();
+        // 3. the decoding lanes store d of their records.
+#pragma unroll
+        for (int j = 0; j < RPL; ++j) {
+            const int c = sub + LPR * j;
+            if (k0 + c >= n) continue;
+            const float *src = dsm + (row_slot + c) * G;
+            float *dst = w.dpix + static_cast<int64_t>(jb + k0 + c) * G;
+            if (G == 8) {  // dpix rows are 32 bytes and the workspace 256-byte aligned
+                stg_v8(dst, *reinterpret_cast<const float4 *>(src), *reinterpret_cast<const float4 *>(src + 4));
+            } else if ((G & 3) == 0) {
+                for (int gg = 0; gg < G; gg += 4)
+                    *reinterpret_cast<float4 *>(dst + gg) = *reinterpret_cast<const float4 *>(src + gg);
+            } else {
+                for (int gg = 0; gg < G; ++gg) dst[gg] = src[gg];
+            }
+        }
+        __syncwarp();
+    }
+
+    if (active) {
+        const float4 a0 = make_float4(acc2[0].x, acc2[0].y, acc2[1].x, acc2[1].y);
+        const float4 a1 = make_float4(acc2[2].x, acc2[2].y, acc2[3].x, acc2[3].y);
+        float *gf = args.grad_feat + R * pb.C + sub * 8;
+        if constexpr (V8) {
+            stg_v8(gf, a0, a1);
+        } else {
+            reinterpret_cast<float4 *>(gf)[0] = a0;
+            reinterpret_cast<float4 *>(gf)[1] = a1;
+        }
+    }
+}
+
+template <typename T, int LPR, int LPG>
+cudaError_t launch_pull_kernel(const PullArgs &pa, cudaStream_t st)
+{
+    if constexpr (LPG > LPR) {
+        return cudaErrorInvalidValue;
+    } else {
+        constexpr int RPW = 32 / LPR;
+        const int64_t warps = (pa.row_end - pa.row_begin + RPW - 1) / RPW;
+        const int64_t grid = (warps + kPullThreads / 32 - 1) / (kPullThreads / 32);
+        if (grid == 0) return cudaSuccess;
+        // 256-bit accesses need 32-byte alignment of every row segment: rows
+        // are C*4 >= 32 bytes of fp32 (grad_out, grad_feat) or C*elem bytes of
+        // features (a 16-byte load per lane when 16-bit), so the base
+        // addresses decide.
+        const bool v8 = aligned(pa.grad_out, 32) && aligned(pa.grad_feat, 32) &&
+                        (sizeof(T) != 4 || aligned(pa.pb.feat, 32));
+        PullArgs p = pa;
+        p.weights_v8 = pa.pb.layout != kLayoutFused && pa.pb.G == 8 && aligned(pa.pb.weights, 32);
+        constexpr int CH = LPR >= 4 ? LPR : 4;
+        const size_t smem = pull_smem_per_warp(RPW * CH, pa.pb.G) * (kPullThreads / 32);
+        const dim3 g(static_cast<unsigned>(grid));
+        if (pa.pb.layout == kLayoutFused) {
+            if (v8) pull_kernel<T, LPR, LPG, true, true><<<g, kPullThreads, smem, st>>>(p);
+            else pull_kernel<T, LPR, LPG, true, false><<<g, kPullThreads, smem, st>>>(p);
+        } else {
+            if (v8) pull_kernel<T, LPR, LPG, false, true><<<g, kPullThreads, smem, st>>>(p);
+            else pull_kernel<T, LPR, LPG, false, false><<<g, kPullThreads, smem, st>>>(p);
+        }
+        return cudaGetLastError();
+    }
+}
+
+template <typename T, int LPR>
+cudaError_t dispatch_lpg(const PullArgs &pa, cudaStream_t st)
+{
+    switch (pa.pb.D / 8) {
+        case 1: return launch_pull_kernel<T, LPR, 1>(pa, st);
+        case 2: return launch_pull_kernel<T, LPR, 2>(pa, st);
+        case 4: return launch_pull_kernel<T, LPR, 4>(pa, st);
+        case 8: return launch_pull_kernel<T, LPR, 8>(pa, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t dispatch_pull(const PullArgs &pa, cudaStream_t st)
+{
+    switch (pa.pb.C / 8) {
+        case 1: return dispatch_lpg<T, 1>(pa, st);
+        case 2: return dispatch_lpg<T, 2>(pa, st);
+        case 4: return dispatch_lpg<T, 4>(pa, st);
+        case 8: return dispatch_lpg<T, 8>(pa, st);
+        case 16: return dispatch_lpg<T, 16>(pa, st);
+        case 32: return dispatch_lpg<T, 32>(pa, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pull(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st)
+{
+    const PullArgs pa{a.pb, a.grad_out, a.grad_feat, w, 0, w.rows_total, 0};
+    return feat_dtype == DA_BF16  ? dispatch_pull<Bf16Tag>(pa, st)
+           : feat_dtype == DA_F16 ? dispatch_pull<F16Tag>(pa, st)
+                                  : dispatch_pull<float>(pa, st);
+}
+
+}  // namespace da

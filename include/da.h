@@ -384,9 +384,12 @@ da_status da_backward_bin(const da_dims *dims,
  * Arguments, layouts and results are those of da_backward. Rules:
  *   - The scratch array exists once per device that loads the library and is
  *     held until the process exits.
- *   - The first call on a device looks up the array's device address (a
- *     one-time set-up per device). Make that first call before any stream
- *     capture.
+ *   - Every call looks up the array's device address in the current
+ *     context. The first call on a device may also load the library's device
+ *     code there (a one-time set-up per device): make that first call before
+ *     any stream capture. Because the address is not cached, a device reset
+ *     between calls is safe: the next call finds the array where the new
+ *     context put it (its contents start over).
  *   - Problems whose workspace (da_backward_workspace_size) exceeds
  *     DA_NOALLOC_SCRATCH_BYTES are rejected with DA_ERR_WORKSPACE. The limit
  *     fits e.g. the 6-camera Sparse4D shape at B = 1 (about 50 MB); the

@@ -77,6 +77,43 @@ def violations(gpu: np.ndarray, ref: np.ndarray, rtol: float, atol, name: str = 
 
 U32 = 2.0 ** -24
 
+# Share of a tensor's elements allowed outside the plain rtol/atol bound that
+# pass only through the kappa*u*M term (the first sp4d_train run had 89 of
+# 842,400 grad_loc elements there, 1.1e-4 of them), with a floor for small
+# tensors.
+PLAIN_EXCESS_SHARE = 5e-4
+PLAIN_EXCESS_FLOOR = 8
+
+
+def plain_excess_cap(size: int) -> int:
+    return max(PLAIN_EXCESS_FLOOR, int(PLAIN_EXCESS_SHARE * size))
+
+
+def plain_bound_excess(gpu: np.ndarray, ref: np.ndarray, rtol: float, atol: float, name: str = "") -> int:
+    """Number of elements outside the plain |g-r| <= rtol*|r| + atol bound
+    (before the kappa*u*M term); printed so a test log shows it."""
+    n, msg = violations(gpu, ref, rtol, atol, name)
+    print(f"{name}: {n}/{np.size(ref)} outside the plain bound" + (f" ({msg})" if n else ""))
+    return n
+
+
+def widened_violations(gpu: np.ndarray, ref: np.ndarray, rtol: float, atol: float, term, name: str = ""):
+    """Messages for an output whose bound carries the kappa*u*M term `term`
+    (an array of ref's size, or None for none): elements outside
+    rtol*|ref| + atol + term, and more elements than plain_excess_cap
+    outside the plain rtol*|ref| + atol bound."""
+    msgs = []
+    if term is not None:
+        n_plain = plain_bound_excess(gpu, ref, rtol, atol, name)
+        cap = plain_excess_cap(np.size(ref))
+        if n_plain > cap:
+            msgs.append(f"{name}: {n_plain} elements pass only through the kappa*u*M term (cap {cap})")
+        atol = atol + np.reshape(term, np.shape(ref))
+    n, msg = violations(gpu, ref, rtol, atol, name)
+    if n:
+        msgs.append(msg)
+    return msgs
+
 
 def conditioning_atol(inp, kind_names=("grad_loc", "grad_weight")):
     """Per-element kappa*u*M for grad_loc, grad_weight and, when asked,

@@ -18,7 +18,7 @@ import torch
 
 import da_inputs
 import oracle
-from parity_util import TOL, conditioning_atol, to_np, violations
+from parity_util import TOL, conditioning_atol, to_np, violations, widened_violations
 
 pytestmark = pytest.mark.gpu
 U32 = 2.0 ** -24
@@ -87,11 +87,7 @@ def _check(inp, got):
     msgs = []
     for name in ("out", "grad_feat", "grad_loc", "grad_weight"):
         rtol, atol = TOL[inp.wl.feat_dtype][name]
-        if name in extra:
-            atol = atol + extra[name].reshape(ref[name].shape)
-        n, msg = violations(got[name], ref[name], rtol, atol, name)
-        if n:
-            msgs.append(msg)
+        msgs += widened_violations(got[name], ref[name], rtol, atol, extra.get(name), name)
     gkp, glg = oracle.projected_chain(kp, pr, inp.image_w, inp.image_h, got["weights"], got["grad_loc"],
                                       got["grad_weight"])
     glg_bound, kp_bound = _chain_bounds(inp, got)
