@@ -215,7 +215,6 @@ da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const floa
         w.row_off = reinterpret_cast<int32_t *>(ws + L.off_row_off);
         w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
         w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
-        w.pos4 = reinterpret_cast<int32_t *>(ws + L.off_pos4);
         w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
         w.rows_total = L.rows_total;
         w.nsid = L.nsid;
@@ -449,7 +448,6 @@ da_status da_backward_bin(const da_dims *dims, const int32_t *spatial_shape, con
     w.row_off = reinterpret_cast<int32_t *>(ws + L.off_row_off);
     w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
     w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
-    w.pos4 = reinterpret_cast<int32_t *>(ws + L.off_pos4);
     w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
     w.rows_total = L.rows_total;
     w.nsid = L.nsid;

@@ -18,20 +18,20 @@
 //   3. fill    the same threads claim their slots (one global range per
 //              touched row per CTA for the small maps, one global atomic per
 //              corner for the large ones) and store the record
-//              {sample*4 + corner, corner weight} (one 8-byte store), plus
-//              the slot of each corner (pos4);
-//   4. pull    C/8 lanes own one feature row (8 channels each, all groups;
-//              a whole warp when C = 256). Per record they read the
-//              anchor's grad_out row, accumulate (w * w_i) * grad_out into
-//              the row's grad_feat, and form d = feat_row . grad_out per
-//              group (a shuffle sum over the D/8 lanes of a group). The
+//              {sample*4 + corner, corner weight} (one 8-byte store);
+//   4. pull    (da_pull.cu) C/8 lanes own one feature row (8 channels each,
+//              all groups; a whole warp when C = 256). Per record they read
+//              the anchor's grad_out row, accumulate (w * w_i) * grad_out
+//              into the row's grad_feat, and form d = feat_row . grad_out
+//              per group (a shuffle sum over the D/8 lanes of a group). The
 //              grad_feat row is stored once (no zero-fill); the G values of
-//              d go to dpix as one contiguous row per record;
-//   5. epilogue one warp per location (b, a, p, k): its lanes take the
-//              (s, g) samples, gather the four corners' d through pos4, and
-//              form grad_weight = sum w_i d_i and the two grad_loc sums,
-//              reduced by shuffles. Every output has one owner, so there
-//              are no atomics.
+//              d go to dpix at the record's key, so the four corners of a
+//              sample land side by side;
+//   5. epilogue one lane per (location, scale) (or one warp per location):
+//              it reads the four corners' d of its samples as one
+//              contiguous run, and forms grad_weight = sum w_i d_i and the
+//              two grad_loc sums, reduced by shuffles. Every output has one
+//              owner, so there are no atomics.
 #include <algorithm>
 #include <climits>
 
@@ -59,8 +59,6 @@ BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, i
     o = align256(o + static_cast<size_t>(L.ntiles + 4) * 4);
     L.off_rec = o;
     o = align256(o + static_cast<size_t>(L.ncap) * 8);
-    L.off_pos4 = o;
-    o = align256(o + static_cast<size_t>(L.nsid) * 16);
     L.off_dpix = o;
     o = align256(o + static_cast<size_t>(L.ncap) * static_cast<size_t>(G) * 4);
     // A row holds more than 8 (128, 2048) records in at most ncap/9
@@ -273,7 +271,6 @@ __global__ void __launch_bounds__(256) scan_add_kernel(int32_t *data, const int3
 // shared memory, claims one contiguous range per touched row with a single
 // global atomic, and then hands out slots inside the range with shared
 // atomics. Every corner of a large map claims its slot with a global atomic.
-// pos4 is stored view-major: index ((b*K + k)*A*P + a*P + p)*S + s.
 template <bool FUSED>
 __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb, const BinArgs w,
                                                                 int ctas_per_view)
@@ -320,7 +317,6 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
     }
     __syncthreads();
     if (!c.valid) return;
-    const int64_t vsid0 = ((static_cast<int64_t>(c.b) * pb.K + c.k) * pb.A * pb.P + c.q) * pb.S;
     for (int s = 0; s < pb.S; ++s) {
         const MapInfo m = maps_s[c.k * pb.S + s];
         Footprint f;
@@ -338,7 +334,6 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
             if (pos[cc] >= 0) w.rec[pos[cc]] = make_int2(static_cast<int>(sid) * 4 + cc, __float_as_int(f.cw[cc]));
-        reinterpret_cast<int4 *>(w.pos4)[vsid0 + s] = make_int4(pos[0], pos[1], pos[2], pos[3]);
     }
 }
 
@@ -348,7 +343,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
 // row's records, and with it the rounding of the pull's sums, changes from
 // run to run. In deterministic mode the records of every row are put in
 // ascending order of their first field (sample id * 4 + corner, unique per
-// record) before the pull, and pos4 is rewritten to match. The sum over a
+// record) before the pull. The sum over a
 // row then always runs in the same order, so grad_feat (and everything
 // computed from it) is the same bit for bit on every run.
 //
@@ -365,20 +360,6 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
 constexpr int kSortThreads = 256;
 constexpr int kSortWarpMax = 128;
 constexpr int kSortSmemMax = 2048;
-
-// Index into pos4 (int32 entries) of record key sid*4 + corner.
-__device__ __forceinline__ int64_t pos4_entry(const Problem &pb, int key)
-{
-    const int sid = key >> 2;
-    const int pk = static_cast<int>(pb.div_S.div(sid));
-    const int s = sid - pk * pb.S;
-    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
-    const int k = pk - bap * pb.K;
-    const int bq = static_cast<int>(pb.div_P.div(bap));
-    const int b = static_cast<int>(pb.div_A.div(bq));
-    const int q = bap - b * pb.A * pb.P;
-    return (((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * pb.S + s) * 4 + (key & 3);
-}
 
 __device__ __forceinline__ int row_begin(const BinArgs &w, int64_t r) { return r > 0 ? w.row_off[r - 1] : 0; }
 
@@ -415,10 +396,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_short_rows_kernel(const Pro
         int rank = 0;
 #pragma unroll
         for (int v = 0; v < 8; ++v) rank += (e[v].x < e[u].x) ? 1 : 0;  // padding keys are never smaller
-        if (rank != u) {
-            w.rec[jb + rank] = e[u];
-            w.pos4[pos4_entry(pb, e[u].x)] = jb + rank;
-        }
+        if (rank != u) w.rec[jb + rank] = e[u];
     }
 }
 
@@ -440,10 +418,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_warp_rows_kernel(const Prob
             const int2 e = buf[warp][j];
             int rank = 0;
             for (int v = 0; v < n; ++v) rank += (buf[warp][v].x < e.x) ? 1 : 0;
-            if (rank != j) {
-                w.rec[jb + rank] = e;
-                w.pos4[pos4_entry(pb, e.x)] = jb + rank;
-            }
+            if (rank != j) w.rec[jb + rank] = e;
         }
         __syncwarp();
     }
@@ -505,11 +480,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_cta_rows_kernel(const Probl
         for (int j = threadIdx.x; j < n; j += kSortThreads) buf[j] = w.rec[jb + j];
         __syncthreads();
         block_bitonic_sort(static_cast<int2 *>(buf), n);
-        for (int j = threadIdx.x; j < n; j += kSortThreads) {
-            const int2 e = buf[j];
-            w.rec[jb + j] = e;
-            w.pos4[pos4_entry(pb, e.x)] = jb + j;
-        }
+        for (int j = threadIdx.x; j < n; j += kSortThreads) w.rec[jb + j] = buf[j];
         __syncthreads();
     }
 }
@@ -526,7 +497,6 @@ __global__ void __launch_bounds__(1024) sort_long_rows_kernel(const Problem pb, 
         const int jb = row_begin(w, r);
         const int n = w.row_off[r] - jb;
         block_bitonic_sort(w.rec + jb, n);
-        for (int j = threadIdx.x; j < n; j += blockDim.x) w.pos4[pos4_entry(pb, w.rec[jb + j].x)] = jb + j;
         __syncthreads();
     }
 }
@@ -543,12 +513,7 @@ __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const B
     const int lane = threadIdx.x & 31;
     if (pk64 >= pk_end) return;  // whole warps leave together
     const int pk = static_cast<int>(pk64);
-    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
-    const int k = pk - bap * pb.K;
-    const int bq = static_cast<int>(pb.div_P.div(bap));  // b*A + a
-    const int b = static_cast<int>(pb.div_A.div(bq));
-    const int q = bap - b * pb.A * pb.P;  // a*P + p
-    const int64_t vsid0 = ((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * pb.S;
+    const int k = pk - static_cast<int>(pb.div_K.div(pk)) * pb.K;
     const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + pk64 * 2);
     float gx = 0.f, gy = 0.f;
     const int sg = pb.S * pb.G;
@@ -560,12 +525,11 @@ __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const B
         Footprint f;
         footprint(xy.x, xy.y, m, f);
         const float wt = pb.weights[sid * pb.G + g];
-        const int4 pos = reinterpret_cast<const int4 *>(w.pos4)[vsid0 + s];
-        const float *dp = w.dpix + g;  // row of record j: dpix[j*G .. j*G + G)
-        const float d0 = pos.x >= 0 ? dp[static_cast<int64_t>(pos.x) * pb.G] : 0.f;
-        const float d1 = pos.y >= 0 ? dp[static_cast<int64_t>(pos.y) * pb.G] : 0.f;
-        const float d2 = pos.z >= 0 ? dp[static_cast<int64_t>(pos.z) * pb.G] : 0.f;
-        const float d3 = pos.w >= 0 ? dp[static_cast<int64_t>(pos.w) * pb.G] : 0.f;
+        const float *dp = w.dpix + sid * 4 * pb.G + g;  // corner c at dp[c * G]
+        const float d0 = f.row[0] >= 0 ? dp[0] : 0.f;
+        const float d1 = f.row[1] >= 0 ? dp[pb.G] : 0.f;
+        const float d2 = f.row[2] >= 0 ? dp[2 * pb.G] : 0.f;
+        const float d3 = f.row[3] >= 0 ? dp[3 * pb.G] : 0.f;
         grad_weight[sid * pb.G + g] = f.cw[0] * d0 + f.cw[1] * d1 + f.cw[2] * d2 + f.cw[3] * d3;
         gx += static_cast<float>(m.W) * wt * (f.lh * (d3 - d2) + f.hh * (d1 - d0));
         gy += static_cast<float>(m.H) * wt * (f.lw * (d3 - d1) + f.hw * (d2 - d0));
@@ -583,8 +547,9 @@ __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const B
 
 // The same with one lane per (location, scale), carrying all G groups in
 // 16-byte vectors (G = 4 or 8, S dividing 32): a warp covers 32/S
-// locations. The weights of a sample, its grad_weight and each corner's d
-// are G contiguous floats, so every access is a 16- or 32-byte vector, and
+// locations. The weights of a sample, its grad_weight and its four corners'
+// d are 1 and 4 runs of G contiguous floats (the corners' side by side, the
+// lanes' samples consecutive), so every access is a 16-byte vector, and
 // the footprint and the bookkeeping run once per sample instead of once per
 // (sample, group). The S lanes of a location sum grad_loc with shuffles.
 template <int G>
@@ -603,19 +568,12 @@ __global__ void __launch_bounds__(256) epilogue_vec_kernel(const Problem pb, con
     // Lanes past the end run on the last location (whole locations, so the
     // shuffles stay within live lanes) and store nothing.
     const int pk = static_cast<int>(live ? pk64 : npk - 1);
-    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
-    const int k = pk - bap * pb.K;
-    const int bq = static_cast<int>(pb.div_P.div(bap));  // b*A + a
-    const int b = static_cast<int>(pb.div_A.div(bq));
-    const int q = bap - b * pb.A * pb.P;  // a*P + p
-    const int64_t vsid = ((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * S + s;
+    const int k = pk - static_cast<int>(pb.div_K.div(pk)) * pb.K;
     const int64_t sid = static_cast<int64_t>(pk) * S + s;
     const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + static_cast<int64_t>(pk) * 2);
     const MapInfo m = maps_s[k * S + s];
     Footprint f;
     footprint(xy.x, xy.y, m, f);
-    const int4 pos = reinterpret_cast<const int4 *>(w.pos4)[vsid];
-    const int pc[4] = {pos.x, pos.y, pos.z, pos.w};
     float wt[G], d[4][G];
 #pragma unroll
     for (int h = 0; h < G / 4; ++h) {
@@ -627,7 +585,7 @@ __global__ void __launch_bounds__(256) epilogue_vec_kernel(const Problem pb, con
 #pragma unroll
         for (int h = 0; h < G / 4; ++h) {
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (pc[c] >= 0) v = __ldg(reinterpret_cast<const float4 *>(w.dpix + static_cast<int64_t>(pc[c]) * G) + h);
+            if (f.row[c] >= 0) v = __ldg(reinterpret_cast<const float4 *>(w.dpix + (sid * 4 + c) * G) + h);
             d[c][4 * h] = v.x; d[c][4 * h + 1] = v.y; d[c][4 * h + 2] = v.z; d[c][4 * h + 3] = v.w;
         }
     }
@@ -668,12 +626,7 @@ __global__ void __launch_bounds__(256) epilogue_fused_kernel(const Problem pb, c
     const int64_t pk64 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (pk64 >= npk) return;
     const int pk = static_cast<int>(pk64);
-    const int bap = static_cast<int>(pb.div_K.div(pk));  // (b*A + a)*P + p
-    const int k = pk - bap * pb.K;
-    const int bq = static_cast<int>(pb.div_P.div(bap));  // b*A + a
-    const int b = static_cast<int>(pb.div_A.div(bq));
-    const int q = bap - b * pb.A * pb.P;  // a*P + p
-    const int64_t vsid0 = ((static_cast<int64_t>(b) * pb.K + k) * pb.A * pb.P + q) * pb.S;
+    const int k = pk - static_cast<int>(pb.div_K.div(pk)) * pb.K;
     const int E = 2 + pb.S;
     float *e = glw + pk64 * E;
     const float *le = pb.loc + pk64 * E;
@@ -684,11 +637,11 @@ __global__ void __launch_bounds__(256) epilogue_fused_kernel(const Problem pb, c
         Footprint f;
         footprint(x, y, m, f);
         const float wt = le[2 + s];
-        const int4 pos = reinterpret_cast<const int4 *>(w.pos4)[vsid0 + s];
-        const float d0 = pos.x >= 0 ? w.dpix[pos.x] : 0.f;
-        const float d1 = pos.y >= 0 ? w.dpix[pos.y] : 0.f;
-        const float d2 = pos.z >= 0 ? w.dpix[pos.z] : 0.f;
-        const float d3 = pos.w >= 0 ? w.dpix[pos.w] : 0.f;
+        const float *dp = w.dpix + (pk64 * pb.S + s) * 4;  // G = 1: corner c at dp[c]
+        const float d0 = f.row[0] >= 0 ? dp[0] : 0.f;
+        const float d1 = f.row[1] >= 0 ? dp[1] : 0.f;
+        const float d2 = f.row[2] >= 0 ? dp[2] : 0.f;
+        const float d3 = f.row[3] >= 0 ? dp[3] : 0.f;
         e[2 + s] = f.cw[0] * d0 + f.cw[1] * d1 + f.cw[2] * d2 + f.cw[3] * d3;
         gx += static_cast<float>(m.W) * wt * (f.lh * (d3 - d2) + f.hh * (d1 - d0));
         gy += static_cast<float>(m.H) * wt * (f.lw * (d3 - d1) + f.hw * (d2 - d0));

@@ -100,12 +100,13 @@ struct BwdArgs {
 //            sum, then (after the fill) the end of the row's record range.
 //            The tail holds the scan's total and the sort's list counters.
 //   tile_sum [ntiles + 4] int32: per-tile totals of the scan
-//   rec      [ncap] int2: {sample id * 4 + corner, corner weight bits},
-//            grouped by feature row; in deterministic mode sorted by the
-//            first field within each row
-//   pos4     [nsid * 4] int32: record index of each (sample, corner), or -1;
-//            samples in view-major order ((b*K + k)*A*P + a*P + p)*S + s
-//   dpix     [ncap * G] fp32: d = grad_out . feat of each (record, group)
+//   rec      [ncap] int2: {key = sample id * 4 + corner, corner weight bits},
+//            grouped by feature row; in deterministic mode sorted by key
+//            within each row
+//   dpix     [ncap * G] fp32: d = grad_out . feat of each (record, group),
+//            at row `key` of the record: the four corners of a sample are
+//            adjacent, in sample order. Entries of corners outside their
+//            map are never written (no record) and never read.
 //   lists    [cap_m + cap_s + cap_g] int32: rows the deterministic sort
 //            hands to a warp (9..128 records), a CTA with shared memory
 //            (129..2048) or a CTA working in global memory (more)
@@ -118,7 +119,7 @@ struct BinLayout {
     int64_t nsid;        // B*A*P*K*S
     int64_t ncap;        // 4 * nsid
     int64_t ntiles;
-    size_t off_row_off, off_tile_sum, off_rec, off_pos4, off_dpix, off_lists, bytes;
+    size_t off_row_off, off_tile_sum, off_rec, off_dpix, off_lists, bytes;
     // Capacities of the three row lists of the deterministic sort (rows
     // with more than 8, 128 and 2048 records).
     int64_t cap_m, cap_s, cap_g;
@@ -137,7 +138,6 @@ struct BinArgs {
     int32_t *row_off;
     int32_t *tile_sum;
     int2 *rec;
-    int32_t *pos4;
     float *dpix;
     int64_t rows_total, nsid, ncap, ntiles;
     // Deterministic mode: the row lists of the per-row sort, and their three

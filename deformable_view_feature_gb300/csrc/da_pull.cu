@@ -12,10 +12,15 @@ namespace {
 
 // Sum d[0..3] over the L lanes of one group, as in the gather kernels: each
 // halving step sends half of the values still held. The lane left holding
-// record u's sum stores it to dst[u * stride] when u < nvalid.
+// record u's sum stores it to base[key[u] * stride] when u < nvalid.
+__device__ __forceinline__ int pick4(const int (&k)[4], int u)
+{
+    return u == 0 ? k[0] : u == 1 ? k[1] : u == 2 ? k[2] : k[3];
+}
+
 template <int L>
-__device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, int nvalid, float *dst,
-                                                int stride)
+__device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, int nvalid, float *base,
+                                                const int (&key)[4], int stride)
 {
     if constexpr (L >= 4) {
         const bool hA = (sub & (L / 2)) != 0;
@@ -30,7 +35,7 @@ __device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, in
 #pragma unroll
         for (int m = L / 8; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
         const int u = (hA ? 2 : 0) + (hB ? 1 : 0);
-        if ((sub & (L / 4 - 1)) == 0 && u < nvalid) dst[u * stride] = r;
+        if ((sub & (L / 4 - 1)) == 0 && u < nvalid) base[static_cast<int64_t>(pick4(key, u)) * stride] = r;
     } else if constexpr (L == 2) {
         const bool h = (sub & 1) != 0;
         float a0 = h ? d[2] : d[0], a1 = h ? d[3] : d[1];
@@ -38,12 +43,12 @@ __device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, in
         a0 += __shfl_xor_sync(0xffffffffu, s0, 1);
         a1 += __shfl_xor_sync(0xffffffffu, s1, 1);
         const int u0 = h ? 2 : 0;
-        if (u0 < nvalid) dst[u0 * stride] = a0;
-        if (u0 + 1 < nvalid) dst[(u0 + 1) * stride] = a1;
+        if (u0 < nvalid) base[static_cast<int64_t>(pick4(key, u0)) * stride] = a0;
+        if (u0 + 1 < nvalid) base[static_cast<int64_t>(pick4(key, u0 + 1)) * stride] = a1;
     } else {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            if (u < nvalid) dst[u * stride] = d[u];
+            if (u < nvalid) base[static_cast<int64_t>(key[u]) * stride] = d[u];
     }
 }
 
@@ -135,12 +140,12 @@ __device__ __forceinline__ float record_fma2(const float2 (&v)[4], const float4 
 // Shared memory of one pull warp, per chunk: for each of its RPW rows, CH
 // records (see pull_kernel), each with
 //   meta  {anchor a of the record within its batch item, corner weight bits},
-//   wsm   the G weights of the record's sample, group-major: wsm[g][slot],
-//   dsm   d of every group, record-major: dsm[slot][g] (pitch G).
+//   ksm   the record's key (sample id * 4 + corner),
+//   wsm   the G weights of the record's sample, group-major: wsm[g][slot].
 // slot = row in warp * CH + record in chunk.
 __host__ __device__ inline size_t pull_smem_per_warp(int slots, int G)
 {
-    return static_cast<size_t>(slots) * (2 + 2 * static_cast<size_t>(G)) * 4;
+    return static_cast<size_t>(slots) * (3 + static_cast<size_t>(G)) * 4;
 }
 
 // LPR = C/8 lanes own one feature row, 8 channels each, all groups; a warp
@@ -155,10 +160,9 @@ __host__ __device__ inline size_t pull_smem_per_warp(int slots, int G)
 //   2. the lanes walk the chunk four records at a time: shared-memory reads
 //      of the table, the four anchors' grad_out rows (independent loads that
 //      issue together), then acc += (w * w_i) * grad_out and the lane's part
-//      of d = feat_row . grad_out, summed over a group's lanes by shuffles
-//      into the table;
-//   3. each decoding lane stores the G values of d of its records as one
-//      contiguous row of dpix.
+//      of d = feat_row . grad_out, summed over a group's lanes by shuffles;
+//      the lane left with a record's sum stores it to dpix at the record's
+//      key, next to the sample's other corners.
 // Slots past a row's last record hold anchor 0 and weight 0: their loads
 // are of a valid row and their products add zero, so the walk needs no
 // predicates.
@@ -181,8 +185,8 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
     const int g = sub / LPG, gsub = sub % LPG;
     const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5;
     int2 *meta = reinterpret_cast<int2 *>(pull_smem + (threadIdx.x >> 5) * pull_smem_per_warp(SLOTS, G));
-    float *wsm = reinterpret_cast<float *>(meta + SLOTS);
-    float *dsm = wsm + SLOTS * G;
+    int *ksm = reinterpret_cast<int *>(meta + SLOTS);
+    float *wsm = reinterpret_cast<float *>(ksm + SLOTS);
     // Rows are taken from the end: each camera's block of rows ends with its
     // coarsest maps, whose rows hold the most records (a sample lands in
     // every scale, and a coarse map has few pixels). Taken last to first,
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
             const int sid = r.x >> 2;
             const int a = valid ? static_cast<int>(pb.div_PKS.div(sid)) - abase : 0;
             meta[row_slot + c] = make_int2(a, r.y);
+            ksm[row_slot + c] = r.x;
             if constexpr (!FUSED) {
                 const float *wp = pb.weights + static_cast<int64_t>(sid) * G;
                 if (args.weights_v8) {
@@ -265,24 +270,9 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
             float d[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) d[u] = record_fma2(v2, x[u], y[u], tw[u], acc2);
-            group_sum_store<LPG>(d, gsub, 4, dsm + (row_slot + u0) * G + g, G);
-        }
-        __syncwarp();
-        // 3. the decoding lanes store d of their records.
-#pragma unroll
-        for (int j = 0; j < RPL; ++j) {
-            const int c = sub + LPR * j;
-            if (k0 + c >= n) continue;
-            const float *src = dsm + (row_slot + c) * G;
-            float *dst = w.dpix + static_cast<int64_t>(jb + k0 + c) * G;
-            if (G == 8) {  // dpix rows are 32 bytes and the workspace 256-byte aligned
-                stg_v8(dst, *reinterpret_cast<const float4 *>(src), *reinterpret_cast<const float4 *>(src + 4));
-            } else if ((G & 3) == 0) {
-                for (int gg = 0; gg < G; gg += 4)
-                    *reinterpret_cast<float4 *>(dst + gg) = *reinterpret_cast<const float4 *>(src + gg);
-            } else {
-                for (int gg = 0; gg < G; ++gg) dst[gg] = src[gg];
-            }
+            const int4 k4 = *reinterpret_cast<const int4 *>(ksm + row_slot + u0);
+            const int keys[4] = {k4.x, k4.y, k4.z, k4.w};
+            group_sum_store<LPG>(d, gsub, n - k0 - u0, w.dpix + g, keys, G);
         }
         __syncwarp();
     }

@@ -154,12 +154,12 @@ def test_workspace_size_and_errors(lib):
               num_pts=13, num_feat_rows=6 * 14960)
     assert lib.da_backward_workspace_size(ctypes.byref(d), ctypes.byref(n)) == DA_OK
     nsid = 6 * 900 * 13 * 6 * 4
-    # records (cid + weight), pos4, dpix for 8 groups: 4*nsid*(4+4) + 16*nsid + 4*nsid*8*4,
+    # records (key + weight) and dpix for 8 groups: 4*nsid*(4+4) + 4*nsid*8*4,
     # plus the deterministic sort's row lists (rows of > 8, > 128, > 2048 records)
     ncap = 4 * nsid
     lists = 4 * (ncap // 9 + ncap // 129 + ncap // 2049 + 3)
-    assert n.value >= nsid * (32 + 16 + 128) + lists
-    assert n.value < nsid * (32 + 16 + 128) + lists + 4 * 1024 * 1024
+    assert n.value >= nsid * (32 + 128) + lists
+    assert n.value < nsid * (32 + 128) + lists + 4 * 1024 * 1024
     assert lib.da_backward_workspace_size(None, ctypes.byref(n)) == DA_ERR_NULL
     big = _dims(batch=1 << 20, num_anchors=1 << 10, num_pts=4)
     assert lib.da_backward_workspace_size(ctypes.byref(big), ctypes.byref(n)) == DA_ERR_UNSUPPORTED
@@ -281,7 +281,8 @@ def test_fused_workspace_size(lib):
     assert bl.da_backward_fused_workspace_size(ctypes.byref(d), ctypes.byref(n)) == DA_OK
     nsid = 64 * 3136 * 4 * 9  # samples of the rewrite: one per (anchor, group, point)
     ncap = 4 * nsid
-    base = ncap * (8 + 4 + 4) + 4 * (ncap // 9 + ncap // 129 + ncap // 2049 + 3)
+    # records (8 bytes) and d (one group: 4 bytes) per record, plus the sort's row lists
+    base = ncap * (8 + 4) + 4 * (ncap // 9 + ncap // 129 + ncap // 2049 + 3)
     assert base <= n.value < base + 4 * 64 * 3136 * 4 + (8 << 20)
     bad = _dims(num_embeds=48, num_groups=4)  # D = 12: not a power of two
     assert bl.da_backward_fused_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == DA_ERR_UNSUPPORTED
