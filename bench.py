@@ -350,9 +350,12 @@ def run_ours(a, wl):
     stream = torch.cuda.Stream(device=dev)
     fwd_bytes, bwd_bytes = algorithmic_bytes(inp)
     ws = None
+    dims = da._dims(feat, da._host_i32(ss), loc, w)
+    if a.bwd_path == "auto":
+        # The binding's choice for these sizes (the one autograd users get).
+        a.bwd_path = da.backward_path(dims)
     path = "scatter" if a.bwd_path == "scatter" else "binned"
     if path == "binned":
-        dims = da._dims(feat, da._host_i32(ss), loc, w)
         ws = torch.empty(max(da.backward_workspace_size(dims), 256), dtype=torch.uint8, device=dev)
 
     # The binning half of the binned backward needs the locations only: it runs
@@ -773,14 +776,15 @@ def main():
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (smaller cases for profiler captures; "
                          "the headline uses the workload's own)")
-    ap.add_argument("--bwd-path", choices=["binned", "binned-det", "scatter"], default=None,
+    ap.add_argument("--bwd-path", choices=["auto", "binned", "binned-det", "scatter"], default=None,
                     help="backward algorithm (binned needs a device workspace; binned-det is its "
-                         "deterministic mode). Default: binned for --op da, scatter for --op fused")
+                         "deterministic mode; auto is da_backward's default choice for the sizes). "
+                         "Default: auto for --op da, scatter for --op fused")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
     if a.bwd_path is None and a.op == "da":
-        a.bwd_path = "binned"
+        a.bwd_path = "auto"
     if a.op in ("projected", "warpaffine"):
         if a.impl == "reference" or a.gpus != 1:
             ap.error(f"--op {a.op} runs our implementation on one GPU")

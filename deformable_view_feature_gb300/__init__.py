@@ -32,7 +32,7 @@ __all__ = ["da_forward", "da_backward", "da_forward_fused", "da_backward_fused",
 
 DA_F32, DA_BF16, DA_F16 = 0, 1, 2
 _STATUS = {0: "DA_OK", 1: "DA_ERR_NULL", 2: "DA_ERR_SHAPE", 3: "DA_ERR_ALIGN",
-           4: "DA_ERR_UNSUPPORTED", 5: "DA_ERR_CUDA", 6: "DA_ERR_WORKSPACE"}
+           4: "DA_ERR_UNSUPPORTED", 5: "DA_ERR_CUDA", 6: "DA_ERR_WORKSPACE", 7: "DA_ERR_DEVICE_BOUNDS"}
 
 
 class DaError(RuntimeError):
@@ -60,7 +60,10 @@ _lib = None
 
 
 def library_path() -> str:
-    return _build.LIB
+    """libda.so, or the bounds-checking libda_debug.so when the environment
+    variable DA_DEBUG_BOUNDS is 1 (build it with
+    `python -m deformable_view_feature_gb300.build --debug-bounds`)."""
+    return _build.DEBUG_LIB if os.environ.get("DA_DEBUG_BOUNDS") == "1" else _build.LIB
 
 
 def load_library():

@@ -20,6 +20,12 @@
 // with the device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DA_NOALLOC_SCRATCH_BYTES];
 
+#ifdef DA_DEBUG_BOUNDS
+// Error word of the bounds-checking build: one bit per kind of index that a
+// kernel found outside its tensor (da_bounds.h).
+static __device__ uint32_t g_bounds_word;
+#endif
+
 namespace da {
 
 namespace {
@@ -43,6 +49,43 @@ da_status cuda_fail(cudaError_t e, const char *what)
 {
     return fail(DA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
+
+#ifdef DA_DEBUG_BOUNDS
+uint32_t *bounds_word()
+{
+    void *p = nullptr;
+    return cudaGetSymbolAddress(&p, g_bounds_word) == cudaSuccess ? static_cast<uint32_t *>(p) : nullptr;
+}
+
+da_status bounds_report(cudaStream_t st)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(st, &cs);
+    if (e != cudaSuccess) return cuda_fail(e, "bounds check: cudaStreamIsCapturing");
+    if (cs != cudaStreamCaptureStatusNone) return DA_OK;  // reported by the next call outside the capture
+    if ((e = cudaStreamSynchronize(st)) != cudaSuccess) return cuda_fail(e, "bounds check: stream synchronize");
+    uint32_t v = 0;
+    if ((e = cudaMemcpyFromSymbol(&v, g_bounds_word, sizeof v)) != cudaSuccess)
+        return cuda_fail(e, "bounds check: read of the error word");
+    if (v == 0) return DA_OK;
+    const uint32_t zero = 0;
+    if ((e = cudaMemcpyToSymbol(g_bounds_word, &zero, sizeof zero)) != cudaSuccess)
+        return cuda_fail(e, "bounds check: clear of the error word");
+    static const char *names[] = {"feature row", "output element", "record slot", "anchor",
+                                  "sample id", "row counter", "shared table entry", "source pixel"};
+    char buf[200] = "";
+    for (int i = 0; i < 8; ++i)
+        if (v & (1u << i)) {
+            std::strncat(buf, buf[0] ? ", " : "", sizeof buf - std::strlen(buf) - 1);
+            std::strncat(buf, names[i], sizeof buf - std::strlen(buf) - 1);
+        }
+    return fail(DA_ERR_DEVICE_BOUNDS, "a kernel computed an index outside its tensor (%s); the accesses were skipped",
+                buf);
+}
+#else
+uint32_t *bounds_word() { return nullptr; }
+da_status bounds_report(cudaStream_t) { return DA_OK; }
+#endif
 
 da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const int32_t *level_start_index,
                         Problem &pb, int &chunks)
@@ -111,6 +154,7 @@ da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const
     pb.div_P = da::FastDiv::make(d.num_pts > 0 ? d.num_pts : 1);
     pb.div_PKS = da::FastDiv::make(pks > 0 ? static_cast<uint32_t>(pks) : 1);
     pb.div_rows = da::FastDiv::make(d.num_feat_rows > 0 ? static_cast<uint32_t>(d.num_feat_rows) : 1);
+    pb.dbg_err = bounds_word();
     return DA_OK;
 }
 
@@ -173,7 +217,7 @@ da_status forward_impl(const da_dims &d, da::FwdArgs &a, int chunks, float *out,
     if (n_out == 0) return DA_OK;
     const cudaError_t e = da::launch_forward(a, d.feat_dtype, chunks, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "forward launch");
-    return DA_OK;
+    return da::bounds_report(reinterpret_cast<cudaStream_t>(stream));
 }
 
 // The part of every backward entry point after the layout-specific checks
@@ -230,7 +274,7 @@ da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const floa
         const cudaError_t e =
             da::launch_backward_binned(a, w, d.feat_dtype, s, ready ? da::kStagePull : da::kStageAll);
         if (e != cudaSuccess) return cuda_fail(e, "binned backward launch");
-        return DA_OK;
+        return da::bounds_report(s);
     }
     cudaError_t e = da::launch_zero_fill(grad_feat, n_gf, s);
     if (e != cudaSuccess) return cuda_fail(e, "grad_feat zero-fill");
@@ -246,7 +290,7 @@ da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const floa
     }
     e = da::launch_backward(a, d.feat_dtype, chunks, s);
     if (e != cudaSuccess) return cuda_fail(e, "backward launch");
-    return DA_OK;
+    return da::bounds_report(s);
 }
 
 // Checks of the fused per-group layout: loc_weight [B,A,G,P,K,2+S] fp32.
@@ -463,7 +507,7 @@ da_status da_backward_bin(const da_dims *dims, const int32_t *spatial_shape, con
     const cudaError_t e = da::launch_backward_binned(a, w, dims->feat_dtype, reinterpret_cast<cudaStream_t>(stream),
                                                      da::kStageBin);
     if (e != cudaSuccess) return cuda_fail(e, "binning launch");
-    return DA_OK;
+    return da::bounds_report(reinterpret_cast<cudaStream_t>(stream));
 }
 
 da_status da_forward_fused(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
@@ -551,7 +595,7 @@ da_status da_backward_projected(const da_dims *dims, const void *mc_ms_feat, con
     const cudaError_t e = da::launch_projected_chain(pp, weights, grad_loc, grad_weight, grad_keypoints, grad_logits,
                                                      reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "projected chain-rule launch");
-    return DA_OK;
+    return da::bounds_report(reinterpret_cast<cudaStream_t>(stream));
 }
 
 da_status da_backward_noalloc(const da_dims *dims, const void *mc_ms_feat, const int32_t *spatial_shape,
@@ -584,6 +628,7 @@ const char *da_status_string(da_status status)
         case DA_ERR_UNSUPPORTED: return "DA_ERR_UNSUPPORTED";
         case DA_ERR_CUDA: return "DA_ERR_CUDA";
         case DA_ERR_WORKSPACE: return "DA_ERR_WORKSPACE";
+        case DA_ERR_DEVICE_BOUNDS: return "DA_ERR_DEVICE_BOUNDS";
     }
     return "DA_ERR_UNKNOWN";
 }

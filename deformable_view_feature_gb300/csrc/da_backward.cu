@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
                                      __int_as_float(e23.w)};
                 uint4 raw[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
+                for (int u = 0; u < 4; ++u) raw[u] = ldg16_if(feat_row_ok(pb, r[u]), row_addr(base, r[u], row_bytes));
                 float d[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
@@ -205,7 +205,7 @@ __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
                                                                        grow_bytes);
 #pragma unroll
                     for (int q = 0; q < VEC / 4; ++q)
-                        red_add_v4_if(r[u] >= 0, dst + 4 * q, tw[u] * go[4 * q], tw[u] * go[4 * q + 1],
+                        red_add_v4_if(feat_row_ok(pb, r[u]), dst + 4 * q, tw[u] * go[4 * q], tw[u] * go[4 * q + 1],
                                       tw[u] * go[4 * q + 2], tw[u] * go[4 * q + 3]);
                 }
                 row_sum_store<CH>(d, chunk, &dtab[warp][i][corner]);
@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kThreads) bwd_small_kernel(const BwdArgs args,
                 f[u].lh = f[u].lw = f[u].hh = f[u].hw = 0.f;
             }
 #pragma unroll
-            for (int c = 0; c < 4; ++c) raw[u][c] = ldg16_if(f[u].row[c] >= 0, row_addr(base, f[u].row[c], row_bytes));
+            for (int c = 0; c < 4; ++c) raw[u][c] = ldg16_if(feat_row_ok(pb, f[u].row[c]), row_addr(base, f[u].row[c], row_bytes));
         }
 #pragma unroll
         for (int u = 0; u < kSmallUnroll; ++u) {
@@ -351,7 +351,7 @@ __global__ void __launch_bounds__(kThreads) bwd_small_kernel(const BwdArgs args,
                 float *dst = gbase + static_cast<int64_t>(f[u].row[c]) * pb.C;
 #pragma unroll
                 for (int q = 0; q < VEC / 4; ++q)
-                    red_add_v4_if(live && f[u].row[c] >= 0, dst + 4 * q, tw * go[4 * q], tw * go[4 * q + 1],
+                    red_add_v4_if(live && feat_row_ok(pb, f[u].row[c]), dst + 4 * q, tw * go[4 * q], tw * go[4 * q + 1],
                                   tw * go[4 * q + 2], tw * go[4 * q + 3]);
             }
             for (int m = 1; m < ch; m <<= 1)

@@ -149,7 +149,8 @@ __device__ __forceinline__ void flush_small_counts(const Problem &pb, const MapI
         const int n = m.H * m.W * gs;
         for (int r = threadIdx.x; r < n; r += kBinThreads) {
             const int v = hist[hoff[s] + r];
-            if (v) atomicAdd(row_base + m.start * gs + r, v);
+            if (v && DA_CHECK(pb.dbg_err, static_cast<int64_t>(m.start) * gs + r, pb.rows, kBoundsRowCount))
+                atomicAdd(row_base + m.start * gs + r, v);
         }
     }
 }
@@ -183,8 +184,13 @@ __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 if (f.row[cc] < 0) continue;
-                if (ho >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + vg], 1);
-                else atomicAdd(cnt + f.row[cc] * gs + vg, 1);
+                if (ho >= 0) {
+                    const int hi = ho + (f.row[cc] - m.start) * gs + vg;
+                    if (DA_CHECK(pb.dbg_err, hi, kBinSmemRows, kBoundsShared)) atomicAdd(&hist[hi], 1);
+                } else {
+                    const int64_t ri = static_cast<int64_t>(f.row[cc]) * gs + vg;
+                    if (DA_CHECK(pb.dbg_err, ri, pb.rows, kBoundsRowCount)) atomicAdd(cnt + ri, 1);
+                }
             }
         }
     }
@@ -299,8 +305,10 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
             Footprint f;
             footprint(xy.x, xy.y, m, f);
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-                if (f.row[cc] >= 0) atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + vg], 1);
+            for (int cc = 0; cc < 4; ++cc) {
+                const int hi = ho + (f.row[cc] - m.start) * gs + vg;
+                if (f.row[cc] >= 0 && DA_CHECK(pb.dbg_err, hi, kBinSmemRows, kBoundsShared)) atomicAdd(&hist[hi], 1);
+            }
         }
     }
     __syncthreads();
@@ -312,7 +320,8 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
         const int n = m.H * m.W * gs;
         for (int r = threadIdx.x; r < n; r += kBinThreads) {
             const int v = hist[hoff[s] + r];
-            if (v) hist[hoff[s] + r] = atomicAdd(cursor + m.start * gs + r, v);
+            if (v && DA_CHECK(pb.dbg_err, static_cast<int64_t>(m.start) * gs + r, pb.rows, kBoundsRowCount))
+                hist[hoff[s] + r] = atomicAdd(cursor + m.start * gs + r, v);
         }
     }
     __syncthreads();
@@ -327,13 +336,19 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
             pos[cc] = -1;
-            if (f.row[cc] >= 0)
-                pos[cc] = ho >= 0 ? atomicAdd(&hist[ho + (f.row[cc] - m.start) * gs + vg], 1)
-                                  : atomicAdd(cursor + f.row[cc] * gs + vg, 1);
+            if (f.row[cc] < 0) continue;
+            if (ho >= 0) {
+                const int hi = ho + (f.row[cc] - m.start) * gs + vg;
+                if (DA_CHECK(pb.dbg_err, hi, kBinSmemRows, kBoundsShared)) pos[cc] = atomicAdd(&hist[hi], 1);
+            } else {
+                const int64_t ri = static_cast<int64_t>(f.row[cc]) * gs + vg;
+                if (DA_CHECK(pb.dbg_err, ri, pb.rows, kBoundsRowCount)) pos[cc] = atomicAdd(cursor + ri, 1);
+            }
         }
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc)
-            if (pos[cc] >= 0) w.rec[pos[cc]] = make_int2(static_cast<int>(sid) * 4 + cc, __float_as_int(f.cw[cc]));
+            if (pos[cc] >= 0 && DA_CHECK(pb.dbg_err, pos[cc], w.ncap, kBoundsRecord))
+                w.rec[pos[cc]] = make_int2(static_cast<int>(sid) * 4 + cc, __float_as_int(f.cw[cc]));
     }
 }
 
@@ -396,7 +411,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_short_rows_kernel(const Pro
         int rank = 0;
 #pragma unroll
         for (int v = 0; v < 8; ++v) rank += (e[v].x < e[u].x) ? 1 : 0;  // padding keys are never smaller
-        if (rank != u) w.rec[jb + rank] = e[u];
+        if (rank != u && DA_CHECK(pb.dbg_err, jb + rank, w.ncap, kBoundsRecord)) w.rec[jb + rank] = e[u];
     }
 }
 
@@ -412,13 +427,14 @@ __global__ void __launch_bounds__(kSortThreads) sort_warp_rows_kernel(const Prob
         const int64_t r = w.sort_lists[i];
         const int jb = row_begin(w, r);
         const int n = w.row_off[r] - jb;
+        if (!DA_CHECK(pb.dbg_err, n - 1, kSortWarpMax, kBoundsShared)) continue;  // the tier bounds n
         for (int j = lane; j < n; j += 32) buf[warp][j] = w.rec[jb + j];
         __syncwarp();
         for (int j = lane; j < n; j += 32) {
             const int2 e = buf[warp][j];
             int rank = 0;
             for (int v = 0; v < n; ++v) rank += (buf[warp][v].x < e.x) ? 1 : 0;
-            if (rank != j) w.rec[jb + rank] = e;
+            if (rank != j && DA_CHECK(pb.dbg_err, jb + rank, w.ncap, kBoundsRecord)) w.rec[jb + rank] = e;
         }
         __syncwarp();
     }
@@ -477,6 +493,7 @@ __global__ void __launch_bounds__(kSortThreads) sort_cta_rows_kernel(const Probl
         const int64_t r = list[i];
         const int jb = row_begin(w, r);
         const int n = w.row_off[r] - jb;
+        if (!DA_CHECK(pb.dbg_err, n - 1, kSortSmemMax, kBoundsShared)) continue;  // the tier bounds n
         for (int j = threadIdx.x; j < n; j += kSortThreads) buf[j] = w.rec[jb + j];
         __syncthreads();
         block_bitonic_sort(static_cast<int2 *>(buf), n);

@@ -120,7 +120,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                 }
                 uint4 raw[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
+                for (int u = 0; u < U; ++u) raw[u] = ldg16_if(feat_row_ok(pb, r[u]), row_addr(base, r[u], row_bytes));
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     float v[VEC];
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads) fwd_proj_kernel(const FwdArgs args)
                 }
                 uint4 raw[U];
 #pragma unroll
-                for (int u = 0; u < U; ++u) raw[u] = ldg16_if(r[u] >= 0, row_addr(base, r[u], row_bytes));
+                for (int u = 0; u < U; ++u) raw[u] = ldg16_if(feat_row_ok(pb, r[u]), row_addr(base, r[u], row_bytes));
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     float v[VEC];
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args,
                 tw[u][2] = __int_as_float(e1.y);
                 tw[u][3] = __int_as_float(e1.w);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) raw[u][c] = ldg16_if(live && r[c] >= 0, row_addr(base, r[c], row_bytes));
+                for (int c = 0; c < 4; ++c) raw[u][c] = ldg16_if(live && feat_row_ok(pb, r[c]), row_addr(base, r[c], row_bytes));
             }
 #pragma unroll
             for (int u = 0; u < 4; ++u)

@@ -7,6 +7,7 @@
 #include <stdint.h>
 
 #include "da.h"
+#include "da_bounds.h"
 
 namespace da {
 
@@ -69,6 +70,9 @@ struct Problem {
     int32_t gsplit;
     FastDiv div_S, div_K, div_G, div_A, div_P, div_PKS, div_rows;
     MapInfo maps[DA_MAX_MAPS];
+    // Bounds-checking builds: the device error word (see da_bounds.h);
+    // NULL in release builds.
+    uint32_t *dbg_err;
     // Projected layout only (after the fields every kernel reads).
     const float *keypoints;
     const float *projection;
@@ -173,8 +177,16 @@ da_status fail(da_status st, const char *fmt, ...);
 const char *last_error();
 da_status cuda_fail(cudaError_t e, const char *what);
 bool aligned(const void *p, uintptr_t a);
+// Bounds-checking builds (DA_DEBUG_BOUNDS): the device address of the error
+// word the kernels set bits in (NULL in release builds, and if the lookup
+// fails), and the check an entry point makes after enqueueing its work: wait
+// for the stream, read and clear the word, DA_ERR_DEVICE_BOUNDS if a bit
+// was set. Release builds: returns DA_OK without a CUDA call.
+uint32_t *bounds_word();
+da_status bounds_report(cudaStream_t st);
 // Validates dims and the two host map tables and fills every field of pb
-// except the tensor pointers. Makes no CUDA call.
+// except the tensor pointers. Makes no CUDA call (but a bounds-checking
+// build looks up its error word).
 da_status prepare_shape(const da_dims *dims, const int32_t *spatial_shape, const int32_t *level_start_index,
                         Problem &pb, int &chunks);
 
@@ -314,6 +326,13 @@ __device__ __forceinline__ void footprint(float x, float y, const MapInfo &m, Fo
     f.cw[1] = f.hh * f.lw;
     f.cw[2] = f.lh * f.hw;
     f.cw[3] = f.lh * f.lw;
+}
+
+// Whether feature row r (of one batch item) is read or written: r >= 0 is a
+// corner inside its map; a bounds-checking build also checks r < rows.
+__device__ __forceinline__ bool feat_row_ok(const Problem &pb, int32_t r)
+{
+    return r >= 0 && DA_CHECK(pb.dbg_err, r, pb.rows, kBoundsFeatRow);
 }
 
 // 16-byte read-only load of one chunk of a feature row, or zeros when `pred`

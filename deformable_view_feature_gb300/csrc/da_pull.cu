@@ -18,9 +18,10 @@ __device__ __forceinline__ int pick4(const int (&k)[4], int u)
     return u == 0 ? k[0] : u == 1 ? k[1] : u == 2 ? k[2] : k[3];
 }
 
+// err, kcap: a bounds-checking build checks every key against kcap records.
 template <int L>
 __device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, int nvalid, float *base,
-                                                const int (&key)[4], int stride)
+                                                const int (&key)[4], int stride, uint32_t *err, int64_t kcap)
 {
     if constexpr (L >= 4) {
         const bool hA = (sub & (L / 2)) != 0;
@@ -35,7 +36,9 @@ __device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, in
 #pragma unroll
         for (int m = L / 8; m >= 1; m >>= 1) r += __shfl_xor_sync(0xffffffffu, r, m);
         const int u = (hA ? 2 : 0) + (hB ? 1 : 0);
-        if ((sub & (L / 4 - 1)) == 0 && u < nvalid) base[static_cast<int64_t>(pick4(key, u)) * stride] = r;
+        const int ku = pick4(key, u);
+        if ((sub & (L / 4 - 1)) == 0 && u < nvalid && DA_CHECK(err, ku, kcap, kBoundsSample))
+            base[static_cast<int64_t>(ku) * stride] = r;
     } else if constexpr (L == 2) {
         const bool h = (sub & 1) != 0;
         float a0 = h ? d[2] : d[0], a1 = h ? d[3] : d[1];
@@ -43,12 +46,13 @@ __device__ __forceinline__ void group_sum_store(const float (&d)[4], int sub, in
         a0 += __shfl_xor_sync(0xffffffffu, s0, 1);
         a1 += __shfl_xor_sync(0xffffffffu, s1, 1);
         const int u0 = h ? 2 : 0;
-        if (u0 < nvalid) base[static_cast<int64_t>(pick4(key, u0)) * stride] = a0;
-        if (u0 + 1 < nvalid) base[static_cast<int64_t>(pick4(key, u0 + 1)) * stride] = a1;
+        const int k0 = pick4(key, u0), k1 = pick4(key, u0 + 1);
+        if (u0 < nvalid && DA_CHECK(err, k0, kcap, kBoundsSample)) base[static_cast<int64_t>(k0) * stride] = a0;
+        if (u0 + 1 < nvalid && DA_CHECK(err, k1, kcap, kBoundsSample)) base[static_cast<int64_t>(k1) * stride] = a1;
     } else {
 #pragma unroll
         for (int u = 0; u < 4; ++u)
-            if (u < nvalid) base[static_cast<int64_t>(key[u]) * stride] = d[u];
+            if (u < nvalid && DA_CHECK(err, key[u], kcap, kBoundsSample)) base[static_cast<int64_t>(key[u]) * stride] = d[u];
     }
 }
 
@@ -232,11 +236,18 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
 #pragma unroll
         for (int j = 0; j < RPL; ++j) {
             const int c = sub + LPR * j;
-            const bool valid = k0 + c < n;
+            bool valid = k0 + c < n && DA_CHECK(pb.dbg_err, jb + k0 + c, w.ncap, kBoundsRecord);
             const int2 r = valid ? __ldg(&w.rec[jb + k0 + c]) : make_int2(0, 0);
             const int sid = r.x >> 2;
-            const int a = valid ? static_cast<int>(pb.div_PKS.div(sid)) - abase : 0;
-            meta[row_slot + c] = make_int2(a, r.y);
+            int a = valid ? static_cast<int>(pb.div_PKS.div(sid)) - abase : 0;
+            // A bounds-checking build drops a record whose anchor or sample
+            // is outside the problem (its weight 0, anchor 0).
+            if (valid && !(DA_CHECK(pb.dbg_err, a, pb.A, kBoundsAnchor) &&
+                           DA_CHECK(pb.dbg_err, sid, w.nsid, kBoundsSample))) {
+                valid = false;
+                a = 0;
+            }
+            meta[row_slot + c] = make_int2(a, valid ? r.y : 0);
             ksm[row_slot + c] = r.x;
             if constexpr (!FUSED) {
                 const float *wp = pb.weights + static_cast<int64_t>(sid) * G;
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
             for (int u = 0; u < 4; ++u) d[u] = record_fma2(v2, x[u], y[u], tw[u], acc2);
             const int4 k4 = *reinterpret_cast<const int4 *>(ksm + row_slot + u0);
             const int keys[4] = {k4.x, k4.y, k4.z, k4.w};
-            group_sum_store<LPG>(d, gsub, n - k0 - u0, w.dpix + g, keys, G);
+            group_sum_store<LPG>(d, gsub, n - k0 - u0, w.dpix + g, keys, G, pb.dbg_err, w.ncap);
         }
         __syncwarp();
     }

@@ -22,6 +22,7 @@ struct WaArgs {
     int H, W, Hd, Wd;
     float fill;
     float mean[3], inv_std[3];
+    uint32_t *dbg_err;  // bounds-checking builds: the device error word
 };
 
 // Interpolated channel values of destination pixel (dx, dy) of frame b, or
@@ -37,6 +38,10 @@ __device__ __forceinline__ void wa_sample(const WaArgs &a, int b, int dx, int dy
         return;
     }
     const int x0 = static_cast<int>(floorf(sx)), y0 = static_cast<int>(floorf(sy));
+    if (!(DA_CHECK(a.dbg_err, x0, a.W, kBoundsPixel) && DA_CHECK(a.dbg_err, y0, a.H, kBoundsPixel))) {
+        v[0] = v[1] = v[2] = a.fill;
+        return;
+    }
     const float wx = __fsub_rn(sx, static_cast<float>(x0)), wy = __fsub_rn(sy, static_cast<float>(y0));
     const float ux = __fsub_rn(1.f, wx), uy = __fsub_rn(1.f, wy);
     const float w00 = __fmul_rn(ux, uy), w10 = __fmul_rn(wx, uy), w01 = __fmul_rn(ux, wy), w11 = __fmul_rn(wx, wy);
@@ -103,6 +108,7 @@ da_status wa_prepare(const wa_dims *dims, const uint8_t *src, const float *d2i, 
     a.W = d.src_w;
     a.Hd = d.dst_h;
     a.Wd = d.dst_w;
+    a.dbg_err = bounds_word();
     return DA_OK;
 }
 
@@ -129,7 +135,8 @@ da_status wa_warpaffine_u8(const wa_dims *dims, const uint8_t *src, const float 
     da::wa_u8_kernel<<<da::wa_grid(a, dims->batch), dim3(da::kWaBx, da::kWaBy), 0,
                        reinterpret_cast<cudaStream_t>(stream)>>>(a, dst);
     const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? DA_OK : da::cuda_fail(e, "warpaffine launch");
+    if (e != cudaSuccess) return da::cuda_fail(e, "warpaffine launch");
+    return da::bounds_report(reinterpret_cast<cudaStream_t>(stream));
 }
 
 da_status wa_preprocess(const wa_dims *dims, const uint8_t *src, const float *d2i, uint8_t fill, const float *mean,
@@ -152,7 +159,8 @@ da_status wa_preprocess(const wa_dims *dims, const uint8_t *src, const float *d2
     da::wa_preprocess_kernel<<<da::wa_grid(a, dims->batch), dim3(da::kWaBx, da::kWaBy), 0,
                                reinterpret_cast<cudaStream_t>(stream)>>>(a, dst);
     const cudaError_t e = cudaGetLastError();
-    return e == cudaSuccess ? DA_OK : da::cuda_fail(e, "preprocess launch");
+    if (e != cudaSuccess) return da::cuda_fail(e, "preprocess launch");
+    return da::bounds_report(reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -65,8 +65,25 @@ typedef enum da_status {
     DA_ERR_ALIGN = 3,       /* a pointer is not aligned as required below */
     DA_ERR_UNSUPPORTED = 4, /* valid sizes this build has no kernel for (see da_forward) */
     DA_ERR_CUDA = 5,        /* a CUDA launch or runtime call failed */
-    DA_ERR_WORKSPACE = 6    /* workspace too small or not 256-byte aligned */
+    DA_ERR_WORKSPACE = 6,   /* workspace too small or not 256-byte aligned */
+    DA_ERR_DEVICE_BOUNDS = 7 /* bounds-checking builds only: see below */
 } da_status;
+
+/*
+ * Bounds-checking builds (compiled with DA_DEBUG_BOUNDS; libda_debug.so).
+ * Every index a kernel computes before it reads or writes device memory
+ * (feature rows from the sampling locations, record slots from the binning,
+ * anchors and sample ids decoded from records, d entries, output elements,
+ * source pixels of the warpaffine kernels) is checked against the extent of
+ * its tensor first. An index outside it is not used: the access is skipped,
+ * and the kernel sets a bit for the kind of index in a device error word.
+ * Nothing traps, so the context stays usable. After enqueueing its work,
+ * each entry point of such a build waits for its stream, reads the word
+ * (then clears it) and returns DA_ERR_DEVICE_BOUNDS if a bit was set;
+ * da_last_error() names the kinds. A call made while its stream is being
+ * captured into a CUDA graph skips that wait; the next call outside a
+ * capture reports what it set. Release builds contain none of this.
+ */
 
 typedef enum da_dtype {
     DA_F32 = 0,  /* IEEE binary32 features */
