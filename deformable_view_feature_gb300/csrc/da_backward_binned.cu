@@ -84,7 +84,7 @@ namespace {
 // of the coarse maps. Larger maps are counted with a global atomic per
 // corner.
 constexpr int kBinThreads = 256;
-constexpr int kBinSmemRows = 4096;
+constexpr int kBinSmemRows = 8192;
 
 struct BinCta {
     int b, k, q;         // batch item, camera, (a*P + p) of this thread
@@ -122,18 +122,25 @@ __device__ __forceinline__ float2 bin_xy(const Problem &pb, int64_t pk)
 }
 
 // Shared-memory offsets of the small maps of camera k (-1: counted globally).
-__device__ __forceinline__ void small_map_offsets(const Problem &pb, const MapInfo *maps_s, int k, int *hoff,
-                                                  int &nsmall, int gs)
+__host__ __device__ inline void small_map_offsets(int S, const MapInfo *maps_s, int k, int *hoff, int &nsmall,
+                                                  int gs)
 {
+    // Smallest maps first: their rows take the most corners each, so they
+    // gain most from counting in shared memory.
+    for (int s = 0; s < S; ++s) hoff[s] = -1;
     int off = 0;
-    for (int s = 0; s < pb.S; ++s) {
-        const int n = maps_s[k * pb.S + s].H * maps_s[k * pb.S + s].W * gs;
-        if (off + n <= kBinSmemRows) {
-            hoff[s] = off;
-            off += n;
-        } else {
-            hoff[s] = -1;
+    for (;;) {
+        int best = -1, bn = 0;
+        for (int s = 0; s < S; ++s) {
+            const int n = maps_s[k * S + s].H * maps_s[k * S + s].W * gs;
+            if (hoff[s] < 0 && off + n <= kBinSmemRows && (best < 0 || n < bn)) {
+                best = s;
+                bn = n;
+            }
         }
+        if (best < 0) break;
+        hoff[best] = off;
+        off += bn;
     }
     nsmall = off;
 }
@@ -157,10 +164,10 @@ __device__ __forceinline__ void flush_small_counts(const Problem &pb, const MapI
 
 template <bool FUSED>
 __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb, const BinArgs w,
-                                                                 int ctas_per_view)
+                                                                 int ctas_per_view, int hist_rows)
 {
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
-    __shared__ int hist[kBinSmemRows];
+    extern __shared__ int hist[];  // hist_rows entries
     __shared__ int hoff[DA_MAX_MAPS];
     __shared__ int nsmall_s;
     stage_maps(pb, maps_s);
@@ -169,7 +176,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb
     // Virtual rows per pixel row: gsplit in the fused rewrite, else 1.
     const int gs = FUSED ? pb.gsplit : 1;
     const int vg = FUSED ? c.vg : 0;
-    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s, gs);
+    if (threadIdx.x == 0) small_map_offsets(pb.S, maps_s, c.k, hoff, nsmall_s, gs);
     __syncthreads();
     for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
     __syncthreads();
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb
                 if (f.row[cc] < 0) continue;
                 if (ho >= 0) {
                     const int hi = ho + (f.row[cc] - m.start) * gs + vg;
-                    if (DA_CHECK(pb.dbg_err, hi, kBinSmemRows, kBoundsShared)) atomicAdd(&hist[hi], 1);
+                    if (DA_CHECK(pb.dbg_err, hi, hist_rows, kBoundsShared)) atomicAdd(&hist[hi], 1);
                 } else {
                     const int64_t ri = static_cast<int64_t>(f.row[cc]) * gs + vg;
                     if (DA_CHECK(pb.dbg_err, ri, pb.rows, kBoundsRowCount)) atomicAdd(cnt + ri, 1);
@@ -279,10 +286,10 @@ __global__ void __launch_bounds__(256) scan_add_kernel(int32_t *data, const int3
 // atomics. Every corner of a large map claims its slot with a global atomic.
 template <bool FUSED>
 __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb, const BinArgs w,
-                                                                int ctas_per_view)
+                                                                int ctas_per_view, int hist_rows)
 {
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
-    __shared__ int hist[kBinSmemRows];
+    extern __shared__ int hist[];  // hist_rows entries
     __shared__ int hoff[DA_MAX_MAPS];
     __shared__ int nsmall_s;
     stage_maps(pb, maps_s);
@@ -291,7 +298,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
     // Virtual rows per pixel row: gsplit in the fused rewrite, else 1.
     const int gs = FUSED ? pb.gsplit : 1;
     const int vg = FUSED ? c.vg : 0;
-    if (threadIdx.x == 0) small_map_offsets(pb, maps_s, c.k, hoff, nsmall_s, gs);
+    if (threadIdx.x == 0) small_map_offsets(pb.S, maps_s, c.k, hoff, nsmall_s, gs);
     __syncthreads();
     for (int i = threadIdx.x; i < nsmall_s; i += kBinThreads) hist[i] = 0;
     __syncthreads();
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
 #pragma unroll
             for (int cc = 0; cc < 4; ++cc) {
                 const int hi = ho + (f.row[cc] - m.start) * gs + vg;
-                if (f.row[cc] >= 0 && DA_CHECK(pb.dbg_err, hi, kBinSmemRows, kBoundsShared)) atomicAdd(&hist[hi], 1);
+                if (f.row[cc] >= 0 && DA_CHECK(pb.dbg_err, hi, hist_rows, kBoundsShared)) atomicAdd(&hist[hi], 1);
             }
         }
     }
@@ -339,7 +346,7 @@ __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb,
             if (f.row[cc] < 0) continue;
             if (ho >= 0) {
                 const int hi = ho + (f.row[cc] - m.start) * gs + vg;
-                if (DA_CHECK(pb.dbg_err, hi, kBinSmemRows, kBoundsShared)) pos[cc] = atomicAdd(&hist[hi], 1);
+                if (DA_CHECK(pb.dbg_err, hi, hist_rows, kBoundsShared)) pos[cc] = atomicAdd(&hist[hi], 1);
             } else {
                 const int64_t ri = static_cast<int64_t>(f.row[cc]) * gs + vg;
                 if (DA_CHECK(pb.dbg_err, ri, pb.rows, kBoundsRowCount)) pos[cc] = atomicAdd(cursor + ri, 1);
@@ -685,11 +692,22 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     {
     const int ctas_per_view = (pb.A * pb.P + kBinThreads - 1) / kBinThreads;
     const int64_t bin_grid = static_cast<int64_t>(pb.B) * pb.K * ctas_per_view;
+    // Shared histogram: as many entries as the largest set of small maps of
+    // any camera needs (the kernels pick the same maps).
+    int hist_rows = 0;
+    for (int k = 0; k < pb.K; ++k) {
+        int hoff[DA_MAX_MAPS], nsmall = 0;
+        small_map_offsets(pb.S, pb.maps, k, hoff, nsmall, pb.layout == kLayoutFused ? pb.gsplit : 1);
+        hist_rows = nsmall > hist_rows ? nsmall : hist_rows;
+    }
+    const size_t hist_bytes = static_cast<size_t>(hist_rows) * sizeof(int);
     if (w.nsid > 0) {
         if (pb.layout == kLayoutFused)
-            bin_count_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+            bin_count_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
+                                                                                            hist_rows);
         else
-            bin_count_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+            bin_count_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
+                                                                                            hist_rows);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 2. offsets
@@ -705,9 +723,11 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     // 3. records
     if (w.nsid > 0) {
         if (pb.layout == kLayoutFused)
-            bin_fill_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+            bin_fill_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
+                                                                                            hist_rows);
         else
-            bin_fill_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, 0, st>>>(pb, w, ctas_per_view);
+            bin_fill_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
+                                                                                            hist_rows);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     // 3b. deterministic order inside every row

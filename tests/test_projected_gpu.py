@@ -10,7 +10,10 @@ Stage by stage, against the oracle (pinned in test_oracle_projection_pins.py):
     oracle's locations and weights, with the usual parity tolerances;
   * grad_keypoints and grad_logits against the oracle's chain rule applied to
     the kernel's own grad_loc / grad_weight / weights, with fp32 error bounds
-    derived from the chain rule's arithmetic.
+    derived from the chain rule's arithmetic;
+  * and end to end against the oracle's chain rule applied to the oracle's
+    own weights, grad_loc and grad_weight, with the parity tolerance of those
+    carried through the (linear) chain rule.
 """
 import numpy as np
 import pytest
@@ -45,12 +48,16 @@ def _run(da, inp, path="binned", deterministic=False):
     return dict(zip(names, (to_np(t) for t in (out, loc, w, gf, gl, gw, gkp, glg))))
 
 
-def _chain_bounds(inp, got):
-    """fp32 error bounds of the two chain-rule outputs (per element)."""
-    w, gw = got["weights"].astype(np.float64), got["grad_weight"].astype(np.float64)
+def _chain_abs(inp, w, gl_abs, gw_abs):
+    """The chain rule applied to magnitudes: (|w| * (gw_abs + sum |w| gw_abs)
+    per (b, a, g), and sum over cameras of |J_k|^T gl_abs), the two factors
+    that carry an error in grad_weight / grad_loc (or a rounding) into
+    grad_logits and grad_keypoints."""
+    w = np.abs(np.asarray(w, np.float64))
+    gw_abs = np.asarray(gw_abs, np.float64)
     B, A, P, K, S, G = w.shape
-    wg = np.abs(w * gw).sum(axis=(2, 3, 4), keepdims=True)
-    glg_bound = (P * K * S + 8) * U32 * np.abs(w) * (np.abs(gw) + wg)
+    wg = (w * gw_abs).sum(axis=(2, 3, 4), keepdims=True)
+    glg = w * (gw_abs + wg)
     kp = inp.keypoints.numpy().astype(np.float64)
     M = inp.projection.numpy().astype(np.float64)
     hom = np.concatenate([kp, np.ones_like(kp[..., :1])], -1)
@@ -59,15 +66,22 @@ def _chain_bounds(inp, got):
     ok = d > 1e-5
     dd = np.where(ok, d, 1.0)
     uv = q[..., :2] / dd[..., None]
-    gl = np.abs(got["grad_loc"].astype(np.float64))
+    gl = np.asarray(gl_abs, np.float64)
     size = np.array([inp.image_w, inp.image_h])
-    kp_bound = np.zeros(kp.shape)
+    kpb = np.zeros(kp.shape)
     for i in range(3):
         mi = np.abs(M[:, None, None, :, :2, i])  # [B,1,1,K,2]
         m2 = np.abs(M[:, None, None, :, 2, i])[..., None]                # [B,1,1,K,1]
         term = gl * (mi + np.abs(uv) * m2) / (dd[..., None] * size)
-        kp_bound[..., i] = np.where(ok[..., None], term, 0.0).sum(axis=(3, 4))
-    return glg_bound, 16 * U32 * kp_bound
+        kpb[..., i] = np.where(ok[..., None], term, 0.0).sum(axis=(3, 4))
+    return glg, kpb
+
+
+def _chain_bounds(inp, got):
+    """fp32 error bounds of the two chain-rule outputs (per element)."""
+    B, A, P, K, S, G = got["weights"].shape
+    glg, kpb = _chain_abs(inp, got["weights"], np.abs(got["grad_loc"]), np.abs(got["grad_weight"]))
+    return (P * K * S + 8) * U32 * glg, 16 * U32 * kpb
 
 
 def _check(inp, got):
@@ -93,6 +107,26 @@ def _check(inp, got):
     glg_bound, kp_bound = _chain_bounds(inp, got)
     for name, r, bound in (("grad_logits", glg, glg_bound), ("grad_keypoints", gkp, kp_bound)):
         n, msg = violations(got[name], r, 1e-5, 1e-9 + bound, name)
+        if n:
+            msgs.append(msg)
+    # End to end: the oracle's chain rule on the oracle's own weights,
+    # grad_loc and grad_weight. The kernel's inputs to the chain may differ
+    # from those by their parity tolerance (and the weights by 2e-6
+    # relative); the chain carries that difference in linearly, so the bound
+    # is the chain applied to the tolerance envelope, plus its own rounding.
+    e_gkp, e_glg = oracle.projected_chain(kp, pr, inp.image_w, inp.image_h, w, ref["grad_loc"], ref["grad_weight"])
+    tol = {}
+    for name in ("grad_loc", "grad_weight"):
+        rtol, atol = TOL[inp.wl.feat_dtype][name]
+        tol[name] = rtol * np.abs(ref[name].astype(np.float64)) + atol + extra[name].reshape(ref[name].shape)
+    p_glg, p_kp = _chain_abs(inp, w, tol["grad_loc"], tol["grad_weight"])
+    w_glg, _ = _chain_abs(inp, w, np.zeros_like(tol["grad_loc"]), np.abs(ref["grad_weight"]))
+    for name, r, bound in (("grad_logits e2e", e_glg, p_glg + 4e-6 * w_glg + glg_bound),
+                           ("grad_keypoints e2e", e_gkp, p_kp + kp_bound)):
+        key = name.split()[0]
+        n, msg = violations(got[key], r, 1e-5, 1e-9 + bound, name)
+        print(f"{name}: max |gpu - oracle| = {np.max(np.abs(got[key] - r)):.3e}, "
+              f"max bound = {np.max(bound):.3e}")
         if n:
             msgs.append(msg)
     assert not msgs, " | ".join(msgs)
