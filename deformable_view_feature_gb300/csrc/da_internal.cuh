@@ -83,6 +83,15 @@ struct Problem {
 struct FwdArgs {
     Problem pb;
     float *out;
+    // Camera parts of the standard forward (1 = all cameras in one CTA).
+    // With parts > 1, CTA c takes anchors of batch item b for the cameras of
+    // part q, in the order (b, q, anchors), and adds its partial sums into
+    // `out`, which the launch zeroes first.
+    int parts;
+    int ctas_per_part;    // CTAs per (batch item, part)
+    int kpart;            // cameras per part (K / parts)
+    FastDiv div_cpp;      // by ctas_per_part
+    FastDiv div_kpart;    // by kpart
     // Projected layout only: where to write the computed locations
     // [B,A,P,K,2] and weights [B,A,P,K,S,G]; NULL = do not write.
     float *loc_out;

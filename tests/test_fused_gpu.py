@@ -6,8 +6,8 @@ Each case is compared element by element with the oracle of the DCNv4 form
 (oracle.forward_fused / backward_fused, pinned in test_oracle_fused_pins.py):
 the DCNv4 workload at full size in fp32, fp16 and bf16, the Sparse4D shape
 cut to a few anchors, and ragged shapes. A consistency case checks that the
-fused forward equals the standard forward bit for bit when every group is
-given the same points.
+fused forward equals the standard forward when every group is given the same
+points: bit for bit where the standard forward runs as one camera part.
 """
 import numpy as np
 import pytest
@@ -117,8 +117,15 @@ def test_ragged_shapes(da, C, G, dtype, path):
     _check(inp, _run(da, inp, path))
 
 
-def test_shared_points_match_standard_forward_bits(da):
-    inp = da_inputs.make_inputs(da_inputs.small_variant("sp4d_inf", num_anchors=40))
+@pytest.mark.parametrize("cams", [2, 6])
+def test_shared_points_match_standard_forward(da, cams):
+    """The DCNv4 form with every group on the same points is the standard
+    operator. With two cameras (one camera part in the standard forward) the
+    bits agree; at six cameras the standard forward sums two camera halves
+    (a different association), so the two agree within the fp32 forward
+    tolerance."""
+    wl = da_inputs.small_variant("sp4d_inf", num_anchors=40).replace(num_cams=cams)
+    inp = da_inputs.make_inputs(wl)
     B, A, P, K, _ = inp.loc.shape
     S, G = inp.weights.shape[4], inp.weights.shape[5]
     lw = torch.empty(B, A, G, P, K, 2 + S)
@@ -129,7 +136,11 @@ def test_shared_points_match_standard_forward_bits(da):
     feat = inp.feat.to(dev)
     a = da.da_forward_fused(feat, inp.spatial_shape, inp.level_start_index, lw.to(dev))
     b = da.da_forward(feat, inp.spatial_shape, inp.level_start_index, inp.loc.to(dev), inp.weights.to(dev))
-    assert torch.equal(a, b)
+    if cams == 2:
+        assert torch.equal(a, b)
+    else:
+        n, msg = violations(to_np(a), to_np(b), 1e-5, 1e-6, "out")
+        assert n == 0, msg
 
 
 @pytest.mark.parametrize("path", PATHS)

@@ -266,8 +266,14 @@ def test_output_guard_bands(da, path):
                    "grad_weight": to_np(gw)}, ref)
 
 
-def test_forward_is_deterministic(da):
-    inp = da_inputs.make_inputs(da_inputs.small_variant("sp4d_train", batch=2, num_anchors=64))
+@pytest.mark.parametrize("name", ["small", "sp4d_train"])
+def test_forward_is_deterministic(da, name):
+    """Bit-equal outputs on repeated runs. At the full training shape the
+    forward splits the cameras in two parts whose partial sums meet in out by
+    reductions; with exactly two addends on a zeroed output the order does
+    not change the bits."""
+    wl = da_inputs.small_variant("sp4d_train", batch=2, num_anchors=64) if name == "small" else name
+    inp = da_inputs.make_inputs(wl)
     a = _run_gpu(da, inp, backward=False)["out"]
     b = _run_gpu(da, inp, backward=False)["out"]
     np.testing.assert_array_equal(a, b)

@@ -163,9 +163,12 @@ def test_forward_without_kept_samples_gives_the_same_out(da):
     b, none_loc, none_w = da.da_forward_projected(*args, keep_samples=False)
     assert none_loc is None and none_w is None
     assert torch.equal(a, b)
-    # And the standard forward on the written samples gives the same bits.
+    # And the standard forward on the written samples gives the same result:
+    # within the fp32 forward tolerance, since at six cameras the standard
+    # forward sums two camera halves (another association of the same sum).
     c = da.da_forward(args[0], inp.spatial_shape, inp.level_start_index, loc, w)
-    assert torch.equal(a, c)
+    n, msg = violations(to_np(a), to_np(c), 1e-5, 1e-6, "out")
+    assert n == 0, msg
 
 
 def test_bad_image_size_refused(da):
