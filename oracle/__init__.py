@@ -57,6 +57,8 @@ def _load():
         lib.dao_grad_loc_magnitude.argtypes = ([i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp,
                                                             i64, i64, vp])
         lib.dao_grad_loc_magnitude.restype = i32
+        lib.dao_row_counts.argtypes = [i32] * 7 + [i64, vp, vp, vp, vp]
+        lib.dao_row_counts.restype = i32
         lib.dao_forward_fused.argtypes = [i32] * 7 + [i64, vp, vp, vp, i32, vp, vp]
         lib.dao_forward_fused.restype = i32
         lib.dao_backward_fused.argtypes = [i32] * 7 + [i64, vp, vp, vp, i32, vp, vp, vp, vp]
@@ -163,6 +165,19 @@ def grad_loc_magnitude(feat, spatial_shape, level_start_index, loc, weights, gra
     if rc != 0:
         raise ValueError(f"oracle magnitude rejected its arguments (code {rc})")
     return mag
+
+
+def row_counts(feat, spatial_shape, level_start_index, loc, weights):
+    """int32 [B, rows]: how many in-map corners of the samples land on each
+    feature row (an error-bound helper for the parity tests; see
+    dao_row_counts in da_oracle.c)."""
+    feat, _, ss, ls, loc, weights, dims = _prep(feat, spatial_shape, level_start_index, loc, weights)
+    B, K, S, C, G, A, P, rows = dims
+    count = np.empty((B, rows), dtype=np.int32)
+    rc = _load().dao_row_counts(B, K, S, C, G, A, P, rows, _ptr(ss), _ptr(ls), _ptr(loc), _ptr(count))
+    if rc != 0:
+        raise ValueError(f"oracle row counts rejected its arguments (code {rc})")
+    return count
 
 
 def _prep_fused(feat, spatial_shape, level_start_index, loc_weight):

@@ -577,3 +577,37 @@ int dao_grad_loc_magnitude(int B, int K, int S, int C, int G, int A, int P, int6
     }
     return DAO_OK;
 }
+
+/*
+ * Records per feature row, an error-bound helper for the parity tests (not
+ * a step of the operator).
+ *
+ * §4.1 scatters one product to each in-map corner of every sample; a row's
+ * grad_feat entry is the sum of the products its row receives, one per
+ * (anchor, point, camera, scale, corner) that lands there. count[b*rows + r]
+ * is that number for feature row r of batch item b. Corners are decided by
+ * the same fp32 footprint as the operator itself.
+ */
+int dao_row_counts(int B, int K, int S, int C, int G, int A, int P, int64_t rows,
+                   const int32_t *shape, const int32_t *start, const float *loc, int32_t *count)
+{
+    if (!check_dims(B, K, S, C, G, A, P, rows, shape, start)) return DAO_ERR_ARGS;
+    memset(count, 0, sizeof(int32_t) * (size_t)B * (size_t)rows);
+    int64_t ba;
+    for (ba = 0; ba < (int64_t)B * A; ++ba) {
+        const int64_t b = ba / A;
+        int p, k, s, i;
+        for (p = 0; p < P; ++p)
+            for (k = 0; k < K; ++k) {
+                const float *xy = loc + ((ba * P + p) * K + k) * 2;
+                for (s = 0; s < S; ++s) {
+                    footprint f;
+                    make_footprint(xy[0], xy[1], shape[(k * S + s) * 2], shape[(k * S + s) * 2 + 1],
+                                   start[k * S + s], &f);
+                    for (i = 0; i < 4; ++i)
+                        if (f.row[i] >= 0) count[b * rows + f.row[i]] += 1;
+                }
+            }
+    }
+    return DAO_OK;
+}

@@ -21,12 +21,13 @@ longest accumulation chain:
     a row's chunks, the four-corner combination);
   * grad_loc: kappa = D + S*G + 8 (the same, plus the sum over the S*G
     samples that share one location).
-grad_feat sums one product per record of its feature row, one fp32 rounding
-each, so its kappa is the row's record count plus 2. Rows of the standard
-workloads hold few records and need no such term. Tests that crowd
-thousands of samples onto a few pixels ask for it ("grad_feat" in
-kind_names) with the bound that holds for every row: a location puts at most
-one corner in a row, so a row holds at most A*P records, and kappa = A*P + 2.
+grad_feat sums one product per record of its feature row. Each product
+carries three fp32 roundings (corner weight, times the sample weight, times
+grad_out) and each addition one more, in any order, so a row of n records
+has kappa = n + 2. Rows of the standard workloads hold few records and need
+no such term. Tests that crowd thousands of samples onto a few pixels ask
+for it ("grad_feat" in kind_names); n is then each row's own count, from
+oracle.row_counts.
 The oracle supplies M:
   * grad_weight: M is the oracle's grad_weight with |feat| and |grad_out|.
     Every product in it is then non-negative.
@@ -133,9 +134,9 @@ def conditioning_atol(inp, kind_names=("grad_loc", "grad_weight")):
         _, _, m_gw = oracle.backward(afeat, *args, np.abs(go))
         res["grad_weight"] = (D + 8) * U32 * m_gw.astype(np.float64)
     if "grad_feat" in kind_names:
-        A, P = inp.loc.shape[1], inp.loc.shape[2]
+        n_row = oracle.row_counts(feat, *args).astype(np.float64)
         m_gf, _, _ = oracle.backward(feat, *args[:3], np.abs(inp.weights.numpy()), np.abs(go))
-        res["grad_feat"] = (A * P + 2) * U32 * m_gf.astype(np.float64)
+        res["grad_feat"] = (n_row[:, :, None] + 2) * U32 * m_gf.astype(np.float64)
     if "grad_loc" in kind_names:
         m_gl = oracle.grad_loc_magnitude(feat, *args, go)
         res["grad_loc"] = (D + S * G + 8) * U32 * m_gl.astype(np.float64)

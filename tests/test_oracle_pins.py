@@ -485,3 +485,41 @@ def test_grad_loc_magnitude_bounds_and_hand_value():
     assert np.all(np.abs(gl) <= m * (1 + 1e-6) + 1e-30)
     m2 = oracle.grad_loc_magnitude(feat, ss, ls, loc, w, (-3.0 * go).astype(np.float32))
     np.testing.assert_allclose(m2, 3.0 * m, rtol=1e-6)
+
+
+def test_row_counts_hand_values_and_brute_force():
+    """The grad_feat error-bound helper counts, per feature row, the in-map
+    corners that land there (§3.2's four corners, §4.1's scatter).
+    Hand values on a 2x2 map: the centre (0.5, 0.5) has h_im = w_im = 0.5,
+    so all four pixels get one corner each; the origin (0, 0) has
+    h_im = w_im = -0.5, so only pixel (0, 0), as corner 4, is in the map.
+    Then a brute-force count on a random two-camera, two-scale problem, with
+    the corner test written out here in numpy fp32."""
+    ss = np.array([[[2, 2]]], np.int32)
+    ls = np.zeros((1, 1), np.int32)
+    feat = np.zeros((1, 4, 1), np.float32)
+    w = np.ones((1, 2, 1, 1, 1, 1), np.float32)
+    loc = np.array([[0.5, 0.5], [0.0, 0.0]], np.float32).reshape(1, 2, 1, 1, 2)
+    np.testing.assert_array_equal(oracle.row_counts(feat, ss, ls, loc, w), [[2, 1, 1, 1]])
+
+    rng = np.random.default_rng(23)
+    shapes = [[(7, 9), (3, 4)], [(5, 6), (2, 2)]]
+    feat, ss, ls, loc, w, _ = _rand_problem(rng, 2, shapes, C=4, G=2, A=6, P=5, lo=-0.3, hi=1.3)
+    B, A, P, K = loc.shape[:4]
+    expect = np.zeros((B, feat.shape[1]), np.int64)
+    for b in range(B):
+        for a in range(A):
+            for p in range(P):
+                for k in range(K):
+                    x, y = loc[b, a, p, k]
+                    for s in range(len(shapes[k])):
+                        H, W = (int(v) for v in ss[k, s])
+                        h_im = np.float32(np.float32(y * np.float32(H)) - np.float32(0.5))
+                        w_im = np.float32(np.float32(x * np.float32(W)) - np.float32(0.5))
+                        h0, w0 = int(np.floor(h_im)), int(np.floor(w_im))
+                        for r, c in ((h0, w0), (h0, w0 + 1), (h0 + 1, w0), (h0 + 1, w0 + 1)):
+                            if 0 <= r < H and 0 <= c < W:
+                                expect[b, ls[k, s] + r * W + c] += 1
+    got = oracle.row_counts(feat, ss, ls, loc, w)
+    np.testing.assert_array_equal(got, expect)
+    assert 0 < got.sum() < 4 * B * A * P * sum(len(s) for s in shapes)
