@@ -172,11 +172,16 @@ __device__ __forceinline__ float record_fma2(const float2 (&v)[4], const float4 
 // records (see pull_kernel), each with
 //   meta  {anchor a of the record within its batch item, corner weight bits},
 //   ksm   the record's key (sample id * 4 + corner),
-//   wsm   the G weights of the record's sample, group-major: wsm[g][slot].
+//   wsm   the G weights of the record's sample, group-major: wsm[g][slot],
+//         each group's row padded by 4 floats. The walk reads four slots of
+//         every group at once (one 16-byte load per lane, the G groups at G
+//         addresses): rows 4 banks apart keep that one wavefront instead of G.
 // slot = row in warp * CH + record in chunk.
+__host__ __device__ constexpr int pull_wpitch(int slots) { return slots + 4; }
+
 __host__ __device__ inline size_t pull_smem_per_warp(int slots, int G)
 {
-    return static_cast<size_t>(slots) * (3 + static_cast<size_t>(G)) * 4;
+    return (static_cast<size_t>(slots) * 3 + static_cast<size_t>(G) * pull_wpitch(slots)) * 4;
 }
 
 // LPR = C/8 lanes own one feature row, 8 channels each, all groups; a warp
@@ -218,6 +223,7 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
     int2 *meta = reinterpret_cast<int2 *>(pull_smem + (threadIdx.x >> 5) * pull_smem_per_warp(SLOTS, G));
     int *ksm = reinterpret_cast<int *>(meta + SLOTS);
     float *wsm = reinterpret_cast<float *>(ksm + SLOTS);
+    constexpr int WP = pull_wpitch(SLOTS);
     // Rows are taken from the end: each camera's block of rows ends with its
     // coarsest maps, whose rows hold the most records (a sample lands in
     // every scale, and a coarse map has few pixels). Taken last to first,
@@ -283,9 +289,9 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
                     if (valid) ldg_v8_stream(wp, x, y);
                     const float wv[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
 #pragma unroll
-                    for (int gg = 0; gg < 8; ++gg) wsm[gg * SLOTS + row_slot + c] = wv[gg];
+                    for (int gg = 0; gg < 8; ++gg) wsm[gg * WP + row_slot + c] = wv[gg];
                 } else {
-                    for (int gg = 0; gg < G; ++gg) wsm[gg * SLOTS + row_slot + c] = valid ? __ldg(wp + gg) : 0.f;
+                    for (int gg = 0; gg < G; ++gg) wsm[gg * WP + row_slot + c] = valid ? __ldg(wp + gg) : 0.f;
                 }
             } else {
                 wsm[row_slot + c] = valid ? bin_weight<true>(pb, sid, 0) : 0.f;
@@ -294,7 +300,7 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
         __syncwarp();
         // 2. walk the chunk four records at a time.
         const int nb = min(CH, nmax - k0);
-        const float *wrow = wsm + g * SLOTS + row_slot;
+        const float *wrow = wsm + g * WP + row_slot;
         for (int u0 = 0; u0 < nb; u0 += 4) {
             const int4 m01 = *reinterpret_cast<const int4 *>(meta + row_slot + u0);
             const int4 m23 = *reinterpret_cast<const int4 *>(meta + row_slot + u0 + 2);
