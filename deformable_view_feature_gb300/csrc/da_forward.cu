@@ -14,6 +14,10 @@
 // Work decomposition (the page's kernel uses one thread per sample; here a
 // warp owns one (b*A+a, g) task and its P*K*S samples):
 //   * A CTA of 8 warps owns `anchors_per_cta` whole anchors: all their groups.
+//     Where a group's slice of a feature row is at most half a 128-byte line
+//     (bf16 or fp16 with D = 32), a warp takes two neighbouring groups of an
+//     anchor and a CTA twice the anchors, so every corner read is one whole
+//     line (the 6-camera bf16 forward: 114 -> 106 us).
 //   * Footprints: 32 samples at a time, one per lane. Each lane writes its
 //     sample's four {row, weight * corner weight} pairs to a per-warp,
 //     corner-major table in shared memory.
@@ -49,14 +53,22 @@ namespace da {
 namespace {
 
 // SPLIT: the camera-part decomposition (FwdArgs::parts == 2), standard layout.
-template <typename T, int CH, bool FUSED, bool SPLIT>
+// GPT: groups per task. A group's slice of a feature row is CH 16-byte
+// chunks; when that is at most half a 128-byte line (bf16 or fp16 with
+// D = 32, fp32 with D = 16), GPT = 2 gives one warp two neighbouring groups
+// of an anchor (standard layout: the groups share the sample locations). Each
+// corner read is then one whole line from one warp, not two half-line
+// requests from two warps.
+template <typename T, int CH, bool FUSED, bool SPLIT, int GPT>
 __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
 {
     static_assert(!(SPLIT && FUSED), "camera parts serve the standard layout");
+    static_assert(GPT == 1 || (GPT == 2 && !FUSED && CH <= 4), "paired groups share locations");
     using Ck = Chunk<T>;
     constexpr int VEC = Ck::kVec;   // channels per 16-byte chunk
     constexpr int ESZ = 16 / VEC;   // bytes per feature element
-    constexpr int SPP = 8 / CH;     // samples per warp-wide load
+    constexpr int TCH = CH * GPT;   // 16-byte chunks of one task's corner row
+    constexpr int SPP = 8 / TCH;    // samples per warp-wide load
     // Samples per lane per step; a warp-wide step covers U * SPP <= 32.
     constexpr int U = DA_FWD_UNROLL * SPP <= 32 ? DA_FWD_UNROLL : 32 / SPP;
     // The steps of U*SPP samples must tile the 32 table entries exactly.
@@ -64,15 +76,18 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     const Problem &pb = args.pb;
 
     __shared__ __align__(16) int2 tab[kWarps][4][kTabPitch];
+    // GPT = 2: weight * corner weight of the task's second group.
+    __shared__ __align__(16) float tab2[GPT > 1 ? kWarps : 1][4][kTabPitch];
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int chunk = lane % CH;
-    const int corner = (lane / CH) & 3;
-    const int slot = lane / (4 * CH);
+    const int chunk = lane % TCH;
+    const int corner = (lane / TCH) & 3;
+    const int slot = lane / (4 * TCH);
+    const bool second = GPT > 1 && chunk >= CH;  // the lane's chunk is in the task's second group
 
     int ba0, na, part = 0;
     if constexpr (SPLIT) {
@@ -89,12 +104,13 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
     }
     // Samples of a task: all P*K*S, or the P*kpart*S of this CTA's cameras.
     const int nsamp = SPLIT ? pb.P * args.kpart * pb.S : pb.pks;
-    const int ntask = na * pb.G;
+    const int ntask = na * (pb.G / GPT);
     const uint32_t row_bytes = static_cast<uint32_t>(pb.C) * ESZ;
 
     for (int task = warp; task < ntask; task += kWarps) {
-        const int tq = static_cast<int>(pb.div_G.div(task));
-        const int g = task - tq * pb.G;
+        // Task (anchor tq, groups g .. g + GPT - 1): task * GPT = tq * G + g.
+        const int tq = static_cast<int>(pb.div_G.div(task * GPT));
+        const int g = task * GPT - tq * pb.G;
         const int ba = ba0 + tq;
         const int b = static_cast<int>(pb.div_A.div(ba));
         const char *base = static_cast<const char *>(pb.feat) +
@@ -109,6 +125,7 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
             {
                 int row[4] = {-1, -1, -1, -1};
                 float tw[4] = {0.f, 0.f, 0.f, 0.f};
+                float tw2[4] = {0.f, 0.f, 0.f, 0.f};
                 if (lane < n) {
                     const int j = j0 + lane;
                     int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k (p*kpart + k' with parts)
@@ -131,9 +148,18 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                         row[c] = f.row[c];
                         tw[c] = w * f.cw[c];
                     }
+                    if constexpr (GPT > 1) {
+                        const float w2 = pb.weights[((static_cast<int64_t>(ba) * pb.pk + jk) * pb.S + s) * pb.G + g + 1];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) tw2[c] = w2 * f.cw[c];
+                    }
                 }
 #pragma unroll
                 for (int c = 0; c < 4; ++c) tab[warp][c][lane] = make_int2(row[c], __float_as_int(tw[c]));
+                if constexpr (GPT > 1) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tab2[warp][c][lane] = tw2[c];
+                }
             }
             __syncwarp();
 
@@ -148,6 +174,13 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
                     cw[2 * h] = __int_as_float(e.y);
                     r[2 * h + 1] = e.z;
                     cw[2 * h + 1] = __int_as_float(e.w);
+                    if constexpr (GPT > 1) {
+                        const float2 e2 = *reinterpret_cast<const float2 *>(&tab2[warp][corner][i + 2 * h]);
+                        if (second) {
+                            cw[2 * h] = e2.x;
+                            cw[2 * h + 1] = e2.y;
+                        }
+                    }
                 }
                 uint4 raw[U];
 #pragma unroll
@@ -166,11 +199,11 @@ __global__ void __launch_bounds__(kThreads) fwd_kernel(const FwdArgs args)
         // Sum the corner and slot partials: lanes that differ only above the
         // chunk bits hold the same channels.
 #pragma unroll
-        for (int m = CH; m < 32; m <<= 1) {
+        for (int m = TCH; m < 32; m <<= 1) {
 #pragma unroll
             for (int q = 0; q < VEC; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], m);
         }
-        if (lane < CH) {
+        if (lane < TCH) {
             float *o = args.out + static_cast<int64_t>(ba) * pb.C + static_cast<int64_t>(g) * pb.D + chunk * VEC;
             if constexpr (SPLIT) {
                 // Exactly two partial sums meet on a zeroed output: 0 + x is
@@ -500,7 +533,7 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
     const int64_t grid = sampling_grid(a.pb);
     if (grid == 0) return cudaSuccess;
     switch (a.pb.layout) {
-        case kLayoutFused: fwd_kernel<T, CH, true, false><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
+        case kLayoutFused: fwd_kernel<T, CH, true, false, 1><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a); break;
         case kLayoutProj: {
             const size_t smem = projected_smem_bytes(a.pb);
             if (smem > 48 * 1024) {
@@ -514,11 +547,19 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
         }
         default: {
             FwdArgs f = a;
+            // Two groups per task when a group's row slice is at most half a
+            // line; a CTA then takes twice the anchors to keep its 8 warps busy.
+            constexpr int GP = CH <= 4 ? 2 : 1;
+            const bool pair = GP == 2 && a.pb.G % 2 == 0;
+            if (pair) {
+                const int tpa = a.pb.G / 2;  // tasks per anchor
+                f.pb.anchors_per_cta = tpa < kWarps ? kWarps / tpa : 1;
+            }
             f.parts = forward_parts(a.pb, ESZ);
             if (f.parts > 1 && (a.pb.K % f.parts) != 0) f.parts = 1;
-            int64_t g = grid;
+            int64_t g = sampling_grid(f.pb);
             if (f.parts > 1) {
-                f.ctas_per_part = (a.pb.A + a.pb.anchors_per_cta - 1) / a.pb.anchors_per_cta;
+                f.ctas_per_part = (a.pb.A + f.pb.anchors_per_cta - 1) / f.pb.anchors_per_cta;
                 f.kpart = a.pb.K / f.parts;
                 f.div_cpp = FastDiv::make(static_cast<uint32_t>(f.ctas_per_part));
                 f.div_kpart = FastDiv::make(static_cast<uint32_t>(f.kpart));
@@ -526,8 +567,14 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
                 const cudaError_t e = cudaMemsetAsync(a.out, 0, static_cast<size_t>(a.pb.num_ba) * a.pb.C * 4, st);
                 if (e != cudaSuccess) return e;
             }
-            if (f.parts > 1) fwd_kernel<T, CH, false, true><<<static_cast<unsigned>(g), kThreads, 0, st>>>(f);
-            else fwd_kernel<T, CH, false, false><<<static_cast<unsigned>(g), kThreads, 0, st>>>(f);
+            const dim3 gg(static_cast<unsigned>(g));
+            if (f.parts > 1) {
+                if (pair) fwd_kernel<T, CH, false, true, GP><<<gg, kThreads, 0, st>>>(f);
+                else fwd_kernel<T, CH, false, true, 1><<<gg, kThreads, 0, st>>>(f);
+            } else {
+                if (pair) fwd_kernel<T, CH, false, false, GP><<<gg, kThreads, 0, st>>>(f);
+                else fwd_kernel<T, CH, false, false, 1><<<gg, kThreads, 0, st>>>(f);
+            }
             break;
         }
     }
