@@ -34,6 +34,8 @@ namespace {
 
 __global__ void zero_fill_kernel(float4 *__restrict__ p, int64_t n4)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride)
         p[i] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -453,8 +455,8 @@ cudaError_t launch_zero_fill(float *p, int64_t n_floats, cudaStream_t st)
     if (e != cudaSuccess) return e;
     const int64_t want = (n4 + 1023) / 1024;
     const int64_t grid = want < static_cast<int64_t>(sms) * 8 ? want : static_cast<int64_t>(sms) * 8;
-    zero_fill_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(reinterpret_cast<float4 *>(p), n4);
-    return cudaGetLastError();
+    return launch_pdl(zero_fill_kernel, dim3(static_cast<unsigned>(grid)), dim3(256), 0, st,
+                      reinterpret_cast<float4 *>(p), n4);
 }
 
 cudaError_t launch_backward(const BwdArgs &a, int feat_dtype, int chunks, cudaStream_t st)

@@ -166,6 +166,8 @@ template <bool FUSED>
 __global__ void __launch_bounds__(kBinThreads) bin_count_kernel(const Problem pb, const BinArgs w,
                                                                  int ctas_per_view, int hist_rows)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     extern __shared__ int hist[];  // hist_rows entries
     __shared__ int hoff[DA_MAX_MAPS];
@@ -236,6 +238,8 @@ __device__ __forceinline__ int block_incl_scan(int v, int *warp_tot, int &total)
 // Each CTA turns kScanTile counts into tile-local exclusive offsets.
 __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t *data, int32_t *tile_sum)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int warp_tot[32];
     int4 *p = reinterpret_cast<int4 *>(data + static_cast<int64_t>(blockIdx.x) * kScanTile) + threadIdx.x;
     const int4 v = *p;
@@ -250,6 +254,8 @@ __global__ void __launch_bounds__(1024) scan_tiles_kernel(int32_t *data, int32_t
 // One CTA: exclusive scan of the tile totals; the grand total goes to `end`.
 __global__ void __launch_bounds__(1024) scan_sums_kernel(int32_t *tile_sum, int64_t ntiles, int32_t *end)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int warp_tot[32];
     int carry = 0;
     for (int64_t base = 0; base < ntiles; base += 1024) {
@@ -266,6 +272,8 @@ __global__ void __launch_bounds__(1024) scan_sums_kernel(int32_t *tile_sum, int6
 
 __global__ void __launch_bounds__(256) scan_add_kernel(int32_t *data, const int32_t *tile_sum, int64_t n4)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (i >= n4) return;
     const int add = tile_sum[(i * 4) / kScanTile];
@@ -288,6 +296,8 @@ template <bool FUSED>
 __global__ void __launch_bounds__(kBinThreads) bin_fill_kernel(const Problem pb, const BinArgs w,
                                                                 int ctas_per_view, int hist_rows)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     extern __shared__ int hist[];  // hist_rows entries
     __shared__ int hoff[DA_MAX_MAPS];
@@ -387,6 +397,8 @@ __device__ __forceinline__ int row_begin(const BinArgs &w, int64_t r) { return r
 
 __global__ void __launch_bounds__(kSortThreads) sort_short_rows_kernel(const Problem pb, const BinArgs w)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int n_list[3], base[3];
     if (threadIdx.x < 3) n_list[threadIdx.x] = 0;
     __syncthreads();
@@ -426,6 +438,8 @@ __global__ void __launch_bounds__(kSortThreads) sort_short_rows_kernel(const Pro
 // shared memory; each lane ranks its records against all of them.
 __global__ void __launch_bounds__(kSortThreads) sort_warp_rows_kernel(const Problem pb, const BinArgs w)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int2 buf[kSortThreads / 32][kSortWarpMax];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int count = w.sort_counts[0];
@@ -493,6 +507,8 @@ __device__ void block_bitonic_sort(Ptr a, int n)
 // Rows of 129..2048 records: one CTA per row, sorted in shared memory.
 __global__ void __launch_bounds__(kSortThreads) sort_cta_rows_kernel(const Problem pb, const BinArgs w)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ int2 buf[kSortSmemMax];
     const int count = w.sort_counts[1];
     const int32_t *list = w.sort_lists + w.cap_m;
@@ -514,6 +530,8 @@ __global__ void __launch_bounds__(kSortThreads) sort_cta_rows_kernel(const Probl
 // kernel, so no read-only cache path).
 __global__ void __launch_bounds__(1024) sort_long_rows_kernel(const Problem pb, const BinArgs w)
 {
+    pdl_wait();
+    pdl_trigger();
     const int count = w.sort_counts[2];
     const int32_t *list = w.sort_lists + w.cap_m + w.cap_s;
     for (int i = blockIdx.x; i < count; i += gridDim.x) {
@@ -530,6 +548,8 @@ __global__ void __launch_bounds__(1024) sort_long_rows_kernel(const Problem pb, 
 __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const BinArgs w, float *grad_loc,
                                                        float *grad_weight, int64_t pk_begin, int64_t pk_end)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
     __syncthreads();
@@ -580,6 +600,8 @@ template <int G>
 __global__ void __launch_bounds__(256) epilogue_vec_kernel(const Problem pb, const BinArgs w, float *grad_loc,
                                                            float *grad_weight, int64_t npk, int s_log2)
 {
+    pdl_wait();
+    pdl_trigger();
     static_assert(G == 4 || G == 8, "16-byte vectors of G floats");
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
@@ -644,6 +666,8 @@ __global__ void __launch_bounds__(256) epilogue_vec_kernel(const Problem pb, con
 __global__ void __launch_bounds__(256) epilogue_fused_kernel(const Problem pb, const BinArgs w, float *glw,
                                                              int64_t npk)
 {
+    pdl_wait();
+    pdl_trigger();
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
     __syncthreads();
@@ -703,53 +727,56 @@ cudaError_t launch_backward_binned(const BwdArgs &a, const BinArgs &w, int feat_
     const size_t hist_bytes = static_cast<size_t>(hist_rows) * sizeof(int);
     if (w.nsid > 0) {
         if (pb.layout == kLayoutFused)
-            bin_count_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
-                                                                                            hist_rows);
+            e = launch_pdl(bin_count_kernel<true>, dim3(static_cast<unsigned>(bin_grid)), dim3(kBinThreads),
+                hist_bytes, st, pb, w, ctas_per_view, hist_rows);
         else
-            bin_count_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
-                                                                                            hist_rows);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            e = launch_pdl(bin_count_kernel<false>, dim3(static_cast<unsigned>(bin_grid)), dim3(kBinThreads),
+                hist_bytes, st, pb, w, ctas_per_view, hist_rows);
+        if (e != cudaSuccess) return e;
     }
     // 2. offsets
     if (w.ntiles > 0) {
-        scan_tiles_kernel<<<static_cast<unsigned>(w.ntiles), 1024, 0, st>>>(w.row_off, w.tile_sum);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        scan_sums_kernel<<<1, 1024, 0, st>>>(w.tile_sum, w.ntiles, w.row_off + w.ntiles * kScanTile);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(scan_tiles_kernel, dim3(static_cast<unsigned>(w.ntiles)), dim3(1024), 0, st,
+            w.row_off, w.tile_sum);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(scan_sums_kernel, dim3(1), dim3(1024), 0, st,
+            w.tile_sum, w.ntiles, w.row_off + w.ntiles * kScanTile);
+        if (e != cudaSuccess) return e;
         const int64_t n4 = w.ntiles * kScanTile / 4;
-        scan_add_kernel<<<static_cast<unsigned>((n4 + 255) / 256), 256, 0, st>>>(w.row_off, w.tile_sum, n4);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(scan_add_kernel, dim3(static_cast<unsigned>((n4 + 255) / 256)), dim3(256), 0, st,
+            w.row_off, w.tile_sum, n4);
+        if (e != cudaSuccess) return e;
     }
     // 3. records
     if (w.nsid > 0) {
         if (pb.layout == kLayoutFused)
-            bin_fill_kernel<true><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
-                                                                                            hist_rows);
+            e = launch_pdl(bin_fill_kernel<true>, dim3(static_cast<unsigned>(bin_grid)), dim3(kBinThreads),
+                hist_bytes, st, pb, w, ctas_per_view, hist_rows);
         else
-            bin_fill_kernel<false><<<static_cast<unsigned>(bin_grid), kBinThreads, hist_bytes, st>>>(pb, w, ctas_per_view,
-                                                                                            hist_rows);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+            e = launch_pdl(bin_fill_kernel<false>, dim3(static_cast<unsigned>(bin_grid)), dim3(kBinThreads),
+                hist_bytes, st, pb, w, ctas_per_view, hist_rows);
+        if (e != cudaSuccess) return e;
     }
     // 3b. deterministic order inside every row
     if (w.sort_lists && w.nsid > 0 && w.rows_total > 0) {
         const int64_t g1 = (w.rows_total + kSortThreads - 1) / kSortThreads;
-        sort_short_rows_kernel<<<static_cast<unsigned>(g1), kSortThreads, 0, st>>>(pb, w);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(sort_short_rows_kernel, dim3(static_cast<unsigned>(g1)), dim3(kSortThreads), 0, st, pb, w);
+        if (e != cudaSuccess) return e;
         int dev = 0, sms = 0;
         if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
         if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
         // Persistent grids over the row lists (their lengths are on the device).
-        sort_warp_rows_kernel<<<static_cast<unsigned>(sms * 8), kSortThreads, 0, st>>>(pb, w);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(sort_warp_rows_kernel, dim3(static_cast<unsigned>(sms * 8)), dim3(kSortThreads), 0, st, pb, w);
+        if (e != cudaSuccess) return e;
         // Sixteen CTAs per SM, twice the resident maximum: each row's bitonic
         // network is a chain of short barrier-separated stages, so the kernel
         // is latency-bound and more CTAs in flight help. Deterministic
         // backward at the 6-camera training shape: 947 us with 4 CTAs per SM,
         // 931 us with 8, 927 us with 16.
-        sort_cta_rows_kernel<<<static_cast<unsigned>(sms * 16), kSortThreads, 0, st>>>(pb, w);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
-        sort_long_rows_kernel<<<static_cast<unsigned>(sms), 1024, 0, st>>>(pb, w);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(sort_cta_rows_kernel, dim3(static_cast<unsigned>(sms * 16)), dim3(kSortThreads), 0, st, pb, w);
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(sort_long_rows_kernel, dim3(static_cast<unsigned>(sms)), dim3(1024), 0, st, pb, w);
+        if (e != cudaSuccess) return e;
     }
     }
 pull_stage:
@@ -761,8 +788,9 @@ pull_stage:
     }
     // 5. grad_weight and grad_loc
     if (npk > 0 && pb.layout == kLayoutFused) {
-        epilogue_fused_kernel<<<static_cast<unsigned>((npk + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc, npk);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_pdl(epilogue_fused_kernel, dim3(static_cast<unsigned>((npk + 255) / 256)), dim3(256), 0, st,
+            pb, w, a.grad_loc, npk);
+        if (e != cudaSuccess) return e;
     } else if (npk > 0) {
         // The vector kernel reads weights and writes grad_weight as 16-byte
         // vectors; the interface promises only 4-byte alignment for those.
@@ -776,14 +804,16 @@ pull_stage:
             const int64_t threads = npk << s_log2;
             const unsigned grid = static_cast<unsigned>((threads + 255) / 256);
             if (pb.G == 8)
-                epilogue_vec_kernel<8><<<grid, 256, 0, st>>>(pb, w, a.grad_loc, a.grad_weight, npk, s_log2);
+                e = launch_pdl(epilogue_vec_kernel<8>, dim3(grid), dim3(256), 0, st,
+                    pb, w, a.grad_loc, a.grad_weight, npk, s_log2);
             else
-                epilogue_vec_kernel<4><<<grid, 256, 0, st>>>(pb, w, a.grad_loc, a.grad_weight, npk, s_log2);
+                e = launch_pdl(epilogue_vec_kernel<4>, dim3(grid), dim3(256), 0, st,
+                    pb, w, a.grad_loc, a.grad_weight, npk, s_log2);
         } else {
-            epilogue_kernel<<<static_cast<unsigned>((npk * 32 + 255) / 256), 256, 0, st>>>(pb, w, a.grad_loc,
-                                                                                             a.grad_weight, 0, npk);
+            e = launch_pdl(epilogue_kernel, dim3(static_cast<unsigned>((npk * 32 + 255) / 256)), dim3(256), 0, st,
+                pb, w, a.grad_loc, a.grad_weight, 0, npk);
         }
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }

@@ -436,6 +436,34 @@ __device__ __forceinline__ void red_add_v4_if(bool pred, float *p, float a, floa
 // four corner groups of a warp read conflict-free.
 constexpr int kTabPitch = 36;
 
+// Programmatic dependent launch for the kernels of one call that follow one
+// another on a stream (the binned backward's chain): such a kernel may be
+// scheduled while its predecessor drains, so its launch and CTA start-up
+// overlap the predecessor's last wave. Every kernel launched this way calls
+// pdl_wait() before any global memory access: it returns once the preceding
+// kernels of the stream have completed and their writes are visible (at
+// once when there is no programmatic dependency). pdl_trigger() lets the
+// next kernel launch once every CTA of this one has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args... args)
+{
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Stage the map table of the kernel parameters in shared memory: lanes index
 // it with divergent (k, s), which the constant bank would serialise.
 __device__ __forceinline__ void stage_maps(const Problem &pb, MapInfo *maps_s)

@@ -207,6 +207,8 @@ __host__ __device__ inline size_t pull_smem_per_warp(int slots, int G)
 template <typename T, int LPR, int LPG, bool FUSED, bool V8>
 __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs args)
 {
+    pdl_wait();
+    pdl_trigger();
     constexpr int RPW = 32 / LPR;
     constexpr int CH = LPR >= 4 ? LPR : 4;
     constexpr int RPL = CH / LPR;  // records each lane decodes per chunk
@@ -358,14 +360,12 @@ cudaError_t launch_pull_kernel(const PullArgs &pa, cudaStream_t st)
         constexpr int CH = LPR >= 4 ? LPR : 4;
         const size_t smem = pull_smem_per_warp(RPW * CH, pa.pb.G) * (kPullThreads / 32);
         const dim3 g(static_cast<unsigned>(grid));
-        if (pa.pb.layout == kLayoutFused) {
-            if (v8) pull_kernel<T, LPR, LPG, true, true><<<g, kPullThreads, smem, st>>>(p);
-            else pull_kernel<T, LPR, LPG, true, false><<<g, kPullThreads, smem, st>>>(p);
-        } else {
-            if (v8) pull_kernel<T, LPR, LPG, false, true><<<g, kPullThreads, smem, st>>>(p);
-            else pull_kernel<T, LPR, LPG, false, false><<<g, kPullThreads, smem, st>>>(p);
-        }
-        return cudaGetLastError();
+        const dim3 blk(kPullThreads);
+        if (pa.pb.layout == kLayoutFused)
+            return v8 ? launch_pdl(pull_kernel<T, LPR, LPG, true, true>, g, blk, smem, st, p)
+                      : launch_pdl(pull_kernel<T, LPR, LPG, true, false>, g, blk, smem, st, p);
+        return v8 ? launch_pdl(pull_kernel<T, LPR, LPG, false, true>, g, blk, smem, st, p)
+                  : launch_pdl(pull_kernel<T, LPR, LPG, false, false>, g, blk, smem, st, p);
     }
 }
 
