@@ -89,6 +89,8 @@ __device__ __forceinline__ void row_sum_store(const float (&d)[4], int chunk, fl
 template <typename T, int CH, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 4) bwd_kernel(const BwdArgs args)
 {
+    pdl_wait();
+    pdl_trigger();
     using Ck = Chunk<T>;
     constexpr int VEC = Ck::kVec;
     constexpr int ESZ = 16 / VEC;
@@ -270,6 +272,8 @@ constexpr int kSmallUnroll = 3;
 template <typename T, bool FUSED>
 __global__ void __launch_bounds__(kThreads) bwd_small_kernel(const BwdArgs args, int cpa_log2, int ch)
 {
+    pdl_wait();
+    pdl_trigger();
     using Ck = Chunk<T>;
     constexpr int VEC = Ck::kVec;
     constexpr int ESZ = 16 / VEC;
@@ -408,8 +412,8 @@ cudaError_t launch_layout(const BwdArgs &a, cudaStream_t st)
             const int64_t threads = static_cast<int64_t>(a.pb.num_ba) << cpa_log2;
             const int64_t grid = (threads + kThreads - 1) / kThreads;
             if (grid == 0) return cudaSuccess;
-            bwd_small_kernel<T, FUSED><<<static_cast<unsigned>(grid), kThreads, 0, st>>>(a, cpa_log2, CH);
-            return cudaGetLastError();
+            return launch_pdl(bwd_small_kernel<T, FUSED>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, st, a,
+                              cpa_log2, CH);
         }
     }
     const int64_t views = static_cast<int64_t>(a.pb.num_ba) * a.pb.K;
@@ -421,8 +425,7 @@ cudaError_t launch_layout(const BwdArgs &a, cudaStream_t st)
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
     }
-    bwd_kernel<T, CH, FUSED><<<static_cast<unsigned>(grid), kThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(bwd_kernel<T, CH, FUSED>, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, st, a);
 }
 
 template <typename T, int CH>

@@ -21,6 +21,8 @@ namespace {
 __global__ void __launch_bounds__(256) logits_grad_kernel(const Problem pb, const float *w, const float *gw,
                                                           float *glog)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t task = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (task >= static_cast<int64_t>(pb.num_ba) * pb.G) return;  // whole warps leave together
@@ -47,6 +49,8 @@ __global__ void __launch_bounds__(256) logits_grad_kernel(const Problem pb, cons
 __global__ void __launch_bounds__(256) logits_grad_anchor_kernel(const Problem pb, const float *w, const float *gw,
                                                                  float *glog)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t ba = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (ba >= pb.num_ba) return;  // whole warps leave together
@@ -60,6 +64,8 @@ __global__ void __launch_bounds__(256) logits_grad_anchor_kernel(const Problem p
 
 __global__ void __launch_bounds__(256) keypoint_grad_kernel(const Problem pb, const float *grad_loc, float *gkp)
 {
+    pdl_wait();
+    pdl_trigger();
     const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;  // (b*A + a)*P + p
     if (i >= static_cast<int64_t>(pb.num_ba) * pb.P) return;
     const int ba = static_cast<int>(pb.div_P.div(static_cast<uint32_t>(i)));
@@ -92,19 +98,20 @@ cudaError_t launch_projected_chain(const Problem &pb, const float *weights, cons
 {
     const int64_t tasks = static_cast<int64_t>(pb.num_ba) * pb.G;
     if (tasks > 0 && pb.pks > 0) {
-        if (32 % pb.G == 0)
-            logits_grad_anchor_kernel<<<static_cast<unsigned>((static_cast<int64_t>(pb.num_ba) * 32 + 255) / 256), 256,
-                                        0, st>>>(pb, weights, grad_weight, grad_logits);
-        else
-            logits_grad_kernel<<<static_cast<unsigned>((tasks * 32 + 255) / 256), 256, 0, st>>>(pb, weights, grad_weight,
-                                                                                              grad_logits);
-        const cudaError_t e = cudaGetLastError();
+        const cudaError_t e =
+            32 % pb.G == 0
+                ? launch_pdl(logits_grad_anchor_kernel,
+                             dim3(static_cast<unsigned>((static_cast<int64_t>(pb.num_ba) * 32 + 255) / 256)), dim3(256),
+                             0, st, pb, weights, grad_weight, grad_logits)
+                : launch_pdl(logits_grad_kernel, dim3(static_cast<unsigned>((tasks * 32 + 255) / 256)), dim3(256), 0,
+                             st, pb, weights, grad_weight, grad_logits);
         if (e != cudaSuccess) return e;
     }
     const int64_t pts = static_cast<int64_t>(pb.num_ba) * pb.P;
     if (pts > 0) {
-        keypoint_grad_kernel<<<static_cast<unsigned>((pts + 255) / 256), 256, 0, st>>>(pb, grad_loc, grad_keypoints);
-        return cudaGetLastError();
+        const cudaError_t e = launch_pdl(keypoint_grad_kernel, dim3(static_cast<unsigned>((pts + 255) / 256)), dim3(256),
+                                         0, st, pb, grad_loc, grad_keypoints);
+        if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
