@@ -4,6 +4,10 @@
 // corner contributions that the binning (da_backward_binned.cu) sorted by
 // feature row, together with d = feat_row . grad_out per record and group,
 // from which grad_weight and grad_loc follow.
+#include <algorithm>
+#include <cmath>
+
+
 #include "da_internal.cuh"
 
 namespace da {
@@ -131,13 +135,24 @@ __device__ __forceinline__ void load_feat8(const void *p, float (&v)[8])
     }
 }
 
+// How the rows are shared out. kRowsAll: one warp per feature row (LPR
+// lanes per row), over every row. With row groups (pull_plan) the maps whose
+// rows hold few records each are pulled in groups of consecutive rows, one
+// group per warp (pull_group_kernel), and the other maps one row per warp
+// (kRowsCoarse, the rows enumerated through pb.maps[].pad).
+constexpr int kRowsAll = 0, kRowsCoarse = 1, kRowGroups = 2;
+
 struct PullArgs {
-    Problem pb;
+    Problem pb;  // with row groups, pb.maps[i].pad: map i's first unit (row or group) of its kind
     const float *grad_out;
     float *grad_feat;
     BinArgs w;
-    int64_t row_begin, row_end;  // feature rows this launch covers
+    int64_t row_begin, row_end;  // units this launch covers: rows (kRowsAll, kRowsCoarse) or groups
     int weights_v8;              // G == 8 and weights 32-byte aligned: one 256-bit load per sample
+    int mode;                    // kRowsAll, kRowsCoarse or kRowGroups
+    int64_t units_per_b;         // kRowsCoarse, kRowGroups: units per batch item
+    uint64_t group_maps;         // bit i: map i is pulled in row groups
+    uint8_t rw_log[DA_MAX_MAPS]; // log2 of the rows per group of each grouped map
 };
 
 // 4 warps per CTA. The register-limited occupancy (32 warps per SM) is the
@@ -236,8 +251,20 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
     // footprint covers 2x2 pixels). Walking 2x2 pixel blocks one pixel after
     // another in one warp instead measured slower (L1 hit rate 21 % against
     // 38 %): the reuse comes from warps running side by side.
-    const int64_t R = args.row_end - 1 - (warp_id * RPW + q);
+    int64_t R = args.row_end - 1 - (warp_id * RPW + q);
     const bool active = R >= args.row_begin;
+    if (args.mode == kRowsCoarse && active) {
+        // Unit R is row ul of the ungrouped maps of batch item bu.
+        const int64_t bu = R / args.units_per_b;
+        const int64_t ul = R - bu * args.units_per_b;
+        int64_t rr = 0;
+        for (int i = 0; i < pb.nmaps; ++i) {
+            const MapInfo mm = pb.maps[i];
+            if (!((args.group_maps >> i) & 1) && ul >= mm.pad && ul < mm.pad + static_cast<int64_t>(mm.H) * mm.W)
+                rr = mm.start + (ul - mm.pad);
+        }
+        R = bu * pb.rows + rr;
+    }
     const int b = active ? static_cast<int>(pb.div_rows.div(static_cast<uint32_t>(R))) : 0;
     const int jb = active ? (R > 0 ? w.row_off[R - 1] : 0) : 0;
     const int je = active ? w.row_off[R] : 0;
@@ -339,6 +366,321 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
     }
 }
 
+// ------------------------------------------------------------ row groups
+//
+// A feature row of a fine map holds few records (at the 6-camera training
+// shape, 4 on the 64x176 maps): a warp that pulls one such row spends most of
+// its time on the chain of dependent loads that precedes its walk (row
+// offsets, then records, then weights and grad_out rows). There a warp takes
+// a group of consecutive rows of one map instead, whose records are one
+// contiguous run of the record array: it walks that run as one stream,
+// in chunks and batches as the per-row pull does, and switches rows where the
+// row offsets say. The rows' features come through a small shared-memory
+// ring filled by asynchronous copies kGroupFeatAhead rows ahead.
+
+constexpr int kGroupFeatAhead = 2;   // feature rows in flight per warp (4 measured slower)
+constexpr int kGroupMaxRows = 16;    // rows per group: a warp's lanes hold the group's row offsets
+
+// 16-byte chunk c of a 1 KB feature row sits at chunk c ^ ((c >> 3) & 7) of
+// its ring slot: each lane copies two chunks of the row and reads two others
+// (8 channels of its own), and both patterns then hit 32 distinct banks per
+// quarter-warp.
+__device__ __forceinline__ int ring_chunk(int c) { return c ^ ((c >> 3) & 7); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+__host__ __device__ inline size_t group_smem_per_warp(int G)
+{
+    return pull_smem_per_warp(32, G) + static_cast<size_t>(kGroupFeatAhead) * 1024;
+}
+
+// Starts the copy of feature row `row` (C = 256 channels of T) into a ring
+// slot: lane l copies chunks l and 32 + l (fp32) or chunk l (16-bit).
+template <typename T>
+__device__ __forceinline__ void group_copy_row(uint32_t slot, const Problem &pb, int64_t row, int lane)
+{
+    constexpr int ESZ = sizeof(T) == 4 ? 4 : 2;
+    const char *src = static_cast<const char *>(pb.feat) + row * 256 * ESZ;
+    cp_async16(slot + ring_chunk(lane) * 16, src + lane * 16);
+    if constexpr (ESZ == 4) cp_async16(slot + ring_chunk(32 + lane) * 16, src + 512 + lane * 16);
+}
+
+// The lane's 8 channels (8l..8l+7) of the row in a ring slot, widened.
+template <typename T>
+__device__ __forceinline__ void group_read_row(const unsigned char *slot, int lane, float (&v)[8])
+{
+    if constexpr (sizeof(T) == 4) {
+        const float4 a = *reinterpret_cast<const float4 *>(slot + ring_chunk(2 * lane) * 16);
+        const float4 c = *reinterpret_cast<const float4 *>(slot + ring_chunk(2 * lane + 1) * 16);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+    } else {
+        Chunk<T>::unpack(*reinterpret_cast<const uint4 *>(slot + ring_chunk(lane) * 16), v);
+    }
+}
+
+// One warp per group of consecutive rows of one grouped map, C = 256 (lane
+// l: channels 8l..8l+7 of all groups). Groups are taken from the end, as
+// rows are in pull_kernel.
+//   - lanes 0..nr load the begin offsets of the group's rows and of the next
+//     row, so the record run is [J0, J1) and row k ends where row k+1 begins;
+//   - the first kGroupFeatAhead rows' features are copied into the ring;
+//   - the run is decoded 32 records at a time into the warp's table (as in
+//     pull_kernel) and walked four at a time; before a record is applied,
+//     every row that ends at or before it is finished: its grad_feat is
+//     stored, the next row's features are read from the ring and the row
+//     kGroupFeatAhead ahead is copied into the freed slot;
+//   - rows after the last record are stored as zeros.
+// 80 registers, 6 CTAs (24 warps) per SM: pull + epilogue 612 us at the
+// training shape, against 630 us with 5 CTAs (94 registers), 624 us with 7
+// (72, with spills) and 791 us with 8 (64, more spills).
+template <typename T, int LPG, bool V8>
+__global__ void __launch_bounds__(kPullThreads, 6) pull_group_kernel(const PullArgs args)
+{
+    pdl_wait();
+    pdl_trigger();
+    constexpr int CH = 32;
+    constexpr int WP = pull_wpitch(CH);
+    extern __shared__ __align__(16) unsigned char pull_smem[];
+    const Problem &pb = args.pb;
+    const BinArgs &w = args.w;
+    const int G = pb.G;
+    const int lane = threadIdx.x & 31;
+    const int g = lane / LPG, gsub = lane % LPG;
+    unsigned char *wbase = pull_smem + (threadIdx.x >> 5) * group_smem_per_warp(G);
+    int2 *meta = reinterpret_cast<int2 *>(wbase);
+    int *ksm = reinterpret_cast<int *>(meta + CH);
+    float *wsm = reinterpret_cast<float *>(ksm + CH);
+    unsigned char *ring = wbase + pull_smem_per_warp(CH, G);
+    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
+
+    const int64_t gid = args.row_end - 1 - ((static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5);
+    if (gid < args.row_begin) return;  // the whole warp
+    const int b = static_cast<int>(gid / args.units_per_b);
+    const int64_t gl = gid - static_cast<int64_t>(b) * args.units_per_b;
+    int mi = 0;
+    for (int i = 0; i < pb.nmaps; ++i) {
+        const MapInfo mm = pb.maps[i];
+        const int rl = args.rw_log[i];
+        const int64_t ng = ((static_cast<int64_t>(mm.H) * mm.W) + (1 << rl) - 1) >> rl;
+        if (((args.group_maps >> i) & 1) && gl >= mm.pad && gl < mm.pad + ng) mi = i;
+    }
+    const MapInfo m = pb.maps[mi];
+    const int rl = args.rw_log[mi];
+    const int first = static_cast<int>(gl - m.pad) << rl;
+    const int nr = min(1 << rl, m.H * m.W - first);
+    const int64_t R0 = static_cast<int64_t>(b) * pb.rows + m.start + first;
+    int rb = 0;  // lane k <= nr: where row R0 + k begins
+    if (lane <= nr) rb = R0 + lane > 0 ? w.row_off[R0 + lane - 1] : 0;
+    const int J0 = __shfl_sync(0xffffffffu, rb, 0), J1 = __shfl_sync(0xffffffffu, rb, nr);
+    const float *go_b = args.grad_out + static_cast<int64_t>(b) * pb.A * pb.C + lane * 8;
+    const int abase = b * pb.A;
+
+#pragma unroll
+    for (int k = 0; k < kGroupFeatAhead; ++k) {
+        if (k < nr) group_copy_row<T>(ring_s + k * 1024, pb, R0 + k, lane);
+        cp_async_commit();
+    }
+    // Row `cur` of the group is the one being summed; it ends at cur_end.
+    int cur = 0;
+    int cur_end = __shfl_sync(0xffffffffu, rb, 1);
+    float2 v2[4], acc2[4];
+    // Takes row `cur`'s features from its ring slot and refills the slot
+    // with the row kGroupFeatAhead ahead.
+    auto next_feats = [&]() {
+        cp_async_wait<kGroupFeatAhead - 1>();
+        __syncwarp();
+        const int slot = cur % kGroupFeatAhead;
+        float v[8];
+        group_read_row<T>(ring + slot * 1024, lane, v);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v2[c] = make_float2(v[2 * c], v[2 * c + 1]);
+        __syncwarp();
+        if (cur + kGroupFeatAhead < nr) group_copy_row<T>(ring_s + slot * 1024, pb, R0 + cur + kGroupFeatAhead, lane);
+        cp_async_commit();
+    };
+    auto store_row = [&](int k) {
+        const float4 a0 = make_float4(acc2[0].x, acc2[0].y, acc2[1].x, acc2[1].y);
+        const float4 a1 = make_float4(acc2[2].x, acc2[2].y, acc2[3].x, acc2[3].y);
+        float *gf = args.grad_feat + (R0 + k) * pb.C + lane * 8;
+        if constexpr (V8) {
+            stg_v8(gf, a0, a1);
+        } else {
+            reinterpret_cast<float4 *>(gf)[0] = a0;
+            reinterpret_cast<float4 *>(gf)[1] = a1;
+        }
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc2[c] = make_float2(0.f, 0.f);
+    };
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc2[c] = make_float2(0.f, 0.f);
+    next_feats();
+
+    for (int k0 = J0; k0 < J1; k0 += CH) {
+        // 1. decode: lane c takes record k0 + c of the run.
+        {
+            const int c = lane;
+            bool valid = k0 + c < J1 && DA_CHECK(pb.dbg_err, k0 + c, w.ncap, kBoundsRecord);
+            const int2 r = valid ? ldg_record_stream(&w.rec[k0 + c]) : make_int2(0, 0);
+            const int sid = r.x >> 2;
+            int a = valid ? static_cast<int>(pb.div_PKS.div(sid)) - abase : 0;
+            if (valid && !(DA_CHECK(pb.dbg_err, a, pb.A, kBoundsAnchor) &&
+                           DA_CHECK(pb.dbg_err, sid, w.nsid, kBoundsSample))) {
+                valid = false;
+                a = 0;
+            }
+            meta[c] = make_int2(a, valid ? r.y : 0);
+            ksm[c] = r.x;
+            const float *wp = pb.weights + static_cast<int64_t>(sid) * G;
+            if (args.weights_v8) {
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f), y = x;
+                if (valid) ldg_v8_stream(wp, x, y);
+                const float wv[8] = {x.x, x.y, x.z, x.w, y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int gg = 0; gg < 8; ++gg) wsm[gg * WP + c] = wv[gg];
+            } else {
+                for (int gg = 0; gg < G; ++gg) wsm[gg * WP + c] = valid ? __ldg(wp + gg) : 0.f;
+            }
+        }
+        __syncwarp();
+        // 2. walk four records at a time, finishing rows as their ends pass.
+        const int nb = min(CH, J1 - k0);
+        const float *wrow = wsm + g * WP;
+        for (int u0 = 0; u0 < nb; u0 += 4) {
+            const int4 m01 = *reinterpret_cast<const int4 *>(meta + u0);
+            const int4 m23 = *reinterpret_cast<const int4 *>(meta + u0 + 2);
+            const float4 w4 = *reinterpret_cast<const float4 *>(wrow + u0);
+            const int an[4] = {m01.x, m01.z, m23.x, m23.z};
+            const float tw[4] = {__int_as_float(m01.y) * w4.x, __int_as_float(m01.w) * w4.y,
+                                 __int_as_float(m23.y) * w4.z, __int_as_float(m23.w) * w4.w};
+            float4 x[4], y[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if constexpr (V8) ldg_v8_keep(go_b + static_cast<int64_t>(an[u]) * pb.C, x[u], y[u]);
+                else ldg_f32x8<V8>(go_b + static_cast<int64_t>(an[u]) * pb.C, x[u], y[u]);
+            }
+            float d[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                d[u] = 0.f;
+                if (u0 + u < nb) {
+                    while (k0 + u0 + u >= cur_end) {  // the same for every lane
+                        store_row(cur);
+                        ++cur;
+                        cur_end = __shfl_sync(0xffffffffu, rb, cur + 1);
+                        next_feats();
+                    }
+                    d[u] = record_fma2(v2, x[u], y[u], tw[u], acc2);
+                }
+            }
+            const int4 k4 = *reinterpret_cast<const int4 *>(ksm + u0);
+            const int keys[4] = {k4.x, k4.y, k4.z, k4.w};
+            group_sum_store<LPG>(d, gsub, nb - u0, w.dpix + g, keys, G, pb.dbg_err, w.ncap);
+        }
+        __syncwarp();
+    }
+    // The row being summed, then the rows with no records left.
+    store_row(cur);
+    for (int k = cur + 1; k < nr; ++k) store_row(k);
+    cp_async_wait<0>();
+}
+
+// Row groups serve the standard layout with C = 256 when the maps cover a
+// batch item's feature rows exactly (every row a pixel of one map). A map
+// whose rows would hold fewer than kGroupMaxRho records each on average
+// (4*A*P samples' corners spread over H*W rows) is grouped, with about
+// kGroupTargetRecs records per group (a power of two of rows, 2 to
+// kGroupMaxRows). Pull + epilogue at the 6-camera training shape (groups of
+// 16 rows on the 64x176 maps, 8 on the 32x88 maps): 610 us against 636 us
+// with one warp per row; 128 records per group measured as 64 (612 us),
+// 32 slower (659 us), 256 slower (629 us).
+constexpr double kGroupMaxRho = 24.0;
+constexpr double kGroupTargetRecs = 128.0;
+
+bool pull_plan(Problem &pb, PullArgs &coarse, PullArgs &grouped)
+{
+    if (pb.layout != kLayoutStd || pb.C != 256 || pb.nmaps <= 0 || pb.rows <= 0 || pb.A <= 0 || pb.P <= 0)
+        return false;
+    int order[DA_MAX_MAPS];
+    for (int i = 0; i < pb.nmaps; ++i) order[i] = i;
+    std::sort(order, order + pb.nmaps, [&](int x, int y) { return pb.maps[x].start < pb.maps[y].start; });
+    int64_t end = 0;
+    for (int i = 0; i < pb.nmaps; ++i) {
+        const MapInfo &m = pb.maps[order[i]];
+        if (m.start != end) return false;
+        end += static_cast<int64_t>(m.H) * m.W;
+    }
+    if (end != pb.rows) return false;
+    uint64_t gm = 0;
+    uint8_t rwl[DA_MAX_MAPS] = {};
+    int64_t rows = 0, groups = 0;
+    for (int i = 0; i < pb.nmaps; ++i) {
+        const MapInfo &m = pb.maps[i];
+        const int64_t px = static_cast<int64_t>(m.H) * m.W;
+        const double rho = 4.0 * pb.A * pb.P / static_cast<double>(px);
+        if (rho < kGroupMaxRho) {
+            int l = static_cast<int>(std::lround(std::log2(kGroupTargetRecs / rho)));
+            l = std::min(std::max(l, 1), 4);  // 2..kGroupMaxRows rows
+            rwl[i] = static_cast<uint8_t>(l);
+            gm |= 1ull << i;
+            pb.maps[i].pad = static_cast<int32_t>(groups);
+            groups += (px + (1 << l) - 1) >> l;
+        } else {
+            pb.maps[i].pad = static_cast<int32_t>(rows);
+            rows += px;
+        }
+    }
+    if (gm == 0) return false;
+    for (PullArgs *p : {&coarse, &grouped}) {
+        p->pb = pb;
+        p->group_maps = gm;
+        std::copy(rwl, rwl + DA_MAX_MAPS, p->rw_log);
+        p->row_begin = 0;
+    }
+    coarse.mode = kRowsCoarse;
+    coarse.units_per_b = rows;
+    coarse.row_end = rows * pb.B;
+    grouped.mode = kRowGroups;
+    grouped.units_per_b = groups;
+    grouped.row_end = groups * pb.B;
+    return true;
+}
+
+template <typename T, int LPG>
+cudaError_t launch_pull_groups(const PullArgs &pa, cudaStream_t st)
+{
+    const int64_t grid = (pa.row_end - pa.row_begin + kPullThreads / 32 - 1) / (kPullThreads / 32);
+    if (grid == 0) return cudaSuccess;
+    const bool v8 = aligned(pa.grad_out, 32) && aligned(pa.grad_feat, 32);
+    PullArgs p = pa;
+    p.weights_v8 = pa.pb.G == 8 && aligned(pa.pb.weights, 32);
+    const size_t smem = group_smem_per_warp(pa.pb.G) * (kPullThreads / 32);
+    const dim3 g(static_cast<unsigned>(grid));
+    const dim3 blk(kPullThreads);
+    return v8 ? launch_pdl(pull_group_kernel<T, LPG, true>, g, blk, smem, st, p)
+              : launch_pdl(pull_group_kernel<T, LPG, false>, g, blk, smem, st, p);
+}
+
+template <typename T>
+cudaError_t dispatch_groups(const PullArgs &pa, cudaStream_t st)
+{
+    switch (pa.pb.D / 8) {
+        case 1: return launch_pull_groups<T, 1>(pa, st);
+        case 2: return launch_pull_groups<T, 2>(pa, st);
+        case 4: return launch_pull_groups<T, 4>(pa, st);
+        case 8: return launch_pull_groups<T, 8>(pa, st);
+        case 16: return launch_pull_groups<T, 16>(pa, st);
+        case 32: return launch_pull_groups<T, 32>(pa, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 template <typename T, int LPR, int LPG>
 cudaError_t launch_pull_kernel(const PullArgs &pa, cudaStream_t st)
 {
@@ -399,7 +741,30 @@ cudaError_t dispatch_pull(const PullArgs &pa, cudaStream_t st)
 
 cudaError_t launch_pull(const BwdArgs &a, const BinArgs &w, int feat_dtype, cudaStream_t st)
 {
-    const PullArgs pa{a.pb, a.grad_out, a.grad_feat, w, 0, w.rows_total, 0};
+    PullArgs pa{};
+    pa.pb = a.pb;
+    pa.grad_out = a.grad_out;
+    pa.grad_feat = a.grad_feat;
+    pa.w = w;
+    pa.row_begin = 0;
+    pa.row_end = w.rows_total;
+    pa.mode = kRowsAll;
+    Problem pb = a.pb;
+    PullArgs grouped = pa;
+    if (pull_plan(pb, pa, grouped)) {
+        // The ungrouped (coarse) maps' rows first: they hold the most records
+        // per row, so their warps start early.
+        cudaError_t e = cudaSuccess;
+        if (pa.row_end > 0) {
+            e = feat_dtype == DA_BF16  ? dispatch_pull<Bf16Tag>(pa, st)
+                : feat_dtype == DA_F16 ? dispatch_pull<F16Tag>(pa, st)
+                                       : dispatch_pull<float>(pa, st);
+            if (e != cudaSuccess) return e;
+        }
+        return feat_dtype == DA_BF16  ? dispatch_groups<Bf16Tag>(grouped, st)
+               : feat_dtype == DA_F16 ? dispatch_groups<F16Tag>(grouped, st)
+                                      : dispatch_groups<float>(grouped, st);
+    }
     return feat_dtype == DA_BF16  ? dispatch_pull<Bf16Tag>(pa, st)
            : feat_dtype == DA_F16 ? dispatch_pull<F16Tag>(pa, st)
                                   : dispatch_pull<float>(pa, st);
