@@ -137,22 +137,23 @@ __device__ __forceinline__ void load_feat8(const void *p, float (&v)[8])
 
 // How the rows are shared out. kRowsAll: one warp per feature row (LPR
 // lanes per row), over every row. With row groups (pull_plan) the maps whose
-// rows hold few records each are pulled in groups of consecutive rows, one
-// group per warp (pull_group_kernel), and the other maps one row per warp
-// (kRowsCoarse, the rows enumerated through pb.maps[].pad).
+// rows hold few records each are pulled in runs of consecutive pixels, one
+// run per warp and four vertically adjacent runs per CTA (kRowGroups,
+// pull_groups), and the other maps one row per warp (kRowsCoarse, the
+// rows enumerated through pb.maps[].pad).
 constexpr int kRowsAll = 0, kRowsCoarse = 1, kRowGroups = 2;
 
 struct PullArgs {
-    Problem pb;  // with row groups, pb.maps[i].pad: map i's first unit (row or group) of its kind
+    Problem pb;  // with row groups, pb.maps[i].pad: map i's first unit (row or block) of its kind
     const float *grad_out;
     float *grad_feat;
     BinArgs w;
-    int64_t row_begin, row_end;  // units this launch covers: rows (kRowsAll, kRowsCoarse) or groups
+    int64_t row_begin, row_end;  // units this launch covers: rows (kRowsAll, kRowsCoarse) or blocks
     int weights_v8;              // G == 8 and weights 32-byte aligned: one 256-bit load per sample
     int mode;                    // kRowsAll, kRowsCoarse or kRowGroups
     int64_t units_per_b;         // kRowsCoarse, kRowGroups: units per batch item
     uint64_t group_maps;         // bit i: map i is pulled in row groups
-    uint8_t rw_log[DA_MAX_MAPS]; // log2 of the rows per group of each grouped map
+    uint8_t rw_log[DA_MAX_MAPS]; // log2 of the pixels per run (block width) of each grouped map
 };
 
 // 4 warps per CTA. The register-limited occupancy (32 warps per SM) is the
@@ -220,23 +221,19 @@ __host__ __device__ inline size_t pull_smem_per_warp(int slots, int G)
 // V8: grad_out, grad_feat (and fp32 features) are 32-byte aligned, so each
 // lane moves its 8 channels with one 256-bit access.
 template <typename T, int LPR, int LPG, bool FUSED, bool V8>
-__global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs args)
+__device__ __forceinline__ void pull_rows(const PullArgs &args, int64_t warp_id, unsigned char *pull_smem)
 {
-    pdl_wait();
-    pdl_trigger();
     constexpr int RPW = 32 / LPR;
     constexpr int CH = LPR >= 4 ? LPR : 4;
     constexpr int RPL = CH / LPR;  // records each lane decodes per chunk
     constexpr int SLOTS = RPW * CH;
     constexpr int ESZ = sizeof(T) == 4 ? 4 : 2;
-    extern __shared__ __align__(16) unsigned char pull_smem[];
     const Problem &pb = args.pb;
     const BinArgs &w = args.w;
     const int G = pb.G;
     const int lane = threadIdx.x & 31;
     const int q = lane / LPR, sub = lane % LPR;
     const int g = sub / LPG, gsub = sub % LPG;
-    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5;
     int2 *meta = reinterpret_cast<int2 *>(pull_smem + (threadIdx.x >> 5) * pull_smem_per_warp(SLOTS, G));
     int *ksm = reinterpret_cast<int *>(meta + SLOTS);
     float *wsm = reinterpret_cast<float *>(ksm + SLOTS);
@@ -366,88 +363,57 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
     }
 }
 
+template <typename T, int LPR, int LPG, bool FUSED, bool V8>
+__global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs args)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(16) unsigned char pull_smem[];
+    pull_rows<T, LPR, LPG, FUSED, V8>(args, (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5,
+                                      pull_smem);
+}
+
 // ------------------------------------------------------------ row groups
 //
 // A feature row of a fine map holds few records (at the 6-camera training
 // shape, 4 on the 64x176 maps): a warp that pulls one such row spends most of
 // its time on the chain of dependent loads that precedes its walk (row
 // offsets, then records, then weights and grad_out rows). There a warp takes
-// a group of consecutive rows of one map instead, whose records are one
-// contiguous run of the record array: it walks that run as one stream,
-// in chunks and batches as the per-row pull does, and switches rows where the
-// row offsets say. The rows' features come through a small shared-memory
-// ring filled by asynchronous copies kGroupFeatAhead rows ahead.
+// a run of consecutive pixels of one map row instead, whose records are one
+// contiguous run of the record array: it walks that run as one stream, in
+// chunks and batches as the per-row pull does, and switches rows where the
+// row offsets say. The four warps of a CTA take the same columns of four
+// consecutive map rows, so vertically adjacent pixels, which share the
+// samples whose footprints straddle them, are walked side by side and their
+// grad_out rows meet in L1.
 
-constexpr int kGroupFeatAhead = 2;   // feature rows in flight per warp (4 measured slower)
-constexpr int kGroupMaxRows = 16;    // rows per group: a warp's lanes hold the group's row offsets
+constexpr int kGroupMaxRows = 16;    // pixels per warp: the warp's lanes hold their row offsets
 
-// 16-byte chunk c of a 1 KB feature row sits at chunk c ^ ((c >> 3) & 7) of
-// its ring slot: each lane copies two chunks of the row and reads two others
-// (8 channels of its own), and both patterns then hit 32 distinct banks per
-// quarter-warp.
-__device__ __forceinline__ int ring_chunk(int c) { return c ^ ((c >> 3) & 7); }
+__host__ __device__ inline size_t group_smem_per_warp(int G) { return pull_smem_per_warp(32, G); }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src)
-{
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-__host__ __device__ inline size_t group_smem_per_warp(int G)
-{
-    return pull_smem_per_warp(32, G) + static_cast<size_t>(kGroupFeatAhead) * 1024;
-}
-
-// Starts the copy of feature row `row` (C = 256 channels of T) into a ring
-// slot: lane l copies chunks l and 32 + l (fp32) or chunk l (16-bit).
-template <typename T>
-__device__ __forceinline__ void group_copy_row(uint32_t slot, const Problem &pb, int64_t row, int lane)
-{
-    constexpr int ESZ = sizeof(T) == 4 ? 4 : 2;
-    const char *src = static_cast<const char *>(pb.feat) + row * 256 * ESZ;
-    cp_async16(slot + ring_chunk(lane) * 16, src + lane * 16);
-    if constexpr (ESZ == 4) cp_async16(slot + ring_chunk(32 + lane) * 16, src + 512 + lane * 16);
-}
-
-// The lane's 8 channels (8l..8l+7) of the row in a ring slot, widened.
-template <typename T>
-__device__ __forceinline__ void group_read_row(const unsigned char *slot, int lane, float (&v)[8])
-{
-    if constexpr (sizeof(T) == 4) {
-        const float4 a = *reinterpret_cast<const float4 *>(slot + ring_chunk(2 * lane) * 16);
-        const float4 c = *reinterpret_cast<const float4 *>(slot + ring_chunk(2 * lane + 1) * 16);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
-    } else {
-        Chunk<T>::unpack(*reinterpret_cast<const uint4 *>(slot + ring_chunk(lane) * 16), v);
-    }
-}
-
-// One warp per group of consecutive rows of one grouped map, C = 256 (lane
-// l: channels 8l..8l+7 of all groups). Groups are taken from the end, as
-// rows are in pull_kernel.
-//   - lanes 0..nr load the begin offsets of the group's rows and of the next
+// One CTA per block of 4 map rows x RW columns of a grouped map, C = 256
+// (lane l: channels 8l..8l+7 of all groups); warp w takes the RW (or fewer,
+// at the right edge) pixels of map row 4*by + w. Blocks are taken from the
+// end, as rows are in pull_kernel.
+//   - lanes 0..nr load the begin offsets of the warp's rows and of the next
 //     row, so the record run is [J0, J1) and row k ends where row k+1 begins;
-//   - the first kGroupFeatAhead rows' features are copied into the ring;
+//   - the first row's features are loaded, and the next row's one row ahead
+//     (with an L2 prefetch four rows ahead);
 //   - the run is decoded 32 records at a time into the warp's table (as in
 //     pull_kernel) and walked four at a time; before a record is applied,
 //     every row that ends at or before it is finished: its grad_feat is
-//     stored, the next row's features are read from the ring and the row
-//     kGroupFeatAhead ahead is copied into the freed slot;
+//     stored and the next row's features take its place;
 //   - rows after the last record are stored as zeros.
-// 80 registers, 6 CTAs (24 warps) per SM: pull + epilogue 612 us at the
-// training shape, against 630 us with 5 CTAs (94 registers), 624 us with 7
-// (72, with spills) and 791 us with 8 (64, more spills).
+// 80 registers, 6 CTAs (24 warps) per SM. Pull + epilogue at the training
+// shape: 589 us; 605 us with 5 CTAs per SM (94 registers); with one warp per
+// 16 pixels of a map row and the CTA's warps on consecutive runs of one map
+// row, 615 us (feature rows in registers) or 608 us (through a shared-memory
+// ring of cp.async copies).
 template <typename T, int LPG, bool V8>
-__global__ void __launch_bounds__(kPullThreads, 6) pull_group_kernel(const PullArgs args)
+__device__ __forceinline__ void pull_groups(const PullArgs &args, int64_t block, unsigned char *pull_smem)
 {
-    pdl_wait();
-    pdl_trigger();
     constexpr int CH = 32;
     constexpr int WP = pull_wpitch(CH);
-    extern __shared__ __align__(16) unsigned char pull_smem[];
     const Problem &pb = args.pb;
     const BinArgs &w = args.w;
     const int G = pb.G;
@@ -457,24 +423,30 @@ __global__ void __launch_bounds__(kPullThreads, 6) pull_group_kernel(const PullA
     int2 *meta = reinterpret_cast<int2 *>(wbase);
     int *ksm = reinterpret_cast<int *>(meta + CH);
     float *wsm = reinterpret_cast<float *>(ksm + CH);
-    unsigned char *ring = wbase + pull_smem_per_warp(CH, G);
-    const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(ring));
 
-    const int64_t gid = args.row_end - 1 - ((static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5);
-    if (gid < args.row_begin) return;  // the whole warp
-    const int b = static_cast<int>(gid / args.units_per_b);
-    const int64_t gl = gid - static_cast<int64_t>(b) * args.units_per_b;
+    // CTA unit: a block of 4 map rows x RW columns; warp w takes map row
+    // 4*by + w, so the CTA's warps walk vertically adjacent pixels side by side.
+    const int64_t cid = args.row_end - 1 - block;
+    if (cid < args.row_begin) return;
+    const int b = static_cast<int>(cid / args.units_per_b);
+    const int64_t gl = cid - static_cast<int64_t>(b) * args.units_per_b;
     int mi = 0;
     for (int i = 0; i < pb.nmaps; ++i) {
         const MapInfo mm = pb.maps[i];
         const int rl = args.rw_log[i];
-        const int64_t ng = ((static_cast<int64_t>(mm.H) * mm.W) + (1 << rl) - 1) >> rl;
+        const int64_t nbx = (mm.W + (1 << rl) - 1) >> rl;
+        const int64_t ng = ((mm.H + 3) / 4) * nbx;
         if (((args.group_maps >> i) & 1) && gl >= mm.pad && gl < mm.pad + ng) mi = i;
     }
     const MapInfo m = pb.maps[mi];
     const int rl = args.rw_log[mi];
-    const int first = static_cast<int>(gl - m.pad) << rl;
-    const int nr = min(1 << rl, m.H * m.W - first);
+    const int nbx = (m.W + (1 << rl) - 1) >> rl;
+    const int ul = static_cast<int>(gl - m.pad);
+    const int by = ul / nbx, bx = ul - by * nbx;
+    const int my = 4 * by + (threadIdx.x >> 5);
+    if (my >= m.H) return;  // the whole warp
+    const int first = my * m.W + (bx << rl);
+    const int nr = min(1 << rl, m.W - (bx << rl));
     const int64_t R0 = static_cast<int64_t>(b) * pb.rows + m.start + first;
     int rb = 0;  // lane k <= nr: where row R0 + k begins
     if (lane <= nr) rb = R0 + lane > 0 ? w.row_off[R0 + lane - 1] : 0;
@@ -482,28 +454,38 @@ __global__ void __launch_bounds__(kPullThreads, 6) pull_group_kernel(const PullA
     const float *go_b = args.grad_out + static_cast<int64_t>(b) * pb.A * pb.C + lane * 8;
     const int abase = b * pb.A;
 
-#pragma unroll
-    for (int k = 0; k < kGroupFeatAhead; ++k) {
-        if (k < nr) group_copy_row<T>(ring_s + k * 1024, pb, R0 + k, lane);
-        cp_async_commit();
-    }
-    // Row `cur` of the group is the one being summed; it ends at cur_end.
+    constexpr int ESZ = sizeof(T) == 4 ? 4 : 2;
+    auto feat_ptr = [&](int k) {
+        return static_cast<const char *>(pb.feat) + ((R0 + k) * pb.C + lane * 8) * ESZ;
+    };
+    // Lanes 0..(row bytes / 128 - 1) each prefetch one 128-byte line of row k.
+    auto l2_prefetch = [&](int k) {
+        if (k < nr && lane * 128 < 256 * ESZ) {
+            const char *p = static_cast<const char *>(pb.feat) + (R0 + k) * pb.C * ESZ + lane * 128;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+        }
+    };
     int cur = 0;
     int cur_end = __shfl_sync(0xffffffffu, rb, 1);
     float2 v2[4], acc2[4];
-    // Takes row `cur`'s features from its ring slot and refills the slot
-    // with the row kGroupFeatAhead ahead.
-    auto next_feats = [&]() {
-        cp_async_wait<kGroupFeatAhead - 1>();
-        __syncwarp();
-        const int slot = cur % kGroupFeatAhead;
+    float vn[8];
+    {
         float v[8];
-        group_read_row<T>(ring + slot * 1024, lane, v);
+        load_feat8<T, V8>(feat_ptr(0), v);
 #pragma unroll
         for (int c = 0; c < 4; ++c) v2[c] = make_float2(v[2 * c], v[2 * c + 1]);
-        __syncwarp();
-        if (cur + kGroupFeatAhead < nr) group_copy_row<T>(ring_s + slot * 1024, pb, R0 + cur + kGroupFeatAhead, lane);
-        cp_async_commit();
+    }
+    if (nr > 1) load_feat8<T, V8>(feat_ptr(1), vn);
+    else {
+#pragma unroll
+        for (int c = 0; c < 8; ++c) vn[c] = 0.f;
+    }
+    for (int k = 2; k < 5; ++k) l2_prefetch(k);
+    auto next_feats = [&]() {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) v2[c] = make_float2(vn[2 * c], vn[2 * c + 1]);
+        if (cur + 1 < nr) load_feat8<T, V8>(feat_ptr(cur + 1), vn);
+        l2_prefetch(cur + 4);
     };
     auto store_row = [&](int k) {
         const float4 a0 = make_float4(acc2[0].x, acc2[0].y, acc2[1].x, acc2[1].y);
@@ -520,7 +502,6 @@ __global__ void __launch_bounds__(kPullThreads, 6) pull_group_kernel(const PullA
     };
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc2[c] = make_float2(0.f, 0.f);
-    next_feats();
 
     for (int k0 = J0; k0 < J1; k0 += CH) {
         // 1. decode: lane c takes record k0 + c of the run.
@@ -588,18 +569,38 @@ __global__ void __launch_bounds__(kPullThreads, 6) pull_group_kernel(const PullA
     // The row being summed, then the rows with no records left.
     store_row(cur);
     for (int k = cur + 1; k < nr; ++k) store_row(k);
-    cp_async_wait<0>();
+}
+
+// Both kinds of unit in one launch: CTAs below n_coarse take coarse rows
+// (one warp per row, longest first), the rest take blocks of grouped maps.
+// One launch lets the blocks fill the SMs while the coarse maps' longest
+// rows are still being walked; as two launches, each ended on its own tail
+// (large_bf16, whose 10x25 maps' rows hold ~370 records: 399 us per step
+// against 358 us with one warp per row everywhere).
+template <typename T, int LPG, bool V8>
+__global__ void __launch_bounds__(kPullThreads, 6)
+    pull_hybrid_kernel(const PullArgs coarse, const PullArgs grouped, int64_t n_coarse)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(16) unsigned char pull_smem[];
+    if (static_cast<int64_t>(blockIdx.x) < n_coarse)
+        pull_rows<T, 32, LPG, false, V8>(coarse, (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5,
+                                         pull_smem);
+    else
+        pull_groups<T, LPG, V8>(grouped, static_cast<int64_t>(blockIdx.x) - n_coarse, pull_smem);
 }
 
 // Row groups serve the standard layout with C = 256 when the maps cover a
 // batch item's feature rows exactly (every row a pixel of one map). A map
 // whose rows would hold fewer than kGroupMaxRho records each on average
 // (4*A*P samples' corners spread over H*W rows) is grouped, with about
-// kGroupTargetRecs records per group (a power of two of rows, 2 to
-// kGroupMaxRows). Pull + epilogue at the 6-camera training shape (groups of
-// 16 rows on the 64x176 maps, 8 on the 32x88 maps): 610 us against 636 us
-// with one warp per row; 128 records per group measured as 64 (612 us),
-// 32 slower (659 us), 256 slower (629 us).
+// kGroupTargetRecs records per warp (runs of a power of two of pixels, 2 to
+// kGroupMaxRows). Pull + epilogue at the 6-camera training shape (runs of 16
+// pixels on the 64x176 maps, 8 on the 32x88 maps): 589 us against 636 us
+// with one warp per row. With the earlier one-warp-per-run layout, 128
+// records per run measured as 64 (610, 612 us), 32 slower (659 us), 256
+// slower (629 us).
 constexpr double kGroupMaxRho = 24.0;
 constexpr double kGroupTargetRecs = 128.0;
 
@@ -626,11 +627,12 @@ bool pull_plan(Problem &pb, PullArgs &coarse, PullArgs &grouped)
         const double rho = 4.0 * pb.A * pb.P / static_cast<double>(px);
         if (rho < kGroupMaxRho) {
             int l = static_cast<int>(std::lround(std::log2(kGroupTargetRecs / rho)));
-            l = std::min(std::max(l, 1), 4);  // 2..kGroupMaxRows rows
+            l = std::min(std::max(l, 1), 4);  // 2..kGroupMaxRows pixels
             rwl[i] = static_cast<uint8_t>(l);
             gm |= 1ull << i;
+            // Units of a grouped map: blocks of 4 map rows x 2^l columns.
             pb.maps[i].pad = static_cast<int32_t>(groups);
-            groups += (px + (1 << l) - 1) >> l;
+            groups += static_cast<int64_t>((m.H + 3) / 4) * ((m.W + (1 << l) - 1) >> l);
         } else {
             pb.maps[i].pad = static_cast<int32_t>(rows);
             rows += px;
@@ -653,30 +655,32 @@ bool pull_plan(Problem &pb, PullArgs &coarse, PullArgs &grouped)
 }
 
 template <typename T, int LPG>
-cudaError_t launch_pull_groups(const PullArgs &pa, cudaStream_t st)
+cudaError_t launch_pull_hybrid(const PullArgs &coarse, const PullArgs &grouped, cudaStream_t st)
 {
-    const int64_t grid = (pa.row_end - pa.row_begin + kPullThreads / 32 - 1) / (kPullThreads / 32);
+    const int64_t n_coarse = (coarse.row_end - coarse.row_begin + kPullThreads / 32 - 1) / (kPullThreads / 32);
+    const int64_t grid = n_coarse + (grouped.row_end - grouped.row_begin);  // one CTA per block
     if (grid == 0) return cudaSuccess;
-    const bool v8 = aligned(pa.grad_out, 32) && aligned(pa.grad_feat, 32);
-    PullArgs p = pa;
-    p.weights_v8 = pa.pb.G == 8 && aligned(pa.pb.weights, 32);
-    const size_t smem = group_smem_per_warp(pa.pb.G) * (kPullThreads / 32);
-    const dim3 g(static_cast<unsigned>(grid));
+    const bool v8 = aligned(coarse.grad_out, 32) && aligned(coarse.grad_feat, 32) &&
+                    (sizeof(T) != 4 || aligned(coarse.pb.feat, 32));
+    PullArgs c = coarse, g = grouped;
+    c.weights_v8 = g.weights_v8 = coarse.pb.G == 8 && aligned(coarse.pb.weights, 32);
+    const size_t smem = group_smem_per_warp(coarse.pb.G) * (kPullThreads / 32);
+    const dim3 gd(static_cast<unsigned>(grid));
     const dim3 blk(kPullThreads);
-    return v8 ? launch_pdl(pull_group_kernel<T, LPG, true>, g, blk, smem, st, p)
-              : launch_pdl(pull_group_kernel<T, LPG, false>, g, blk, smem, st, p);
+    return v8 ? launch_pdl(pull_hybrid_kernel<T, LPG, true>, gd, blk, smem, st, c, g, n_coarse)
+              : launch_pdl(pull_hybrid_kernel<T, LPG, false>, gd, blk, smem, st, c, g, n_coarse);
 }
 
 template <typename T>
-cudaError_t dispatch_groups(const PullArgs &pa, cudaStream_t st)
+cudaError_t dispatch_hybrid(const PullArgs &coarse, const PullArgs &grouped, cudaStream_t st)
 {
-    switch (pa.pb.D / 8) {
-        case 1: return launch_pull_groups<T, 1>(pa, st);
-        case 2: return launch_pull_groups<T, 2>(pa, st);
-        case 4: return launch_pull_groups<T, 4>(pa, st);
-        case 8: return launch_pull_groups<T, 8>(pa, st);
-        case 16: return launch_pull_groups<T, 16>(pa, st);
-        case 32: return launch_pull_groups<T, 32>(pa, st);
+    switch (coarse.pb.D / 8) {
+        case 1: return launch_pull_hybrid<T, 1>(coarse, grouped, st);
+        case 2: return launch_pull_hybrid<T, 2>(coarse, grouped, st);
+        case 4: return launch_pull_hybrid<T, 4>(coarse, grouped, st);
+        case 8: return launch_pull_hybrid<T, 8>(coarse, grouped, st);
+        case 16: return launch_pull_hybrid<T, 16>(coarse, grouped, st);
+        case 32: return launch_pull_hybrid<T, 32>(coarse, grouped, st);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -752,18 +756,9 @@ cudaError_t launch_pull(const BwdArgs &a, const BinArgs &w, int feat_dtype, cuda
     Problem pb = a.pb;
     PullArgs grouped = pa;
     if (pull_plan(pb, pa, grouped)) {
-        // The ungrouped (coarse) maps' rows first: they hold the most records
-        // per row, so their warps start early.
-        cudaError_t e = cudaSuccess;
-        if (pa.row_end > 0) {
-            e = feat_dtype == DA_BF16  ? dispatch_pull<Bf16Tag>(pa, st)
-                : feat_dtype == DA_F16 ? dispatch_pull<F16Tag>(pa, st)
-                                       : dispatch_pull<float>(pa, st);
-            if (e != cudaSuccess) return e;
-        }
-        return feat_dtype == DA_BF16  ? dispatch_groups<Bf16Tag>(grouped, st)
-               : feat_dtype == DA_F16 ? dispatch_groups<F16Tag>(grouped, st)
-                                      : dispatch_groups<float>(grouped, st);
+        return feat_dtype == DA_BF16  ? dispatch_hybrid<Bf16Tag>(pa, grouped, st)
+               : feat_dtype == DA_F16 ? dispatch_hybrid<F16Tag>(pa, grouped, st)
+                                      : dispatch_hybrid<float>(pa, grouped, st);
     }
     return feat_dtype == DA_BF16  ? dispatch_pull<Bf16Tag>(pa, st)
            : feat_dtype == DA_F16 ? dispatch_pull<F16Tag>(pa, st)
