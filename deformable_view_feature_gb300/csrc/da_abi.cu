@@ -260,6 +260,8 @@ da_status backward_impl(const da_dims &d, da::BwdArgs &a, int chunks, const floa
         w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
         w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
         w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
+        w.left = reinterpret_cast<int32_t *>(ws + L.off_left);
+        w.left_count = w.row_off + L.ntiles * da::kScanTile + 1;
         w.rows_total = L.rows_total;
         w.nsid = L.nsid;
         w.ncap = L.ncap;
@@ -493,6 +495,8 @@ da_status da_backward_bin(const da_dims *dims, const int32_t *spatial_shape, con
     w.tile_sum = reinterpret_cast<int32_t *>(ws + L.off_tile_sum);
     w.rec = reinterpret_cast<int2 *>(ws + L.off_rec);
     w.dpix = reinterpret_cast<float *>(ws + L.off_dpix);
+    w.left = reinterpret_cast<int32_t *>(ws + L.off_left);
+    w.left_count = w.row_off + L.ntiles * da::kScanTile + 1;
     w.rows_total = L.rows_total;
     w.nsid = L.nsid;
     w.ncap = L.ncap;

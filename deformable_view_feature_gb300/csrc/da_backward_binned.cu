@@ -61,6 +61,8 @@ BinLayout bin_layout(int64_t B, int64_t rows, int64_t A, int64_t P, int64_t K, i
     o = align256(o + static_cast<size_t>(L.ncap) * 8);
     L.off_dpix = o;
     o = align256(o + static_cast<size_t>(L.ncap) * static_cast<size_t>(G) * 4);
+    L.off_left = o;
+    o = align256(o + static_cast<size_t>(L.rows_total) * 4);
     // A row holds more than 8 (128, 2048) records in at most ncap/9
     // (ncap/129, ncap/2049) rows.
     L.cap_m = L.ncap / 9 + 1;
@@ -545,11 +547,19 @@ __global__ void __launch_bounds__(1024) sort_long_rows_kernel(const Problem pb, 
 
 // ---------------------------------------------------------------- 5. epilogue
 
+// The pull's leftover-row count is spent once the pull has finished; the
+// epilogue, which follows it, clears it for the next pull of this workspace.
+__device__ __forceinline__ void reset_left_count(const BinArgs &w)
+{
+    if (blockIdx.x == 0 && threadIdx.x == 0 && w.left_count) *w.left_count = 0;
+}
+
 __global__ void __launch_bounds__(256) epilogue_kernel(const Problem pb, const BinArgs w, float *grad_loc,
                                                        float *grad_weight, int64_t pk_begin, int64_t pk_end)
 {
     pdl_wait();
     pdl_trigger();
+    reset_left_count(w);
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
     __syncthreads();
@@ -602,6 +612,7 @@ __global__ void __launch_bounds__(256) epilogue_vec_kernel(const Problem pb, con
 {
     pdl_wait();
     pdl_trigger();
+    reset_left_count(w);
     static_assert(G == 4 || G == 8, "16-byte vectors of G floats");
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
@@ -668,6 +679,7 @@ __global__ void __launch_bounds__(256) epilogue_fused_kernel(const Problem pb, c
 {
     pdl_wait();
     pdl_trigger();
+    reset_left_count(w);
     __shared__ MapInfo maps_s[DA_MAX_MAPS];
     stage_maps(pb, maps_s);
     __syncthreads();

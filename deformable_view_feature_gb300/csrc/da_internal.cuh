@@ -120,19 +120,22 @@ struct BwdArgs {
 //            at row `key` of the record: the four corners of a sample are
 //            adjacent, in sample order. Entries of corners outside their
 //            map are never written (no record) and never read.
+//   left     [rows_total] int32: rows the pull hands from a warp's pixel run
+//            to one warp each (runs of more than kRunMaxRecs records); their
+//            count is row_off's tail word 1, reset by the epilogue
 //   lists    [cap_m + cap_s + cap_g] int32: rows the deterministic sort
 //            hands to a warp (9..128 records), a CTA with shared memory
 //            (129..2048) or a CTA working in global memory (more)
 // A sample id here is ((b*A + a)*P + p)*K + k)*S + s: a sample of all groups.
 constexpr int kScanTile = 4096;
-constexpr int kRowOffTail = 8;  // [0] scan total, [4..6] sort list counters
+constexpr int kRowOffTail = 8;  // [0] scan total, [1] pull's leftover rows, [4..6] sort list counters
 
 struct BinLayout {
     int64_t rows_total;  // B * rows
     int64_t nsid;        // B*A*P*K*S
     int64_t ncap;        // 4 * nsid
     int64_t ntiles;
-    size_t off_row_off, off_tile_sum, off_rec, off_dpix, off_lists, bytes;
+    size_t off_row_off, off_tile_sum, off_rec, off_dpix, off_left, off_lists, bytes;
     // Capacities of the three row lists of the deterministic sort (rows
     // with more than 8, 128 and 2048 records).
     int64_t cap_m, cap_s, cap_g;
@@ -158,6 +161,9 @@ struct BinArgs {
     int32_t *sort_lists;
     int32_t *sort_counts;
     int64_t cap_m, cap_s, cap_g;
+    // Rows the pull hands over to one warp each, and their count.
+    int32_t *left;
+    int32_t *left_count;
 };
 
 // `chunks` = D * sizeof(feature) / 16, one of 1, 2, 4, 8.

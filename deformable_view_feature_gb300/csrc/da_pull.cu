@@ -140,8 +140,9 @@ __device__ __forceinline__ void load_feat8(const void *p, float (&v)[8])
 // rows hold few records each are pulled in runs of consecutive pixels, one
 // run per warp and four vertically adjacent runs per CTA (kRowGroups,
 // pull_groups), and the other maps one row per warp (kRowsCoarse, the
-// rows enumerated through pb.maps[].pad).
-constexpr int kRowsAll = 0, kRowsCoarse = 1, kRowGroups = 2;
+// rows enumerated through pb.maps[].pad). Rows past a run's record cap are
+// pulled one warp per row from a list afterwards (kRowsListed, w.left).
+constexpr int kRowsAll = 0, kRowsCoarse = 1, kRowGroups = 2, kRowsListed = 3;
 
 struct PullArgs {
     Problem pb;  // with row groups, pb.maps[i].pad: map i's first unit (row or block) of its kind
@@ -249,7 +250,14 @@ __device__ __forceinline__ void pull_rows(const PullArgs &args, int64_t warp_id,
     // another in one warp instead measured slower (L1 hit rate 21 % against
     // 38 %): the reuse comes from warps running side by side.
     int64_t R = args.row_end - 1 - (warp_id * RPW + q);
-    const bool active = R >= args.row_begin;
+    bool active = R >= args.row_begin;
+    if (args.mode == kRowsListed) {
+        // Entry warp_id of the leftover-row list (one row per warp: RPW = 1).
+        const int64_t cnt = min(static_cast<int64_t>(*reinterpret_cast<volatile int32_t *>(w.left_count)),
+                                w.rows_total);
+        active = warp_id < cnt;
+        R = active ? w.left[warp_id] : 0;
+    }
     if (args.mode == kRowsCoarse && active) {
         // Unit R is row ul of the ungrouped maps of batch item bu.
         const int64_t bu = R / args.units_per_b;
@@ -388,6 +396,7 @@ __global__ void __launch_bounds__(kPullThreads, 8) pull_kernel(const PullArgs ar
 // grad_out rows meet in L1.
 
 constexpr int kGroupMaxRows = 16;    // pixels per warp: the warp's lanes hold their row offsets
+constexpr int kRunMaxRecs = 256;     // records a run walks before it hands rows on
 
 __host__ __device__ inline size_t group_smem_per_warp(int G) { return pull_smem_per_warp(32, G); }
 
@@ -450,7 +459,22 @@ __device__ __forceinline__ void pull_groups(const PullArgs &args, int64_t block,
     const int64_t R0 = static_cast<int64_t>(b) * pb.rows + m.start + first;
     int rb = 0;  // lane k <= nr: where row R0 + k begins
     if (lane <= nr) rb = R0 + lane > 0 ? w.row_off[R0 + lane - 1] : 0;
-    const int J0 = __shfl_sync(0xffffffffu, rb, 0), J1 = __shfl_sync(0xffffffffu, rb, nr);
+    const int J0 = __shfl_sync(0xffffffffu, rb, 0);
+    // The run keeps its first rows up to kRunMaxRecs records (row offsets
+    // grow with k, so the rows that fit are a prefix); the rest go to the
+    // leftover list, to be pulled one warp per row. Uniform locations never
+    // get there; clustered ones (projected key points) do.
+    const int kc = 31 - __clz(__ballot_sync(0xffffffffu, lane <= nr && rb - J0 <= kRunMaxRecs));
+    if (kc < nr) {
+        int base = 0;
+        if (lane == 0) base = atomicAdd(w.left_count, nr - kc);
+        base = __shfl_sync(0xffffffffu, base, 0);
+        if (lane >= kc && lane < nr && DA_CHECK(pb.dbg_err, base + lane - kc, w.rows_total, kBoundsRowCount))
+            w.left[base + lane - kc] = static_cast<int32_t>(R0 + lane);
+        if (kc == 0) return;
+    }
+    const int nrw = kc;  // rows walked here
+    const int J1 = __shfl_sync(0xffffffffu, rb, nrw);
     const float *go_b = args.grad_out + static_cast<int64_t>(b) * pb.A * pb.C + lane * 8;
     const int abase = b * pb.A;
 
@@ -460,7 +484,7 @@ __device__ __forceinline__ void pull_groups(const PullArgs &args, int64_t block,
     };
     // Lanes 0..(row bytes / 128 - 1) each prefetch one 128-byte line of row k.
     auto l2_prefetch = [&](int k) {
-        if (k < nr && lane * 128 < 256 * ESZ) {
+        if (k < nrw && lane * 128 < 256 * ESZ) {
             const char *p = static_cast<const char *>(pb.feat) + (R0 + k) * pb.C * ESZ + lane * 128;
             asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
         }
@@ -475,7 +499,7 @@ __device__ __forceinline__ void pull_groups(const PullArgs &args, int64_t block,
 #pragma unroll
         for (int c = 0; c < 4; ++c) v2[c] = make_float2(v[2 * c], v[2 * c + 1]);
     }
-    if (nr > 1) load_feat8<T, V8>(feat_ptr(1), vn);
+    if (nrw > 1) load_feat8<T, V8>(feat_ptr(1), vn);
     else {
 #pragma unroll
         for (int c = 0; c < 8; ++c) vn[c] = 0.f;
@@ -484,7 +508,7 @@ __device__ __forceinline__ void pull_groups(const PullArgs &args, int64_t block,
     auto next_feats = [&]() {
 #pragma unroll
         for (int c = 0; c < 4; ++c) v2[c] = make_float2(vn[2 * c], vn[2 * c + 1]);
-        if (cur + 1 < nr) load_feat8<T, V8>(feat_ptr(cur + 1), vn);
+        if (cur + 1 < nrw) load_feat8<T, V8>(feat_ptr(cur + 1), vn);
         l2_prefetch(cur + 4);
     };
     auto store_row = [&](int k) {
@@ -568,7 +592,7 @@ __device__ __forceinline__ void pull_groups(const PullArgs &args, int64_t block,
     }
     // The row being summed, then the rows with no records left.
     store_row(cur);
-    for (int k = cur + 1; k < nr; ++k) store_row(k);
+    for (int k = cur + 1; k < nrw; ++k) store_row(k);
 }
 
 // Both kinds of unit in one launch: CTAs below n_coarse take coarse rows
@@ -589,6 +613,23 @@ __global__ void __launch_bounds__(kPullThreads, 6)
                                          pull_smem);
     else
         pull_groups<T, LPG, V8>(grouped, static_cast<int64_t>(blockIdx.x) - n_coarse, pull_smem);
+}
+
+// The leftover rows of the runs: one warp per listed row, a grid of at most
+// eight CTAs per SM looping over the list (its length is known only on the
+// device). Launched after the hybrid kernel; with no leftovers it only reads
+// the count.
+template <typename T, int LPG, bool V8>
+__global__ void __launch_bounds__(kPullThreads, 8) pull_listed_kernel(const PullArgs args)
+{
+    pdl_wait();
+    pdl_trigger();
+    extern __shared__ __align__(16) unsigned char pull_smem[];
+    const int64_t cnt = min(static_cast<int64_t>(*reinterpret_cast<volatile int32_t *>(args.w.left_count)),
+                            args.w.rows_total);
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * (kPullThreads / 32);
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * kPullThreads + threadIdx.x) >> 5; i < cnt; i += nw)
+        pull_rows<T, 32, LPG, false, V8>(args, i, pull_smem);
 }
 
 // Row groups serve the standard layout with C = 256 when the maps cover a
@@ -667,8 +708,21 @@ cudaError_t launch_pull_hybrid(const PullArgs &coarse, const PullArgs &grouped, 
     const size_t smem = group_smem_per_warp(coarse.pb.G) * (kPullThreads / 32);
     const dim3 gd(static_cast<unsigned>(grid));
     const dim3 blk(kPullThreads);
-    return v8 ? launch_pdl(pull_hybrid_kernel<T, LPG, true>, gd, blk, smem, st, c, g, n_coarse)
-              : launch_pdl(pull_hybrid_kernel<T, LPG, false>, gd, blk, smem, st, c, g, n_coarse);
+    cudaError_t e = v8 ? launch_pdl(pull_hybrid_kernel<T, LPG, true>, gd, blk, smem, st, c, g, n_coarse)
+                       : launch_pdl(pull_hybrid_kernel<T, LPG, false>, gd, blk, smem, st, c, g, n_coarse);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const int64_t rows_grouped = coarse.pb.B * coarse.pb.rows - (coarse.row_end - coarse.row_begin);
+    const int64_t lgrid =
+        std::max<int64_t>(1, std::min<int64_t>((rows_grouped + 3) / 4, static_cast<int64_t>(sms) * 8));
+    PullArgs l = c;
+    l.mode = kRowsListed;
+    const size_t lsmem = pull_smem_per_warp(32, coarse.pb.G) * (kPullThreads / 32);
+    const dim3 lg(static_cast<unsigned>(lgrid));
+    return v8 ? launch_pdl(pull_listed_kernel<T, LPG, true>, lg, blk, lsmem, st, l)
+              : launch_pdl(pull_listed_kernel<T, LPG, false>, lg, blk, lsmem, st, l);
 }
 
 template <typename T>

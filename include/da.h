@@ -143,7 +143,7 @@ da_status da_forward(const da_dims *dims,
  * Size in bytes of the device workspace that the binned path of da_backward
  * needs for `dims` (stored in *bytes). It depends on the sizes only:
  * about 4*B*A*P*K*S*(8.5 + 4*G) bytes plus 4 bytes per feature row. This
- * is about 275 MB for B=6, A=900, P=13, K=6, S=4, G=8. The same workspace
+ * is about 277 MB for B=6, A=900, P=13, K=6, S=4, G=8. The same workspace
  * serves both modes of da_backward_ex.
  * Returns DA_ERR_UNSUPPORTED when 4*B*A*P*K*S or B*num_feat_rows does not
  * fit in int32. It also returns DA_ERR_UNSUPPORTED unless C is a power of
@@ -410,7 +410,7 @@ da_status da_backward_bin(const da_dims *dims,
  *   - Problems whose workspace (da_backward_workspace_size) exceeds
  *     DA_NOALLOC_SCRATCH_BYTES are rejected with DA_ERR_WORKSPACE. The limit
  *     fits e.g. the 6-camera Sparse4D shape at B = 1 (about 46 MB); the
- *     B = 6 training shape needs about 275 MB and must use da_backward.
+ *     B = 6 training shape needs about 277 MB and must use da_backward.
  *   - Every call uses the same array. Each call clears what must start at
  *     zero, so a call does not depend on what the last one left there.
  *   - Calls that overlap on the GPU (on different streams, or from

@@ -156,8 +156,9 @@ def test_workspace_size_and_errors(lib):
     nsid = 6 * 900 * 13 * 6 * 4
     # records (key + weight) and dpix for 8 groups: 4*nsid*(4+4) + 4*nsid*8*4,
     # plus the deterministic sort's row lists (rows of > 8, > 128, > 2048 records)
+    # and the pull's leftover-row list (one int32 per feature row)
     ncap = 4 * nsid
-    lists = 4 * (ncap // 9 + ncap // 129 + ncap // 2049 + 3)
+    lists = 4 * (ncap // 9 + ncap // 129 + ncap // 2049 + 3) + 4 * 6 * 14960
     assert n.value >= nsid * (32 + 128) + lists
     assert n.value < nsid * (32 + 128) + lists + 4 * 1024 * 1024
     assert lib.da_backward_workspace_size(None, ctypes.byref(n)) == DA_ERR_NULL

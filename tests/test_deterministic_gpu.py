@@ -68,17 +68,21 @@ def _same_bits(a, b):
         assert np.array_equal(a[name].view(np.uint32), b[name].view(np.uint32)), name
 
 
-def _crowded(seed, n_spot, H=16, W=16, A=600, P=8, C=64, G=2):
+def _crowded(seed, n_spot, H=16, W=16, A=600, P=8, C=64, G=2, softmax_w=False):
     """One 16x16 map and A*P = 4800 locations. The first n_spot*P sit on one
     spot, the rest are spread uniformly. A pixel then gets about
     4*(4800 - n_spot*P)/256 records from the spread locations, and the four
-    pixels around the spot n_spot*P more."""
+    pixels around the spot n_spot*P more. softmax_w: the weights of each
+    (anchor, group) are a softmax over its P points, as in the Sparse4D
+    workloads, instead of N(0, 1) draws."""
     g = torch.Generator().manual_seed(seed)
     ss, ls = da_inputs.map_tables(1, [(H, W)])
     feat = torch.randn(1, H * W, C, generator=g)
     loc = torch.rand(1, A, P, 1, 2, generator=g)
     loc.view(1, A * P, 2)[:, :n_spot * P] = torch.tensor([0.37, 0.61])
     w = torch.randn(1, A, P, 1, 1, G, generator=g)
+    if softmax_w:
+        w = w.softmax(dim=2)
     go = torch.randn(1, A, C, generator=g)
     wl = da_inputs.WORKLOADS["tiny"].replace(name=f"crowded{n_spot}", batch=1, num_embeds=C, num_groups=G,
                                              num_anchors=A, num_pts=P, shapes=((H, W),))
@@ -95,6 +99,44 @@ def test_crowded_rows_every_sort_tier(da, n_spot):
     _check_oracle(inp, a, crowded=True)
     b = _backward(da, inp, garbage_seed=2, stream=torch.cuda.Stream())
     _same_bits(a, b)
+
+
+@pytest.mark.parametrize("n_spot", [0, 100, 600])
+@pytest.mark.parametrize("deterministic", [False, True])
+def test_crowded_pixel_runs_hand_rows_on(da, n_spot, deterministic):
+    # C = 256 on a 64x64 map: about 4.7 records per row from the spread
+    # locations, so the pull walks the map in runs of 16 pixels per warp.
+    # The runs around the spot hold up to 4800 records, beyond a run's cap:
+    # their rows past the cap go to the leftover list and its own launch.
+    # Softmax weights: 8 groups of 32 channels sum many signed products per
+    # grad_loc element, and N(0, 1) weights on top of that put about 0.1 % of
+    # them past the plain bound through cancellation alone.
+    inp = _crowded(90 + n_spot, n_spot, H=64, W=64, C=256, G=8, softmax_w=True)
+    a = _backward(da, inp, deterministic=deterministic, garbage_seed=7)
+    _check_oracle(inp, a, crowded=True)
+    b = _backward(da, inp, deterministic=deterministic, garbage_seed=8, stream=torch.cuda.Stream())
+    if deterministic:
+        _same_bits(a, b)
+    else:
+        _check_oracle(inp, b, crowded=True)
+
+
+def test_pull_twice_on_one_binning(da):
+    # The leftover-row count lives in the workspace: the epilogue clears it,
+    # so a second pull of the same binned workspace hands on the same rows
+    # and gives the same bits.
+    inp = _crowded(95, 600, H=64, W=64, C=256, G=8, softmax_w=True)
+    dev = torch.device("cuda")
+    feat, loc, w, go = (t.to(dev) for t in (inp.feat, inp.loc, inp.weights, inp.grad_out))
+    ws = da.da_backward_bin(feat, inp.spatial_shape, inp.level_start_index, loc, w, deterministic=True)
+    outs = []
+    for _ in range(2):
+        res = da.da_backward(feat, inp.spatial_shape, inp.level_start_index, loc, w, go, path="binned",
+                             workspace=ws, deterministic=True, binned_ready=True)
+        torch.cuda.synchronize()
+        outs.append(dict(zip(NAMES, (to_np(t) for t in res))))
+    _same_bits(outs[0], outs[1])
+    _check_oracle(inp, outs[0], crowded=True)
 
 
 def test_short_rows_and_many_maps(da):
