@@ -60,10 +60,10 @@ METRIC = "fwd+bwd bilinear samples/sec at 6-cam Sparse4D shape; GB/s vs HBM peak
 # describe the kernels whose sources hash to "digest", and are reported as null
 # once the sources change.
 NCU_TRAFFIC = {
-    "digest": "01efe9c8173c7960",
+    "digest": "9f8da60678c11abf",
     "workload": "sp4d_train",
-    "da_forward": 618_248_192,
-    "da_backward[binned]": 1_660_251_136,
+    "da_forward": 617_562_880,
+    "da_backward[binned]": 1_723_979_520,
 }
 
 
@@ -94,7 +94,25 @@ def ncu_traffic(workload: str, call: str):
 # Kernels da_backward launches: binned = row-count zero-fill, count, 3 scan
 # steps, fill, pull, epilogue; scatter = grad_feat zero-fill, gather-scatter.
 # binned-det adds the four kernels of the per-row sort (DA_BACKWARD_DETERMINISTIC).
+# Where the pull takes fine maps in pixel runs it is two launches (the pull,
+# then its leftover rows): see pull_launches.
 BWD_LAUNCHES = {"binned": 8, "binned-det": 12, "scatter": 2}
+
+
+def pull_launches(wl) -> int:
+    """Kernels of the binned path's pull: 2 when the library pulls fine maps
+    in pixel runs (standard layout, 256 channels, packed maps, and a map whose
+    rows average fewer than 24 records: 4*A*P/(H*W) < 24), else 1. The rule
+    is the one the library applies to choose its pull."""
+    if wl.num_embeds != 256:
+        return 1
+    ap = wl.num_anchors * wl.num_pts
+    return 2 if any(4.0 * ap / (h * w) < 24.0 for h, w in wl.shapes) else 1
+
+
+def bwd_launches(path: str, wl) -> int:
+    n = BWD_LAUNCHES[path]
+    return n + pull_launches(wl) - 1 if path != "scatter" else n
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -531,7 +549,7 @@ def run_ours(a, wl):
                      "algorithmic_bytes": step_bytes, "traffic": traffic,
                      "parts": parts},
         "e2e": e2e,
-        "gpu_launches": a.steps * (1 + (BWD_LAUNCHES[a.bwd_path] if wl.backward else 0)),
+        "gpu_launches": a.steps * (1 + (bwd_launches(a.bwd_path, wl) if wl.backward else 0)),
         "bwd_path": a.bwd_path,
         "binning": "on a side stream during the forward (da_backward_bin)" if overlap else "inside da_backward",
         "workspace_bytes": int(ws.numel()) if ws is not None else 0,
@@ -700,7 +718,7 @@ def run_projected(a, wl):
                      "achieved": bwd_b / (bwd_ms / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": bwd_b / (bwd_ms / 1e3) / 1e9 / peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
                      "algorithmic_bytes": bwd_b, "traffic": None},
-        "gpu_launches": a.steps * (1 + BWD_LAUNCHES["binned"] + 2),
+        "gpu_launches": a.steps * (1 + bwd_launches("binned", wl) + 2),
         "clocks": clocks,
     }), flush=True)
 
