@@ -497,6 +497,177 @@ __global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args,
     for (int q = 0; q < VEC / 4; ++q) o[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
 }
 
+// ------------------------------------------------------------ row forward
+//
+// The standard layout with C = 256 (one 1 KB fp32 or 512-byte 16-bit feature
+// row per pixel) and at most 8 groups: a warp owns one anchor (and camera
+// part), all its groups, and lane l channels 8l..8l+7 of every row. A corner
+// of a sample is then one warp-wide 256-bit (fp32) or 128-bit (16-bit) load
+// of the whole feature row, the sample's footprint is computed once for all
+// G groups, and each lane applies its own group's weight: about 30 warp
+// instructions per sample and corner set instead of 8 group-warps' 20 each,
+// for the same bytes from L2.
+//
+// Two samples per step (8 row loads of 32 bytes per lane in flight), 104
+// registers, 2 CTAs (16 warps) per SM. The 6-camera training-shape forward
+// alone: 344 us against 385 us for the group-per-warp kernel; one sample per
+// step (59 registers, 32 warps per SM): 380 us; two at 3 CTAs per SM (80
+// registers): 349 us. A warp per anchor gives few warps on small batches:
+// B = 1 at 900 anchors took 87-101 us against 86 us, so the kernel serves
+// problems with at least kRowTasksMin (anchor, camera part) tasks.
+constexpr int kFwdRowU = 2;
+constexpr int kRowTasksMin = 8192;
+
+// 32 bytes (8 floats) at a 32-byte aligned address, or zeros when `pred` is
+// false (then nothing is read).
+__device__ __forceinline__ void ldg32_if(bool pred, const void *p, float4 &x, float4 &y)
+{
+    asm("{\n\t.reg .pred q;\n\t"
+        "setp.ne.b32 q, %9, 0;\n\t"
+        "mov.b32 %0, 0;\n\tmov.b32 %1, 0;\n\tmov.b32 %2, 0;\n\tmov.b32 %3, 0;\n\t"
+        "mov.b32 %4, 0;\n\tmov.b32 %5, 0;\n\tmov.b32 %6, 0;\n\tmov.b32 %7, 0;\n\t"
+        "@q ld.global.nc.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n\t}"
+        : "=f"(x.x), "=f"(x.y), "=f"(x.z), "=f"(x.w), "=f"(y.x), "=f"(y.y), "=f"(y.z), "=f"(y.w)
+        : "l"(p), "r"(static_cast<int>(pred)));
+}
+
+// The lane's 8 channels of one feature row (fp32: 32 bytes; 16-bit: 16
+// bytes), widened; zeros when `pred` is false.
+template <typename T>
+__device__ __forceinline__ void row_chunk_if(bool pred, const char *p, float (&v)[8])
+{
+    if constexpr (sizeof(T) == 4) {
+        float4 x, y;
+        ldg32_if(pred, p, x, y);
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+        v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+    } else {
+        Chunk<T>::unpack(ldg16_if(pred, p), v);
+    }
+}
+
+// One CTA = 8 warps = 8 anchors of one (batch item, camera part); warp w
+// takes anchor 8*ci + w over the part's cameras. Per round of 32 samples each
+// lane computes one sample's footprint into the warp's table (rows and corner
+// weights sample-major, the G weights group-major); the lanes then walk the
+// round U samples at a time: four predicated row loads per sample, and
+// acc += (w_g * cw_i) * v_i with the lane's group g. SPLIT: as fwd_kernel,
+// two camera parts add their sums into the zeroed output.
+template <typename T, bool SPLIT, int U>
+__global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs args)
+{
+    constexpr int ESZ = sizeof(T) == 4 ? 4 : 2;
+    constexpr int WP = 36;  // weight row pitch: the 8 groups' rows 4 banks apart
+    const Problem &pb = args.pb;
+    __shared__ MapInfo maps_s[DA_MAX_MAPS];
+    __shared__ __align__(16) int4 rows_s[kWarps][32];
+    __shared__ __align__(16) float4 cw_s[kWarps][32];
+    __shared__ __align__(16) float w_s[kWarps][8][WP];
+    stage_maps(pb, maps_s);
+    __syncthreads();
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int gl = (lane * pb.G) >> 5;  // the lane's group: channels 8*lane.. of D = 256/G
+    int ba, part = 0;
+    bool valid;
+    if constexpr (SPLIT) {
+        const int c = static_cast<int>(blockIdx.x);
+        const int bq = static_cast<int>(args.div_cpp.div(c));  // b * parts + part
+        const int ci = c - bq * args.ctas_per_part;
+        const int bb = bq / args.parts;
+        part = bq - bb * args.parts;
+        const int a = ci * kWarps + warp;
+        valid = a < pb.A;
+        ba = bb * pb.A + a;
+    } else {
+        ba = static_cast<int>(blockIdx.x) * kWarps + warp;
+        valid = ba < pb.num_ba;
+    }
+    if (!valid) return;  // the whole warp; no CTA-wide barrier follows
+    const int b = static_cast<int>(pb.div_A.div(ba));
+    const int nsamp = SPLIT ? pb.P * args.kpart * pb.S : pb.pks;
+    const uint32_t row_bytes = 256u * ESZ;
+    const char *base = static_cast<const char *>(pb.feat) + static_cast<int64_t>(b) * pb.rows * row_bytes + lane * 8 * ESZ;
+    float2 acc[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
+
+    for (int j0 = 0; j0 < nsamp; j0 += 32) {
+        const int n = min(32, nsamp - j0);
+        {
+            int4 rr = make_int4(-1, -1, -1, -1);
+            float4 cw = make_float4(0.f, 0.f, 0.f, 0.f);
+            float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (lane < n) {
+                const int j = j0 + lane;
+                int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k (p*kpart + k' with parts)
+                const int s = j - jk * pb.S;
+                int k;
+                if constexpr (SPLIT) {
+                    const int p = static_cast<int>(args.div_kpart.div(jk));
+                    k = part * args.kpart + (jk - p * args.kpart);
+                    jk = p * pb.K + k;
+                } else {
+                    k = jk - static_cast<int>(pb.div_K.div(jk)) * pb.K;
+                }
+                const int64_t locid = static_cast<int64_t>(ba) * pb.pk + jk;
+                const float2 xy = *reinterpret_cast<const float2 *>(pb.loc + locid * 2);
+                Footprint f;
+                footprint(xy.x, xy.y, maps_s[k * pb.S + s], f);
+                rr = make_int4(feat_row_ok(pb, f.row[0]) ? f.row[0] : -1, feat_row_ok(pb, f.row[1]) ? f.row[1] : -1,
+                               feat_row_ok(pb, f.row[2]) ? f.row[2] : -1, feat_row_ok(pb, f.row[3]) ? f.row[3] : -1);
+                cw = make_float4(f.cw[0], f.cw[1], f.cw[2], f.cw[3]);
+                const float *wp = pb.weights + (locid * pb.S + s) * pb.G;
+                for (int g = 0; g < pb.G; ++g) wv[g] = wp[g];
+            }
+            rows_s[warp][lane] = rr;
+            cw_s[warp][lane] = cw;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) w_s[warp][g][lane] = wv[g];
+        }
+        __syncwarp();
+        for (int i0 = 0; i0 < n; i0 += U) {
+            float v[U][4][8];
+            float tw[U][4];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u;
+                const bool live = U == 1 || i < n;
+                const int4 rr = live ? rows_s[warp][i] : make_int4(-1, -1, -1, -1);
+                const float4 cw = live ? cw_s[warp][i] : make_float4(0.f, 0.f, 0.f, 0.f);
+                const float wg = live ? w_s[warp][gl][i] : 0.f;
+                const int r4[4] = {rr.x, rr.y, rr.z, rr.w};
+                tw[u][0] = wg * cw.x;
+                tw[u][1] = wg * cw.y;
+                tw[u][2] = wg * cw.z;
+                tw[u][3] = wg * cw.w;
+#pragma unroll
+                for (int c = 0; c < 4; ++c) row_chunk_if<T>(r4[c] >= 0, row_addr(base, r4[c], row_bytes), v[u][c]);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+#pragma unroll
+                for (int c = 0; c < 4; ++c) {
+                    const float2 t2 = make_float2(tw[u][c], tw[u][c]);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        acc[q] = __ffma2_rn(t2, make_float2(v[u][c][2 * q], v[u][c][2 * q + 1]), acc[q]);
+                }
+            }
+        }
+        __syncwarp();
+    }
+    float *o = args.out + static_cast<int64_t>(ba) * 256 + lane * 8;
+    if constexpr (SPLIT) {
+        red_add_v4_if(true, o, acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        red_add_v4_if(true, o + 4, acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    } else {
+        reinterpret_cast<float4 *>(o)[0] = make_float4(acc[0].x, acc[0].y, acc[1].x, acc[1].y);
+        reinterpret_cast<float4 *>(o)[1] = make_float4(acc[2].x, acc[2].y, acc[3].x, acc[3].y);
+    }
+}
+
 // Camera parts of the standard forward: 2 when a batch item's feature maps
 // are large next to L2 and the cameras split evenly, else 1. A CTA then
 // gathers from half the cameras, so the CTAs resident at once (about one
@@ -546,6 +717,28 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
             break;
         }
         default: {
+            const int row_parts = forward_parts(a.pb, ESZ);
+            if (a.pb.C == 256 && a.pb.G <= 8 && (sizeof(T) != 4 || aligned(a.pb.feat, 32)) &&
+                static_cast<int64_t>(a.pb.num_ba) * row_parts >= kRowTasksMin) {
+                FwdArgs f = a;
+                f.parts = row_parts;
+                const int ctas = (a.pb.A + kWarps - 1) / kWarps;  // per (batch item, part)
+                int64_t g = (static_cast<int64_t>(a.pb.num_ba) + kWarps - 1) / kWarps;
+                if (f.parts > 1) {
+                    f.ctas_per_part = ctas;
+                    f.kpart = a.pb.K / f.parts;
+                    f.div_cpp = FastDiv::make(static_cast<uint32_t>(ctas));
+                    f.div_kpart = FastDiv::make(static_cast<uint32_t>(f.kpart));
+                    g = static_cast<int64_t>(a.pb.B) * f.parts * ctas;
+                    const cudaError_t e = cudaMemsetAsync(a.out, 0, static_cast<size_t>(a.pb.num_ba) * a.pb.C * 4, st);
+                    if (e != cudaSuccess) return e;
+                }
+                if (g == 0) return cudaSuccess;
+                const dim3 gg(static_cast<unsigned>(g));
+                if (f.parts > 1) fwd_row_kernel<T, true, kFwdRowU><<<gg, kThreads, 0, st>>>(f);
+                else fwd_row_kernel<T, false, kFwdRowU><<<gg, kThreads, 0, st>>>(f);
+                break;
+            }
             FwdArgs f = a;
             // Two groups per task when a group's row slice is at most half a
             // line; a CTA then takes twice the anchors to keep its 8 warps busy.

@@ -117,14 +117,19 @@ def test_ragged_shapes(da, C, G, dtype, path):
     _check(inp, _run(da, inp, path))
 
 
+@pytest.mark.parametrize("channels,groups", [(128, 4), (256, 8)])
 @pytest.mark.parametrize("cams", [2, 6])
-def test_shared_points_match_standard_forward(da, cams):
+def test_shared_points_match_standard_forward(da, cams, channels, groups):
     """The DCNv4 form with every group on the same points is the standard
-    operator. With two cameras (one camera part in the standard forward) the
-    bits agree; at six cameras the standard forward sums two camera halves
-    (a different association), so the two agree within the fp32 forward
-    tolerance."""
-    wl = da_inputs.small_variant("sp4d_inf", num_anchors=40).replace(num_cams=cams)
+    operator. With two cameras (one camera part in the standard forward) and
+    128 channels in 4 groups of 32 both run the same per-group decomposition
+    and the bits agree.
+    At six cameras the standard forward sums two camera halves, and with 256
+    channels it sums each lane's channels sample by sample in one warp per
+    anchor: other associations of the same sum, so the two agree within the
+    fp32 forward tolerance."""
+    wl = da_inputs.small_variant("sp4d_inf", num_anchors=40).replace(num_cams=cams, num_embeds=channels,
+                                                                     num_groups=groups)
     inp = da_inputs.make_inputs(wl)
     B, A, P, K, _ = inp.loc.shape
     S, G = inp.weights.shape[4], inp.weights.shape[5]
@@ -136,7 +141,7 @@ def test_shared_points_match_standard_forward(da, cams):
     feat = inp.feat.to(dev)
     a = da.da_forward_fused(feat, inp.spatial_shape, inp.level_start_index, lw.to(dev))
     b = da.da_forward(feat, inp.spatial_shape, inp.level_start_index, inp.loc.to(dev), inp.weights.to(dev))
-    if cams == 2:
+    if cams == 2 and channels != 256:
         assert torch.equal(a, b)
     else:
         n, msg = violations(to_np(a), to_np(b), 1e-5, 1e-6, "out")
