@@ -132,6 +132,24 @@ def binned_supported(C, G):
     return 8 <= C <= 256 and C & (C - 1) == 0 and D % 8 == 0
 
 
+@pytest.mark.parametrize("split", [False, True])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+def test_row_forward_every_feature_type(da, dtype, split):
+    """The forward with a warp per anchor and all its groups serves 256
+    channels in at most 8 groups from 8,192 (anchor, camera part) tasks up.
+    Two cameras: with maps of 48 MB or more per batch item the cameras split
+    in two parts (4,096 anchors make 8,192 tasks), else one part (8,192
+    anchors)."""
+    if split:
+        side = 160 if dtype == "f32" else 224  # 2 * side^2 rows of 256 channels >= 48 MB
+        shapes, A = [[(side, side)], [(side, side - 7)]], 4096
+    else:
+        shapes, A = [[(16, 16), (8, 5)], [(9, 12), (4, 4)]], 8192
+    inp = _custom(300 + (1 if split else 0) + {"f32": 0, "bf16": 2, "f16": 4}[dtype], shapes, 1, 256, 8, A, 2, dtype)
+    got = _run_gpu(da, inp, backward=False)
+    _compare(inp, got, oracle.run_inputs(inp, backward_pass=False))
+
+
 @pytest.mark.parametrize("path", PATHS)
 @pytest.mark.parametrize("case", CASES, ids=[f"case{c[0]}" for c in CASES])
 def test_parity_shapes(da, case, path):
