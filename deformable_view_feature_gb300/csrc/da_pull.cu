@@ -406,6 +406,8 @@ __host__ __device__ inline size_t group_smem_per_warp(int G) { return pull_smem_
 // end, as rows are in pull_kernel.
 //   - lanes 0..nr load the begin offsets of the warp's rows and of the next
 //     row, so the record run is [J0, J1) and row k ends where row k+1 begins;
+//     the warp keeps its first rows up to kRunMaxRecs records and lists the
+//     rest for pull_listed_kernel;
 //   - the first row's features are loaded, and the next row's one row ahead
 //     (with an L2 prefetch four rows ahead);
 //   - the run is decoded 32 records at a time into the warp's table (as in
@@ -413,8 +415,9 @@ __host__ __device__ inline size_t group_smem_per_warp(int G) { return pull_smem_
 //     every row that ends at or before it is finished: its grad_feat is
 //     stored and the next row's features take its place;
 //   - rows after the last record are stored as zeros.
-// 80 registers, 6 CTAs (24 warps) per SM. Pull + epilogue at the training
-// shape: 589 us; 605 us with 5 CTAs per SM (94 registers); with one warp per
+// In pull_hybrid_kernel: 80 registers, 6 CTAs (24 warps) per SM. Pull +
+// epilogue at the training shape: 589 us; 605 us with 5 CTAs per SM (94
+// registers); with one warp per
 // 16 pixels of a map row and the CTA's warps on consecutive runs of one map
 // row, 615 us (feature rows in registers) or 608 us (through a shared-memory
 // ring of cp.async copies).
