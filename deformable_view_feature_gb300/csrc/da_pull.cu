@@ -298,13 +298,27 @@ __device__ __forceinline__ void pull_rows(const PullArgs &args, int64_t warp_id,
         for (int o = 16; o >= LPR; o >>= 1) nmax = max(nmax, __shfl_xor_sync(0xffffffffu, nmax, o));
     }
 
+    // With one record per lane per chunk (RPL = 1), the next chunk's record
+    // is loaded one chunk ahead, so a chunk's decode waits only for weights.
+    int2 rnext = make_int2(0, 0);
+    if constexpr (RPL == 1) {
+        if (sub < n && DA_CHECK(pb.dbg_err, jb + sub, w.ncap, kBoundsRecord)) rnext = ldg_record_stream(&w.rec[jb + sub]);
+    }
     for (int k0 = 0; k0 < nmax; k0 += CH) {
         // 1. decode: lane sub takes records k0 + sub + LPR*j of its row.
 #pragma unroll
         for (int j = 0; j < RPL; ++j) {
             const int c = sub + LPR * j;
             bool valid = k0 + c < n && DA_CHECK(pb.dbg_err, jb + k0 + c, w.ncap, kBoundsRecord);
-            const int2 r = valid ? ldg_record_stream(&w.rec[jb + k0 + c]) : make_int2(0, 0);
+            int2 r;
+            if constexpr (RPL == 1) {
+                r = valid ? rnext : make_int2(0, 0);
+                const int kn = k0 + CH + c;
+                rnext = make_int2(0, 0);
+                if (kn < n && DA_CHECK(pb.dbg_err, jb + kn, w.ncap, kBoundsRecord)) rnext = ldg_record_stream(&w.rec[jb + kn]);
+            } else {
+                r = valid ? ldg_record_stream(&w.rec[jb + k0 + c]) : make_int2(0, 0);
+            }
             const int sid = r.x >> 2;
             int a = valid ? static_cast<int>(pb.div_PKS.div(sid)) - abase : 0;
             // A bounds-checking build drops a record whose anchor or sample
@@ -530,12 +544,20 @@ __device__ __forceinline__ void pull_groups(const PullArgs &args, int64_t block,
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc2[c] = make_float2(0.f, 0.f);
 
+    // Each lane's record of the next round is loaded one round ahead, so a
+    // round's decode waits only for the weights.
+    int2 rnext = make_int2(0, 0);
+    if (J0 + lane < J1 && DA_CHECK(pb.dbg_err, J0 + lane, w.ncap, kBoundsRecord))
+        rnext = ldg_record_stream(&w.rec[J0 + lane]);
     for (int k0 = J0; k0 < J1; k0 += CH) {
         // 1. decode: lane c takes record k0 + c of the run.
         {
             const int c = lane;
             bool valid = k0 + c < J1 && DA_CHECK(pb.dbg_err, k0 + c, w.ncap, kBoundsRecord);
-            const int2 r = valid ? ldg_record_stream(&w.rec[k0 + c]) : make_int2(0, 0);
+            const int2 r = valid ? rnext : make_int2(0, 0);
+            const int kn = k0 + CH + c;
+            rnext = make_int2(0, 0);
+            if (kn < J1 && DA_CHECK(pb.dbg_err, kn, w.ncap, kBoundsRecord)) rnext = ldg_record_stream(&w.rec[kn]);
             const int sid = r.x >> 2;
             int a = valid ? static_cast<int>(pb.div_PKS.div(sid)) - abase : 0;
             if (valid && !(DA_CHECK(pb.dbg_err, a, pb.A, kBoundsAnchor) &&
