@@ -500,22 +500,27 @@ __global__ void __launch_bounds__(kThreads) fwd_small_kernel(const FwdArgs args,
 // ------------------------------------------------------------ row forward
 //
 // The standard layout with C = 256 (one 1 KB fp32 or 512-byte 16-bit feature
-// row per pixel) and at most 8 groups: a warp owns one anchor (and camera
-// part), all its groups, and lane l channels 8l..8l+7 of every row. A corner
-// of a sample is then one warp-wide 256-bit (fp32) or 128-bit (16-bit) load
-// of the whole feature row, the sample's footprint is computed once for all
-// G groups, and each lane applies its own group's weight: about 30 warp
-// instructions per sample and corner set instead of 8 group-warps' 20 each,
-// for the same bytes from L2.
+// row per pixel) and at most 8 groups: a warp owns half the scales of one
+// anchor (and camera part), all its groups, and lane l channels 8l..8l+7 of
+// every row. A corner of a sample is then one warp-wide 256-bit (fp32) or
+// 128-bit (16-bit) load of the whole feature row, the sample's footprint is
+// computed once for all G groups, and each lane applies its own group's
+// weight: about 110 warp instructions per sample (all groups) instead of 8
+// group-warps' 20 each, for the same bytes from L2.
 //
-// Two samples per step (8 row loads of 32 bytes per lane in flight), 104
+// Two samples per step (8 row loads of 32 bytes per lane in flight), 113
 // registers, 2 CTAs (16 warps) per SM. The 6-camera training-shape forward
-// alone: 344 us against 385 us for the group-per-warp kernel; one sample per
-// step (59 registers, 32 warps per SM): 380 us; two at 3 CTAs per SM (80
-// registers): 349 us. A warp per anchor gives few warps on small batches:
-// B = 1 at 900 anchors took 87-101 us against 86 us, so the kernel serves
-// problems with at least kRowTasksMin (anchor, camera part) tasks.
+// alone: 344 us against 385 us for the group-per-warp kernel (one sample per
+// step, 59 registers and 32 warps per SM: 380 us; two at 3 CTAs per SM, 80
+// registers: 349 us). With one warp per (anchor, camera part) the resident
+// warps spanned about 2.7 (batch item, part) slices of the maps and read
+// 1.12 GB of DRAM (70.6 % L2 hits); two warps per anchor, one per half of the
+// scales, halve the anchors in flight: 0.72 GB (79.1 % L2 hits), 310 against
+// 314 us under ncu. A warp per anchor gives few warps on small batches: B = 1
+// at 900 anchors took 87-101 us against 86 us, so the kernel serves problems
+// with at least kRowTasksMin (anchor, camera part) tasks.
 constexpr int kFwdRowU = 2;
+constexpr int kRowAnchors = kWarps / 2;  // anchors per CTA: two warps (scale halves) each
 constexpr int kRowTasksMin = 8192;
 
 // 32 bytes (8 floats) at a 32-byte aligned address, or zeros when `pred` is
@@ -546,13 +551,20 @@ __device__ __forceinline__ void row_chunk_if(bool pred, const char *p, float (&v
     }
 }
 
-// One CTA = 8 warps = 8 anchors of one (batch item, camera part); warp w
-// takes anchor 8*ci + w over the part's cameras. Per round of 32 samples each
+// One CTA = 8 warps = 4 anchors of one (batch item, camera part), two warps
+// each: warp 2*q + h takes anchor 4*ci + q over the part's cameras and scale
+// half h (scales [0, ceil(S/2)) or [ceil(S/2), S)). The two halves have the
+// same number of samples, so they finish together, and a CTA's resident
+// anchors (about 1,200 at 16 warps per SM) keep about one (batch item,
+// camera part) slice of the maps live in L2. Per round of 32 samples each
 // lane computes one sample's footprint into the warp's table (rows and corner
 // weights sample-major, the G weights group-major); the lanes then walk the
-// round U samples at a time: four predicated row loads per sample, and
-// acc += (w_g * cw_i) * v_i with the lane's group g. SPLIT: as fwd_kernel,
-// two camera parts add their sums into the zeroed output.
+// round U samples at a time: four row loads per sample (zeros, and no load,
+// for a corner outside its map), and acc += (w_g * cw_i) * v_i
+// with the lane's group g. The second half's sums are added to the first's
+// in shared memory, and the first writes the anchor's row: a plain store, or
+// with SPLIT (two camera parts) a vector reduction into the zeroed output,
+// as in fwd_kernel.
 template <typename T, bool SPLIT, int U>
 __global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs args)
 {
@@ -563,11 +575,15 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs args
     __shared__ __align__(16) int4 rows_s[kWarps][32];
     __shared__ __align__(16) float4 cw_s[kWarps][32];
     __shared__ __align__(16) float w_s[kWarps][8][WP];
+    __shared__ float sum_s[kWarps][8][33];  // a warp's 8 channels per lane
     stage_maps(pb, maps_s);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int half = warp & 1, q = warp >> 1;
+    const int s0 = half ? (pb.S + 1) / 2 : 0;           // first scale of this half
+    const int sh = half ? pb.S / 2 : (pb.S + 1) / 2;    // scales in this half
     const int gl = (lane * pb.G) >> 5;  // the lane's group: channels 8*lane.. of D = 256/G
     int ba, part = 0;
     bool valid;
@@ -577,22 +593,22 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs args
         const int ci = c - bq * args.ctas_per_part;
         const int bb = bq / args.parts;
         part = bq - bb * args.parts;
-        const int a = ci * kWarps + warp;
+        const int a = ci * kRowAnchors + q;
         valid = a < pb.A;
         ba = bb * pb.A + a;
     } else {
-        ba = static_cast<int>(blockIdx.x) * kWarps + warp;
+        ba = static_cast<int>(blockIdx.x) * kRowAnchors + q;
         valid = ba < pb.num_ba;
     }
-    if (!valid) return;  // the whole warp; no CTA-wide barrier follows
-    const int b = static_cast<int>(pb.div_A.div(ba));
-    const int nsamp = SPLIT ? pb.P * args.kpart * pb.S : pb.pks;
-    const uint32_t row_bytes = 256u * ESZ;
-    const char *base = static_cast<const char *>(pb.feat) + static_cast<int64_t>(b) * pb.rows * row_bytes + lane * 8 * ESZ;
     float2 acc[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) acc[c] = make_float2(0.f, 0.f);
 
+    // Samples of this warp: (p, camera of the part, scale of the half).
+    const int nsamp = valid ? pb.P * (SPLIT ? args.kpart : pb.K) * sh : 0;
+    const int b = valid ? static_cast<int>(pb.div_A.div(ba)) : 0;
+    const uint32_t row_bytes = 256u * ESZ;
+    const char *base = static_cast<const char *>(pb.feat) + static_cast<int64_t>(b) * pb.rows * row_bytes + lane * 8 * ESZ;
     for (int j0 = 0; j0 < nsamp; j0 += 32) {
         const int n = min(32, nsamp - j0);
         {
@@ -601,8 +617,8 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs args
             float wv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (lane < n) {
                 const int j = j0 + lane;
-                int jk = static_cast<int>(pb.div_S.div(j));  // p*K + k (p*kpart + k' with parts)
-                const int s = j - jk * pb.S;
+                int jk = j / sh;  // p*K + k (p*kpart + k' with parts)
+                const int s = s0 + (j - jk * sh);
                 int k;
                 if constexpr (SPLIT) {
                     const int p = static_cast<int>(args.div_kpart.div(jk));
@@ -651,12 +667,25 @@ __global__ void __launch_bounds__(kThreads, 2) fwd_row_kernel(const FwdArgs args
                 for (int c = 0; c < 4; ++c) {
                     const float2 t2 = make_float2(tw[u][c], tw[u][c]);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        acc[q] = __ffma2_rn(t2, make_float2(v[u][c][2 * q], v[u][c][2 * q + 1]), acc[q]);
+                    for (int m = 0; m < 4; ++m)
+                        acc[m] = __ffma2_rn(t2, make_float2(v[u][c][2 * m], v[u][c][2 * m + 1]), acc[m]);
                 }
             }
         }
         __syncwarp();
+    }
+    // The two halves of an anchor meet in shared memory: first + second.
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        sum_s[warp][2 * m][lane] = acc[m].x;
+        sum_s[warp][2 * m + 1][lane] = acc[m].y;
+    }
+    __syncthreads();
+    if (half != 0 || !valid) return;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        acc[m].x += sum_s[warp + 1][2 * m][lane];
+        acc[m].y += sum_s[warp + 1][2 * m + 1][lane];
     }
     float *o = args.out + static_cast<int64_t>(ba) * 256 + lane * 8;
     if constexpr (SPLIT) {
@@ -722,8 +751,8 @@ cudaError_t launch(const FwdArgs &a, cudaStream_t st)
                 static_cast<int64_t>(a.pb.num_ba) * row_parts >= kRowTasksMin) {
                 FwdArgs f = a;
                 f.parts = row_parts;
-                const int ctas = (a.pb.A + kWarps - 1) / kWarps;  // per (batch item, part)
-                int64_t g = (static_cast<int64_t>(a.pb.num_ba) + kWarps - 1) / kWarps;
+                const int ctas = (a.pb.A + kRowAnchors - 1) / kRowAnchors;  // per (batch item, part)
+                int64_t g = (static_cast<int64_t>(a.pb.num_ba) + kRowAnchors - 1) / kRowAnchors;
                 if (f.parts > 1) {
                     f.ctas_per_part = ctas;
                     f.kpart = a.pb.K / f.parts;
