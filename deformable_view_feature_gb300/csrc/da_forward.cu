@@ -553,8 +553,10 @@ __device__ __forceinline__ void row_chunk_if(bool pred, const char *p, float (&v
 
 // One CTA = 8 warps = 4 anchors of one (batch item, camera part), two warps
 // each: warp 2*q + h takes anchor 4*ci + q over the part's cameras and scale
-// half h (scales [0, ceil(S/2)) or [ceil(S/2), S)). The two halves have the
-// same number of samples, so they finish together, and a CTA's resident
+// half h (scales [0, ceil(S/2)) or [ceil(S/2), S)). For even S the two
+// halves have the same number of samples, so they finish together (for odd S
+// the first takes one scale more; at S = 1 the second has no samples and only
+// adds zeros); a CTA's resident
 // anchors (about 1,200 at 16 warps per SM) keep about one (batch item,
 // camera part) slice of the maps live in L2. Per round of 32 samples each
 // lane computes one sample's footprint into the warp's table (rows and corner

@@ -132,20 +132,62 @@ def binned_supported(C, G):
     return 8 <= C <= 256 and C & (C - 1) == 0 and D % 8 == 0
 
 
+def _softmax_over_samples(inp):
+    """Weights of each (anchor, group) made a softmax over its P*K*S samples,
+    as Sparse4D's weights are. With N(0,1) weights an output that is a sum of
+    hundreds of +-1 terms can cancel to near zero, where fp32 rounding of the
+    large terms exceeds the relative bound; softmax weights sum to 1."""
+    B, A, P, K, S, G = inp.weights.shape
+    inp.weights = inp.weights.reshape(B, A, P * K * S, G).softmax(dim=2).reshape(B, A, P, K, S, G).contiguous()
+    return inp
+
+
+def _takes_row_forward(inp) -> bool:
+    """The forward's choice of its warp-per-anchor kernel, restated: 256
+    channels in at most 8 groups, not a small-task problem (P*K*S <= 16
+    samples per (anchor, group) with rows of at most 512 bytes), and at least
+    8,192 (anchor, camera part) tasks, where a batch item's cameras split in
+    two parts when K is even and its maps hold 48 MB or more."""
+    B, rows, C = inp.feat.shape
+    _, A, P, K, S, G = inp.weights.shape
+    esz = inp.feat.element_size()
+    small = P * K * S <= 16 and C * esz <= 512
+    parts = 2 if K >= 2 and K % 2 == 0 and rows * C * esz >= 48 << 20 else 1
+    return C == 256 and G <= 8 and not small and B * A * parts >= 8192
+
+
 @pytest.mark.parametrize("split", [False, True])
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 def test_row_forward_every_feature_type(da, dtype, split):
     """The forward with a warp per anchor and all its groups serves 256
-    channels in at most 8 groups from 8,192 (anchor, camera part) tasks up.
-    Two cameras: with maps of 48 MB or more per batch item the cameras split
-    in two parts (4,096 anchors make 8,192 tasks), else one part (8,192
-    anchors)."""
+    channels in at most 8 groups from 8,192 (anchor, camera part) tasks up,
+    with more than 16 samples per (anchor, group) (fewer, with 16-bit
+    features, take the small-task kernel). Two cameras: with maps of 48 MB or
+    more per batch item the cameras split in two parts (4,096 anchors make
+    8,192 tasks; one scale, so the second scale-half warp has no samples),
+    else one part (8,192 anchors, two scales)."""
     if split:
         side = 160 if dtype == "f32" else 224  # 2 * side^2 rows of 256 channels >= 48 MB
-        shapes, A = [[(side, side)], [(side, side - 7)]], 4096
+        shapes, A, P = [[(side, side)], [(side, side - 7)]], 4096, 9
     else:
-        shapes, A = [[(16, 16), (8, 5)], [(9, 12), (4, 4)]], 8192
-    inp = _custom(300 + (1 if split else 0) + {"f32": 0, "bf16": 2, "f16": 4}[dtype], shapes, 1, 256, 8, A, 2, dtype)
+        shapes, A, P = [[(16, 16), (8, 5)], [(9, 12), (4, 4)]], 8192, 5
+    inp = _softmax_over_samples(_custom(300 + (1 if split else 0) + {"f32": 0, "bf16": 2, "f16": 4}[dtype],
+                                        shapes, 1, 256, 8, A, P, dtype))
+    assert _takes_row_forward(inp)
+    got = _run_gpu(da, inp, backward=False)
+    _compare(inp, got, oracle.run_inputs(inp, backward_pass=False))
+
+
+@pytest.mark.parametrize("dtype,groups,P", [("f32", 8, 2), ("bf16", 4, 3)])
+def test_row_forward_odd_scales_ragged_anchors(da, dtype, groups, P):
+    """The same forward with three scales per camera (the first scale-half
+    warp takes two, the second one), two batch items and an anchor count
+    that leaves the last CTA part-empty: 4,099 anchors per item make 8,198
+    tasks. With bf16 features 4 groups of 64 channels (128 bytes, the widest
+    group served), so a lane's group lane*G/32 spans 8 lanes."""
+    shapes = [[(13, 11), (6, 9), (3, 2)], [(10, 10), (5, 3), (1, 4)]]
+    inp = _softmax_over_samples(_custom(310 + groups, shapes, 2, 256, groups, 4099, P, dtype))
+    assert _takes_row_forward(inp)
     got = _run_gpu(da, inp, backward=False)
     _compare(inp, got, oracle.run_inputs(inp, backward_pass=False))
 
