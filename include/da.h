@@ -124,7 +124,7 @@ typedef struct da_dims {
  *   out               device [B, A, C] fp32, 16-byte aligned; overwritten.
  *
  * Supported: D * sizeof(feature) in {16, 32, 64, 128} bytes. That is D in
- * {4, 8, 16, 32} for fp32 and D in {8, 16, 32, 64} for bf16. Other D return
+ * {4, 8, 16, 32} for fp32 and D in {8, 16, 32, 64} for bf16 and fp16. Other D return
  * DA_ERR_UNSUPPORTED.
  * Arithmetic: h = y*H - 0.5 and w = x*W - 0.5 are each rounded twice (a
  * product, then a difference; no fused multiply-add). Corner weights and sums
