@@ -6,7 +6,8 @@ Each test pins the oracle to something independent of it:
   * linearity and adjoint identities;
   * brute-force Jacobians and finite differences on tiny inputs;
   * torch.nn.functional.grid_sample, which computes the same bilinear sample
-    when there is one camera and one scale.
+    for one map; with several cameras and scales the operator is a weighted
+    sum of grid_samples.
 Together they fail on a dropped corner, a wrong sign, a swapped x/y or H/W,
 a wrong level offset or a transposed operand.
 
@@ -348,6 +349,46 @@ def test_single_map_matches_grid_sample(B, H, W, C, G, A, P):
     np.testing.assert_allclose(gl.reshape(B, A, P, 2),
                                2.0 * grid.grad.view(B, A, P, 2).numpy(), rtol=1e-4, atol=1e-3)
     np.testing.assert_allclose(gw.reshape(B, A, P, G), wt.grad.numpy(), rtol=1e-5, atol=1e-5)
+
+
+@pytest.mark.parametrize("B,shapes,C,G,A,P", [
+    (2, [[(7, 9), (4, 5)], [(6, 11), (3, 2)], [(5, 5), (2, 7)]], 8, 2, 5, 3),
+    (1, [[(12, 10), (6, 5), (3, 3)], [(9, 14), (5, 7), (2, 4)]], 16, 4, 4, 2),
+])
+def test_many_maps_match_a_sum_of_grid_samples(B, shapes, C, G, A, P):
+    """With several cameras and scales, out is the sum over (p, k, s) of
+    w[b,a,p,k,s,g] times grid_sample of map (k, s) at camera k's location of
+    point p, the same location at every scale of the camera (page §5.1's sum
+    over the sampling dimensions). Every map has its own (H, W), so a
+    transposed camera/scale index or a location taken per scale fails. Each
+    map is a view of one packed float64 leaf, so autograd gives grad_feat in
+    the packed layout and grad_loc summed over the scales."""
+    rng = np.random.default_rng(21)
+    feat, ss, ls, loc, w, go = _rand_problem(rng, B, shapes, C, G, A, P)
+    K, S = ss.shape[:2]
+    D = C // G
+    out = oracle.forward(feat, ss, ls, loc, w)
+    gf, gl, gw = oracle.backward(feat, ss, ls, loc, w, go)
+
+    f = torch.tensor(feat, dtype=torch.float64, requires_grad=True)
+    lt = torch.tensor(loc, dtype=torch.float64, requires_grad=True)
+    wt = torch.tensor(w, dtype=torch.float64, requires_grad=True)
+    ref = torch.zeros(B, A, G, D, dtype=torch.float64)
+    for k in range(K):
+        grid = (2.0 * lt[:, :, :, k, :] - 1.0).reshape(B, A * P, 1, 2)
+        for s in range(S):
+            H, W, r0 = int(ss[k, s, 0]), int(ss[k, s, 1]), int(ls[k, s])
+            m = f[:, r0:r0 + H * W].reshape(B, H, W, C).permute(0, 3, 1, 2)
+            samp = torch.nn.functional.grid_sample(m, grid, mode="bilinear", padding_mode="zeros",
+                                                   align_corners=False)  # [B, C, A*P, 1]
+            samp = samp.view(B, G, D, A, P).permute(0, 3, 4, 1, 2)  # [B, A, P, G, D]
+            ref = ref + (wt[:, :, :, k, s, :, None] * samp).sum(2)
+    ref = ref.reshape(B, A, C)
+    ref.backward(torch.tensor(go, dtype=torch.float64))
+    np.testing.assert_allclose(out, ref.detach().numpy(), rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(gf, f.grad.numpy(), rtol=1e-5, atol=1e-5)
+    np.testing.assert_allclose(gl, lt.grad.numpy(), rtol=1e-4, atol=1e-3)
+    np.testing.assert_allclose(gw, wt.grad.numpy(), rtol=1e-5, atol=1e-5)
 
 
 # --------------------------------------------------------------------------- layout & edges
